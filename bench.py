@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark: one decode step of the Llama-3.1-8B GQA attention block.
+
+Workload (default): B = 16 sequences at P = 1000 cached positions, T = 1 —
+the decode point of "Llama 3.1 8B · Grouped-query attention" (1,001 keys
+read, row 1000 written). A step is one call of the whole path (Q|K|V
+projection with RoPE and cache append, split-K decode attention, output
+projection) over the batch. Metric: seq-steps/s = B / step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed steps, then exactly K steps bracketed by barrier +
+synchronize, CUDA events on the launching stream. L2 (129 MB) is defeated by
+rotating REPLICAS copies of weights + cache (each 150 MB) so every step
+streams its bytes from HBM. Under torchrun (N > 1) every rank runs its own
+replica of the step on its own GPU (no collective: batch rows are
+independent); value = all ranks' sequences / max elapsed.
+
+--impl reference times the CPU oracle (the plain fp64 definition of the
+block) on rank 0: each step is one sequence of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+if "OMP_NUM_THREADS" not in os.environ:
+    os.environ["OPENBLAS_NUM_THREADS"] = os.environ.get("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import gqa_inputs as I  # noqa: E402
+
+METRIC = "GQA block decode seq-steps/s & HBM GB/s vs peak; prefill TFLOP/s vs peak"
+WEIGHT_BYTES = 2 * (4096 * 4096 * 2 + 1024 * 4096 * 2)   # 83,886,080
+KERNELS = ("qkv_projection", "decode_attention", "o_projection")
+
+
+def args_():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_b16_p1000")
+    ap.add_argument("--replicas", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def step_bytes(B: int, starts) -> dict:
+    """Algorithmic HBM bytes of one decode step, per kernel (see the design notes)."""
+    kv_read = sum((int(p) + 1) * 4096 for p in starts)
+    return {
+        "qkv_projection": 50331648 + B * 8192 + B * 8192 + B * 4096,   # Wq|Wk|Wv, x, rotated q, new K/V rows
+        "decode_attention": kv_read + B * 8192 + B * 8192,           # cache rows 0..P, q, o
+        "o_projection": 33554432 + B * 8192 + B * 8192,              # Wo, o, delta
+        "step": WEIGHT_BYTES + kv_read + B * 4096 + 2 * B * 8192,    # the roofline's byte count
+    }
+
+
+def step_flops(B: int, T: int, start: int) -> dict:
+    """Algorithmic FLOPs of one prefill call: projections 2*41,943,040 per
+    token, attention 16,384 per visible (query, key) pair (causal half only)."""
+    pairs = B * sum(start + t + 1 for t in range(T))
+    return {
+        "qkv_projection": 2.0 * B * T * 4096 * 6144,
+        "prefill_attention": 16384.0 * pairs,
+        "o_projection": 2.0 * B * T * 4096 * 4096,
+        "step": 2.0 * 41943040 * B * T + 16384.0 * pairs,
+    }
+
+
+def load_peaks():
+    """(hbm GB/s, bf16 TFLOP/s burst, kind)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_traffic(name: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get(name)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "grouped_query_attention_gemv_gb300", "csrc", ent["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] if os.path.exists(src) else None
+    return ent["bytes_per_launch"] if h == ent.get("source_sha256_16") else None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 50 ms) while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        self.idx = gpu_index
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [r for t, r in self.rows if self.t0 and self.t1 and self.t0 <= t <= self.t1]
+        use = inside or [r for _, r in self.rows]
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in use:
+            f = [x.strip() for x in r.split(",")]
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+def cpu_baseline(w: I.Workload, budget_s: float = 12.0):
+    """The oracle, as it stands, on a bounded sample: whole sequences of the
+    workload (projections, attention, output) until the budget is spent."""
+    from oracle import gqa as O
+    gen, wt = I.draw_weights(seed=w.seed)
+    x = I.draw_x(gen, w.B, w.T)
+    starts = w.start_positions().tolist()
+    ck, cv = I.draw_cache(w.B, w.cache_rows(), starts, seed=w.seed, device="cpu")
+    W = {k: v.to(torch.float64).numpy() for k, v in wt.items()}
+    r = I.LLAMA31_ROPE
+    freqs = O.rope_frequencies(128, r.theta, r.scaled, r.factor, r.low_freq_factor, r.high_freq_factor,
+                               r.original_context)
+    per = []
+    for b in range(w.B):
+        per.append((x[b].to(torch.float64).numpy(), ck[b, :starts[b]].to(torch.float64).numpy(),
+                    cv[b, :starts[b]].to(torch.float64).numpy(), starts[b]))
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        xb, kb, vb, sp = per[n % w.B]
+        O.sequence_forward(xb, W["wq"], W["wk"], W["wv"], W["wo"], sp, kb, vb, freqs, 32, 8)
+        n += 1
+        el = time.perf_counter() - t0
+        if el > budget_s or n >= 64 * w.B:
+            break
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
+    return {"value": n / el, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} single-sequence decode steps of {w.name} (whole sequences: projections, "
+                      f"attention over P+1 keys, output projection), {el:.1f} s, numpy float64"}
+
+
+def run_reference(a, w: I.Workload, rank: int, world: int):
+    if rank != 0:
+        return
+    from oracle import gqa as O
+    gen, wt = I.draw_weights(seed=w.seed)
+    x = I.draw_x(gen, w.B, w.T)
+    starts = w.start_positions().tolist()
+    ck, cv = I.draw_cache(w.B, w.cache_rows(), starts, seed=w.seed, device="cpu")
+    W = {k: v.to(torch.float64).numpy() for k, v in wt.items()}
+    r = I.LLAMA31_ROPE
+    freqs = O.rope_frequencies(128, r.theta, r.scaled, r.factor, r.low_freq_factor, r.high_freq_factor,
+                               r.original_context)
+    per = [(x[b].to(torch.float64).numpy(), ck[b, :starts[b]].to(torch.float64).numpy(),
+            cv[b, :starts[b]].to(torch.float64).numpy(), starts[b]) for b in range(w.B)]
+
+    def step(i):
+        xb, kb, vb, sp = per[i % w.B]
+        O.sequence_forward(xb, W["wq"], W["wk"], W["wv"], W["wo"], sp, kb, vb, freqs, 32, 8)
+
+    for i in range(a.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(a.steps):
+        step(i)
+    el = time.perf_counter() - t0
+    val = a.steps / el
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "seq-steps/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * el / a.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, a, starts), "e2e": {"value": val, "unit": "seq-steps/s", "h2d_bytes_per_step": 0,
+                                             "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": val, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: one sequence of {w.name} through the CPU oracle "
+                                   "(numpy float64, whole sequence)"},
+    }))
+
+
+def config_dict(w: I.Workload, a, starts):
+    c = {"workload": w.name, "B": w.B, "T": w.T, "s_max": w.cache_rows(), "d_model": 4096, "n_heads": 32,
+         "n_kv_heads": 8, "head_dim": 128,
+         "l2": f"inputs larger than L2: {a.replicas} rotating replicas of weights+cache+x, one per step",
+         "parallelism": "replicas"}
+    if w.start_pos is not None:
+        c["start_pos"] = w.start_pos
+    else:
+        c["start_pos_range"] = list(w.p_range)
+        c["sum_keys"] = int(sum(int(p) + 1 for p in starts))
+    return c
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v, world, dev):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    a = args_()
+    rank, world, local = dist_env()
+    w = I.workload(a.workload)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo" if a.impl == "reference" else "nccl")
+    if a.impl == "reference":
+        run_reference(a, w, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import grouped_query_attention_gemv_gb300 as G
+    from grouped_query_attention_gemv_gb300 import build
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    decode = w.T == 1
+    kernels = KERNELS if decode else ("qkv_projection", "prefill_attention", "o_projection")
+
+    starts = w.start_positions().tolist()
+    s_max = w.cache_rows()
+    gen, wt = I.draw_weights(seed=w.seed)
+    x0 = I.draw_x(gen, w.B, w.T)
+    ck0, cv0 = I.draw_cache(w.B, s_max, starts, seed=w.seed)
+    R = max(1, a.replicas)
+    max_start = max(starts)
+    reps = []
+    for _ in range(R):
+        reps.append({**{k: v.to(dev) for k, v in wt.items()}, "x": x0.to(dev), "ck": ck0.to(dev), "cv": cv0.to(dev),
+                     "out": torch.empty_like(x0, device=dev),
+                     "ws": G.make_workspace(w.B, w.T, max_start + w.T, dev)})
+    sp = torch.tensor(starts, dtype=torch.int32, device=dev)
+    rope = G.rope_table(s_max, device=dev)
+
+    def step(i):
+        # stream=None: the current stream (the capture stream while a graph is recorded)
+        r = reps[i % R]
+        if decode:
+            G.decode(r["x"], sp, max_start, r["wq"], r["wk"], r["wv"], r["wo"], rope, r["ck"], r["cv"],
+                     out=r["out"], workspace=r["ws"])
+        else:
+            G.prefill(r["x"], starts[0], r["wq"], r["wk"], r["wv"], r["wo"], rope, r["ck"], r["cv"],
+                      out=r["out"], workspace=r["ws"])
+
+    for i in range(max(a.warmup, R)):
+        step(i)
+    torch.cuda.synchronize()
+    per_step_launches = G.last_launch_count()
+    for r in reps:
+        assert G.device_status(r["ws"]) == 0, "device status set during warm-up"
+
+    # one graph per replica holding that replica's step: the timed loop replays
+    # them, so the device never waits for the host
+    graphs = []
+    for r_i in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(r_i)
+        graphs.append(g)
+    for i in range(R):
+        graphs[i].replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region (device)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    _barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark("t0")
+    e0.record(stream)
+    for i in range(a.steps):
+        graphs[i % R].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    _barrier(world)
+    time.sleep(0.1)
+    clocks.stop()
+    ms = _max_over_ranks(e0.elapsed_time(e1), world, dev)
+    ms_step = ms / a.steps
+    launches = per_step_launches * a.steps
+    for r in reps:
+        assert G.device_status(r["ws"]) == 0, "device status set during the timed steps"
+
+    # ---- per-kernel attribution: events recorded by the library around each
+    # kernel, with a device-side backlog so host gaps do not enter the intervals
+    ksteps = min(a.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(ksteps)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(3e8))
+    for i in range(ksteps):
+        G.set_profile_events(evs[i])
+        step(i)
+    G.set_profile_events(None)
+    torch.cuda.synchronize()
+    per_kernel = {k: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs) for j, k in enumerate(kernels)}
+
+    # ---- end to end through the public API with host buffers: pinned x in,
+    # delta out, copies inside the timed region
+    xh = x0.pin_memory()
+    oh = torch.empty_like(x0).pin_memory()
+    for i in range(min(a.warmup, 5)):
+        reps[i % R]["x"].copy_(xh, non_blocking=True)
+        step(i)
+        oh.copy_(reps[i % R]["out"], non_blocking=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for i in range(a.steps):
+        r = reps[i % R]
+        r["x"].copy_(xh, non_blocking=True)
+        step(i)
+        oh.copy_(r["out"], non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    ems = _max_over_ranks(f0.elapsed_time(f1), world, dev)
+    for r in reps:
+        assert G.device_status(r["ws"]) == 0, "device status set during the end-to-end steps"
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    hbm, tflops, peak_kind = load_peaks()
+    dom = max(per_kernel, key=per_kernel.get)
+    if decode:
+        work = step_bytes(w.B, starts)
+        value = world * w.B * a.steps / (ms / 1e3)
+        unit = "seq-steps/s"
+        e2e_value = world * w.B * a.steps / (ems / 1e3)
+        achieved = work[dom] / (per_kernel[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": kernel_traffic(dom), "algorithmic_bytes_per_launch": work[dom],
+                "launch_ms": per_kernel[dom], "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}
+        step_rate = {"step_hbm_gbs": work["step"] / (ms_step / 1e3) / 1e9}
+        step_rate["step_hbm_frac"] = step_rate["step_hbm_gbs"] / hbm
+    else:
+        work = step_flops(w.B, w.T, starts[0])
+        value = world * work["step"] * a.steps / (ms / 1e3) / 1e12
+        unit = "TFLOP/s"
+        e2e_value = world * work["step"] * a.steps / (ems / 1e3) / 1e12
+        achieved = work[dom] / (per_kernel[dom] / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+                "frac": achieved / tflops, "traffic": kernel_traffic(dom), "algorithmic_flops_per_launch": work[dom],
+                "launch_ms": per_kernel[dom], "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({peak_kind})"}
+        step_rate = {"step_tflops": work["step"] / (ms_step / 1e3) / 1e12}
+        step_rate["step_tensor_frac"] = step_rate["step_tflops"] / tflops
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) x and cache, N(0,1/4096) weights)",
+        "config": config_dict(w, a, starts), **step_rate, "peak_kind": peak_kind,
+        "roofline": roof,
+        "kernels_ms": per_kernel,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": x0.numel() * 2,
+                "d2h_bytes_per_step": x0.numel() * 2},
+        "gpu_launches": launches,
+        "timing": "device region replays one CUDA graph per replica (the same C-ABI call captured); "
+                  "e2e calls the Python API per step",
+        "clocks": clocks.summary(),
+    }
+    if not a.no_cpu_baseline and world == 1 and decode:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

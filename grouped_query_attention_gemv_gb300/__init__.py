@@ -1,0 +1,228 @@
+"""GB300 grouped-query attention block (Llama 3.1 8B) — Python binding.
+
+A thin ctypes layer over the C ABI in ``include/gqa.h`` (``lib/libgqa.so``,
+built in-tree by ``python -m grouped_query_attention_gemv_gb300.build``).
+It only checks and marshals arguments: every step of the block runs in the
+library's CUDA kernels. PyTorch supplies device memory and streams.
+
+Functions mirror the C entry points: ``block_forward``, ``decode``,
+``prefill``, ``rope_table``, ``workspace_bytes``, ``device_status``,
+``last_launch_count``. If the library has not been built every call raises
+``ImportError``; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "GQAError", "D_MODEL", "N_HEADS", "N_KV_HEADS", "HEAD_DIM", "library_path", "lib",
+    "exported_symbols", "workspace_bytes", "make_workspace", "rope_table", "block_forward",
+    "decode", "prefill", "device_status", "last_launch_count", "set_profile_events",
+]
+
+D_MODEL, N_HEADS, N_KV_HEADS, HEAD_DIM = 4096, 32, 8, 128
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "lib", "libgqa.so")
+_HEADER = os.path.join(os.path.dirname(_PKG), "include", "gqa.h")
+
+_vp, _i, _sz, _d = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_double
+_SIGNATURES = {
+    "gqa_workspace_bytes": (_sz, [_i, _i, _i]),
+    "gqa_workspace_init": (_i, [_vp, _sz, _vp]),
+    "gqa_device_status": (_i, [_vp, ctypes.POINTER(_i), _i]),
+    "gqa_rope_table": (_i, [_vp, _i, _d, _i, _d, _d, _d, _d, _vp]),
+    "gqa_block_forward": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
+    "gqa_prefill": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
+    "gqa_decode": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
+    "gqa_strerror": (ctypes.c_char_p, [_i]),
+    "gqa_last_launch_count": (_i, []),
+    "gqa_set_profile_events": (_i, [ctypes.POINTER(_vp), _i]),
+}
+
+
+class GQAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = lib().gqa_strerror(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgqa; raises ImportError when it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(f"libgqa.so is not built ({_LIB_PATH}); run "
+                              "`python -m grouped_query_attention_gemv_gb300.build`")
+        handle = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def exported_symbols():
+    """Names of the functions declared in include/gqa.h."""
+    text = open(_HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(gqa_\w+)\s*\(", text, re.M)))
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def workspace_bytes(B: int, T: int, max_keys: int) -> int:
+    return int(lib().gqa_workspace_bytes(B, T, max_keys))
+
+
+def make_workspace(B: int, T: int, max_keys: int, device=None) -> torch.Tensor:
+    """A zero-filled uint8 workspace sized for (B, T, max_keys)."""
+    n = workspace_bytes(B, T, max_keys)
+    if n == 0:
+        raise ValueError(f"invalid workspace request B={B} T={T} max_keys={max_keys}")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def rope_table(rows: int, theta: float = 500000.0, scaled: bool = True, factor: float = 8.0,
+               low_freq_factor: float = 1.0, high_freq_factor: float = 4.0,
+               original_context: float = 8192.0, device=None, stream=None) -> torch.Tensor:
+    """fp32 [rows, 64, 2] table of (cos, sin), built on the device."""
+    out = torch.empty(rows, 64, 2, dtype=torch.float32, device=device or "cuda")
+    r = lib().gqa_rope_table(_p(out), rows, theta, int(scaled), factor, low_freq_factor,
+                             high_freq_factor, original_context, _s(stream))
+    if r:
+        raise GQAError(r, "gqa_rope_table")
+    return out
+
+
+def _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, T):
+    B = x.shape[0]
+    _check(x, "x", torch.bfloat16, (B, T, D_MODEL))
+    _check(wq, "wq", torch.bfloat16, (N_HEADS * HEAD_DIM, D_MODEL))
+    _check(wk, "wk", torch.bfloat16, (N_KV_HEADS * HEAD_DIM, D_MODEL))
+    _check(wv, "wv", torch.bfloat16, (N_KV_HEADS * HEAD_DIM, D_MODEL))
+    _check(wo, "wo", torch.bfloat16, (D_MODEL, N_HEADS * HEAD_DIM))
+    _check(rope, "rope", torch.float32)
+    if rope.dim() != 3 or rope.shape[1:] != (64, 2):
+        raise ValueError("rope must be [rows, 64, 2]")
+    _check(cache_k, "cache_k", torch.bfloat16)
+    _check(cache_v, "cache_v", torch.bfloat16, cache_k.shape)
+    if cache_k.dim() != 4 or cache_k.shape[0] != B or cache_k.shape[2:] != (N_KV_HEADS, HEAD_DIM):
+        raise ValueError(f"cache must be [B, S_max, 8, 128], got {tuple(cache_k.shape)}")
+    if out is None:
+        out = torch.empty_like(x)
+    _check(out, "out", torch.bfloat16, (B, T, D_MODEL))
+    return B, out
+
+
+def _ws(workspace, B, T, max_keys, device):
+    if workspace is None:
+        workspace = make_workspace(B, T, max_keys, device)
+    _check(workspace, "workspace", torch.uint8)
+    return workspace
+
+
+def block_forward(x, start_pos: int, wq, wk, wv, wo, rope, cache_k, cache_v, out=None,
+                  workspace=None, stream=None) -> torch.Tensor:
+    """delta_attn for x [B, T, 4096] after ``start_pos`` cached rows; updates the cache."""
+    T = x.shape[1]
+    B, out = _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, T)
+    workspace = _ws(workspace, B, T, start_pos + T, x.device)
+    r = lib().gqa_block_forward(_p(x), B, T, int(start_pos), _p(wq), _p(wk), _p(wv), _p(wo), _p(rope),
+                                rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
+                                _p(workspace), workspace.numel(), _s(stream))
+    if r:
+        raise GQAError(r, "gqa_block_forward")
+    return out
+
+
+def prefill(x, start_pos: int, wq, wk, wv, wo, rope, cache_k, cache_v, out=None, workspace=None,
+            stream=None) -> torch.Tensor:
+    T = x.shape[1]
+    B, out = _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, T)
+    workspace = _ws(workspace, B, T, start_pos + T, x.device)
+    r = lib().gqa_prefill(_p(x), B, T, int(start_pos), _p(wq), _p(wk), _p(wv), _p(wo), _p(rope),
+                          rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
+                          _p(workspace), workspace.numel(), _s(stream))
+    if r:
+        raise GQAError(r, "gqa_prefill")
+    return out
+
+
+def decode(x, start_pos: torch.Tensor, max_start_pos: int, wq, wk, wv, wo, rope, cache_k, cache_v,
+           out=None, workspace=None, stream=None) -> torch.Tensor:
+    """One decode step; ``start_pos`` is a device int32 [B] of cached rows per sequence."""
+    B, out = _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, 1)
+    _check(start_pos, "start_pos", torch.int32, (B,))
+    workspace = _ws(workspace, B, 1, max_start_pos + 1, x.device)
+    r = lib().gqa_decode(_p(x), B, _p(start_pos), int(max_start_pos), _p(wq), _p(wk), _p(wv), _p(wo),
+                         _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
+                         _p(workspace), workspace.numel(), _s(stream))
+    if r:
+        raise GQAError(r, "gqa_decode")
+    return out
+
+
+def device_status(workspace: torch.Tensor, clear: bool = False) -> int:
+    """Synchronise and return the workspace status word (0 = no device error)."""
+    st = ctypes.c_int(0)
+    r = lib().gqa_device_status(_p(workspace), ctypes.byref(st), int(clear))
+    if r not in (0, -5):
+        raise GQAError(r, "gqa_device_status")
+    return st.value
+
+
+def last_launch_count() -> int:
+    return int(lib().gqa_last_launch_count())
+
+
+_prof_keep = None
+
+
+def set_profile_events(events) -> None:
+    """Record ``events[0]`` before and ``events[i]`` after kernel i of every
+    following call on this thread (torch.cuda.Event objects with timing);
+    ``None`` stops it."""
+    global _prof_keep
+    if not events:
+        _prof_keep = None
+        lib().gqa_set_profile_events(None, 0)
+        return
+    arr = (_vp * len(events))(*[e.cuda_event for e in events])
+    _prof_keep = (arr, events)
+    r = lib().gqa_set_profile_events(arr, len(events))
+    if r:
+        raise GQAError(r, "gqa_set_profile_events")

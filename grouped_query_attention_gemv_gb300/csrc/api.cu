@@ -1,0 +1,386 @@
+// C ABI of libgqa (declared in include/gqa.h): argument validation on the
+// host, workspace layout, TMA descriptor encoding and the launch sequence of
+// one block call on the caller's stream. Nothing here allocates or waits.
+#include <stdio.h>
+#include <string.h>
+
+#include "gqa.h"
+#include "kernels.h"
+
+using namespace gqa;
+
+namespace {
+
+thread_local cudaError_t t_last_cuda = cudaSuccess;
+thread_local int t_launches = 0;
+thread_local char t_msg[256];
+thread_local void* const* t_prof_events = nullptr;
+thread_local int t_prof_count = 0;
+
+void prof_mark(int i, cudaStream_t s) {
+  if (t_prof_events && i < t_prof_count && t_prof_events[i])
+    cudaEventRecord(static_cast<cudaEvent_t>(t_prof_events[i]), s);
+}
+
+// Workspace regions, each 256-byte aligned. The status word is always first.
+struct Layout {
+  size_t status = 0, q = 0, o = 0, acc = 0, tickets = 0, part_o = 0, part_ml = 0, att_tickets = 0;
+  size_t total = 0;
+  int mp = 0, chunk = 0, nsplit = 0;
+};
+
+// SM count the split-K sizing assumes (GB300); kernels still run on any count.
+constexpr int REF_SMS = 152;
+
+bool make_layout(int B, int T, int max_keys, Layout* L) {
+  if (B <= 0 || T <= 0 || max_keys < T) return false;
+  const long long M = static_cast<long long>(B) * T;
+  if (M > (1LL << 24)) return false;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t r = off;
+    off += (bytes + 255) & ~static_cast<size_t>(255);
+    return r;
+  };
+  L->status = take(256);
+  L->q = take(static_cast<size_t>(M) * D_MODEL * 2);
+  L->o = take(static_cast<size_t>(M) * D_MODEL * 2);
+  L->mp = gemv_padded_m(static_cast<int>(M));
+  if (L->mp) {
+    L->acc = take(static_cast<size_t>(QKV_ROWS) * L->mp * 4);
+    L->tickets = take(static_cast<size_t>(QKV_ROWS / 16) * 4);
+  }
+  if (T == 1) {
+    L->chunk = decode_chunk(B, max_keys, REF_SMS);
+    L->nsplit = (max_keys + L->chunk - 1) / L->chunk;
+    const size_t n = static_cast<size_t>(B) * N_KV * L->nsplit * N_REP;
+    L->part_o = take(n * HEAD_DIM * 4);
+    L->part_ml = take(n * 2 * 4);
+    L->att_tickets = take(static_cast<size_t>(B) * N_KV * 4);
+  }
+  L->total = off;
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int fail_cuda(cudaError_t e) {
+  t_last_cuda = e;
+  return GQA_ECUDA;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 [outer, 4096] row-major, boxes of box_rows x 64 (128B swizzle).
+bool map_rows(CUtensorMap* m, const void* ptr, long long rows, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D_MODEL), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D_MODEL) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// KV cache [B, s_max, 8, 128] bf16 as a 4-D tensor (d, g, pos, b); boxes of
+// 64 dims x 1 head x 64 positions. Positions past s_max read as zero.
+bool map_cache(CUtensorMap* m, const void* ptr, int B, int s_max) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {HEAD_DIM, N_KV, static_cast<cuuint64_t>(s_max), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {HEAD_DIM * 2, KV_ROW * 2, static_cast<cuuint64_t>(s_max) * KV_ROW * 2};
+  const cuuint32_t box[4] = {64, 1, 64, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return REF_SMS;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = REF_SMS;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+struct Call {
+  const gqa_bf16* x;
+  int B, T;
+  StartPos sp;
+  int max_keys;
+  const gqa_bf16 *wq, *wk, *wv, *wo;
+  const float* rope;
+  gqa_bf16 *cache_k, *cache_v;
+  int s_max;
+  gqa_bf16* out;
+  uint8_t* ws;
+  cudaStream_t stream;
+  Layout L;
+};
+
+int check_common(const gqa_bf16* x, int B, int T, const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv,
+                 const gqa_bf16* wo, const float* rope, int rope_rows, const gqa_bf16* ck, const gqa_bf16* cv,
+                 int s_max, const gqa_bf16* out, const void* ws, int max_keys, size_t ws_bytes, Layout* L) {
+  if (!x || !wq || !wk || !wv || !wo || !rope || !ck || !cv || !out || !ws) return GQA_EINVAL;
+  if (B <= 0 || T <= 0 || s_max <= 0 || rope_rows <= 0) return GQA_EINVAL;
+  if (max_keys > s_max || max_keys > rope_rows) return GQA_EINVAL;
+  if (!aligned16(x) || !aligned16(wq) || !aligned16(wk) || !aligned16(wv) || !aligned16(wo) ||
+      !aligned16(rope) || !aligned16(ck) || !aligned16(cv) || !aligned16(out) || !aligned16(ws))
+    return GQA_EALIGN;
+  if (!make_layout(B, T, max_keys, L)) return GQA_EINVAL;
+  if (ws_bytes < L->total) return GQA_EWORKSPACE;
+  return GQA_OK;
+}
+
+ProjParams proj_params(const Call& c, bool qkv) {
+  ProjParams p{};
+  p.M = c.B * c.T;
+  p.T = c.T;
+  if (qkv) {
+    p.x = reinterpret_cast<const __nv_bfloat16*>(c.x);
+    p.w0 = reinterpret_cast<const __nv_bfloat16*>(c.wq);
+    p.w1 = reinterpret_cast<const __nv_bfloat16*>(c.wk);
+    p.w2 = reinterpret_cast<const __nv_bfloat16*>(c.wv);
+    p.r1 = D_MODEL;
+    p.r2 = D_MODEL + KV_ROW;
+    p.N = QKV_ROWS;
+    p.qkv = 1;
+    p.out = reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.q);
+  } else {
+    p.x = reinterpret_cast<const __nv_bfloat16*>(c.ws + c.L.o);
+    p.w0 = p.w1 = p.w2 = reinterpret_cast<const __nv_bfloat16*>(c.wo);
+    p.r1 = p.r2 = p.N = D_MODEL;
+    p.qkv = 0;
+    p.out = reinterpret_cast<__nv_bfloat16*>(c.out);
+  }
+  p.cache_k = reinterpret_cast<__nv_bfloat16*>(c.cache_k);
+  p.cache_v = reinterpret_cast<__nv_bfloat16*>(c.cache_v);
+  p.s_max = c.s_max;
+  p.rope = c.rope;
+  p.sp = c.sp;
+  p.status = reinterpret_cast<int*>(c.ws + c.L.status);
+  return p;
+}
+
+int run_projection(const Call& c, bool qkv) {
+  const ProjParams p = proj_params(c, qkv);
+  cudaError_t e;
+  if (c.L.mp) {
+    e = launch_gemv(p, reinterpret_cast<float*>(c.ws + c.L.acc), reinterpret_cast<int*>(c.ws + c.L.tickets),
+                    sm_count(), c.stream);
+  } else {
+    GemmMaps maps;
+    if (!map_rows(&maps.a, p.x, p.M, GEMM_BM)) return fail_cuda(cudaErrorInvalidValue);
+    if (qkv) {
+      if (!map_rows(&maps.b[0], c.wq, D_MODEL, GEMM_BN) || !map_rows(&maps.b[1], c.wk, KV_ROW, GEMM_BN) ||
+          !map_rows(&maps.b[2], c.wv, KV_ROW, GEMM_BN))
+        return fail_cuda(cudaErrorInvalidValue);
+    } else {
+      if (!map_rows(&maps.b[0], c.wo, D_MODEL, GEMM_BN)) return fail_cuda(cudaErrorInvalidValue);
+      maps.b[1] = maps.b[0];
+      maps.b[2] = maps.b[0];
+    }
+    e = launch_gemm_tc(maps, p, c.stream);
+  }
+  if (e != cudaSuccess) return fail_cuda(e);
+  ++t_launches;
+  return GQA_OK;
+}
+
+int run_attention(const Call& c) {
+  CUtensorMap mk, mv;
+  if (!map_cache(&mk, c.cache_k, c.B, c.s_max) || !map_cache(&mv, c.cache_v, c.B, c.s_max))
+    return fail_cuda(cudaErrorInvalidValue);
+  cudaError_t e;
+  if (c.T == 1) {
+    DecodeAttnParams a{};
+    a.q = reinterpret_cast<const __nv_bfloat16*>(c.ws + c.L.q);
+    a.B = c.B;
+    a.sp = c.sp;
+    a.chunk = c.L.chunk;
+    a.nsplit = c.L.nsplit;
+    a.part_o = reinterpret_cast<float*>(c.ws + c.L.part_o);
+    a.part_ml = reinterpret_cast<float*>(c.ws + c.L.part_ml);
+    a.tickets = reinterpret_cast<int*>(c.ws + c.L.att_tickets);
+    a.o = reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.o);
+    a.status = reinterpret_cast<int*>(c.ws + c.L.status);
+    e = launch_attn_decode(mk, mv, a, c.stream);
+  } else {
+    PrefillAttnParams a{};
+    a.q = reinterpret_cast<const __nv_bfloat16*>(c.ws + c.L.q);
+    a.B = c.B;
+    a.T = c.T;
+    a.sp = c.sp;
+    a.o = reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.o);
+    a.status = reinterpret_cast<int*>(c.ws + c.L.status);
+    e = launch_attn_prefill(mk, mv, a, c.stream);
+  }
+  if (e != cudaSuccess) return fail_cuda(e);
+  ++t_launches;
+  return GQA_OK;
+}
+
+int run_block(Call& c) {
+  t_launches = 0;
+  prof_mark(0, c.stream);
+  int r = run_projection(c, true);
+  prof_mark(1, c.stream);
+  if (r == GQA_OK) r = run_attention(c);
+  prof_mark(2, c.stream);
+  if (r == GQA_OK) r = run_projection(c, false);
+  prof_mark(3, c.stream);
+  return r;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gqa_workspace_bytes(int B, int T, int max_keys) {
+  Layout L;
+  return make_layout(B, T, max_keys, &L) ? L.total : 0;
+}
+
+int gqa_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes == 0) return GQA_EINVAL;
+  if (!aligned16(workspace)) return GQA_EALIGN;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GQA_OK : fail_cuda(e);
+}
+
+int gqa_device_status(void* workspace, int* status, int clear) {
+  if (!workspace || !status) return GQA_EINVAL;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(status, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(workspace, 0, sizeof(int));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return *status ? GQA_EDEVICE : GQA_OK;
+}
+
+int gqa_rope_table(float* rope, int rows, double theta, int scaled, double factor, double low_freq_factor,
+                   double high_freq_factor, double original_context, void* stream) {
+  if (!rope || rows <= 0 || !(theta > 1.0)) return GQA_EINVAL;
+  if (scaled && !(factor > 0.0 && high_freq_factor > low_freq_factor && low_freq_factor > 0.0 &&
+                  original_context > 0.0))
+    return GQA_EINVAL;
+  if (!aligned16(rope)) return GQA_EALIGN;
+  t_launches = 0;
+  cudaError_t e = launch_rope_table(rope, rows, theta, scaled, factor, low_freq_factor, high_freq_factor,
+                                    original_context, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  t_launches = 1;
+  return GQA_OK;
+}
+
+int gqa_block_forward(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* wq, const gqa_bf16* wk,
+                      const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
+                      gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  if (start_pos < 0 || T <= 0 || start_pos > (1 << 30)) return GQA_EINVAL;
+  Call c{};
+  const int max_keys = start_pos + T;
+  int r = check_common(x, B, T, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, out, workspace, max_keys,
+                       workspace_bytes, &c.L);
+  if (r != GQA_OK) return r;
+  c.x = x;
+  c.B = B;
+  c.T = T;
+  c.sp = StartPos{nullptr, start_pos, start_pos};
+  c.max_keys = max_keys;
+  c.wq = wq;
+  c.wk = wk;
+  c.wv = wv;
+  c.wo = wo;
+  c.rope = rope;
+  c.cache_k = cache_k;
+  c.cache_v = cache_v;
+  c.s_max = s_max;
+  c.out = out;
+  c.ws = static_cast<uint8_t*>(workspace);
+  c.stream = static_cast<cudaStream_t>(stream);
+  return run_block(c);
+}
+
+int gqa_prefill(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* wq, const gqa_bf16* wk,
+                const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
+                gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return gqa_block_forward(x, B, T, start_pos, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, out,
+                           workspace, workspace_bytes, stream);
+}
+
+int gqa_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos, const gqa_bf16* wq,
+               const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows,
+               gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  if (!start_pos || max_start_pos < 0 || max_start_pos > (1 << 30)) return GQA_EINVAL;
+  Call c{};
+  const int max_keys = max_start_pos + 1;
+  int r = check_common(x, B, 1, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, out, workspace, max_keys,
+                       workspace_bytes, &c.L);
+  if (r != GQA_OK) return r;
+  if ((reinterpret_cast<uintptr_t>(start_pos) & 3u) != 0) return GQA_EALIGN;
+  c.x = x;
+  c.B = B;
+  c.T = 1;
+  c.sp = StartPos{start_pos, 0, max_start_pos};
+  c.max_keys = max_keys;
+  c.wq = wq;
+  c.wk = wk;
+  c.wv = wv;
+  c.wo = wo;
+  c.rope = rope;
+  c.cache_k = cache_k;
+  c.cache_v = cache_v;
+  c.s_max = s_max;
+  c.out = out;
+  c.ws = static_cast<uint8_t*>(workspace);
+  c.stream = static_cast<cudaStream_t>(stream);
+  return run_block(c);
+}
+
+const char* gqa_strerror(int status) {
+  switch (status) {
+    case GQA_OK: return "success";
+    case GQA_EINVAL: return "invalid argument (null pointer, non-positive size, or position beyond cache/table)";
+    case GQA_EALIGN: return "pointer not 16-byte aligned";
+    case GQA_EWORKSPACE: return "workspace smaller than gqa_workspace_bytes()";
+    case GQA_EDEVICE: return "a kernel recorded an error in the workspace status word";
+    case GQA_ECUDA:
+      snprintf(t_msg, sizeof(t_msg), "CUDA error: %s", cudaGetErrorName(t_last_cuda));
+      return t_msg;
+    default: return "unknown status";
+  }
+}
+
+int gqa_last_launch_count(void) { return t_launches; }
+
+int gqa_set_profile_events(void* const* events, int count) {
+  if (count < 0) return GQA_EINVAL;
+  t_prof_events = count > 0 ? events : nullptr;
+  t_prof_count = events ? count : 0;
+  return GQA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,151 @@
+// Internal interface between the C ABI (api.cu) and the kernel translation
+// units. Not installed; the public contract is include/gqa.h.
+#pragma once
+
+#include "common.cuh"
+
+namespace gqa {
+
+// One projection y = x W^T over M tokens (rows of x, stride 4096) and N
+// output features. The weight is up to three [rows, 4096] matrices stacked
+// along the output axis: rows [0, r1) from w0, [r1, r2) from w1, [r2, N) from
+// w2 (the fused Q|K|V projection uses wq, wk, wv with r1 = 4096, r2 = 5120).
+struct ProjParams {
+  const __nv_bfloat16* x;
+  int M;   // tokens
+  int T;   // tokens per sequence: token m is (b = m / T, t = m % T)
+  const __nv_bfloat16* w0;
+  const __nv_bfloat16* w1;
+  const __nv_bfloat16* w2;
+  int r1, r2, N;
+  int qkv;  // 0: plain store out[m][n]; 1: Q|K|V epilogue (RoPE, cache append)
+  __nv_bfloat16* out;  // plain: [M][N]; Q|K|V: rotated queries [M][4096]
+  __nv_bfloat16* cache_k;
+  __nv_bfloat16* cache_v;
+  int s_max;
+  const float* rope;  // [rope_rows][64][2] (cos, sin)
+  StartPos sp;
+  int* status;
+};
+
+// Rotate pair (a, b) of feature f (even) by the table row `pos`.
+__device__ __forceinline__ void rope_pair(const float* rope, int pos, int f, float& a, float& b) {
+  const float2 cs = *reinterpret_cast<const float2*>(rope + (static_cast<size_t>(pos) * ROPE_PAIRS +
+                                                             ((f & (HEAD_DIM - 1)) >> 1)) * 2);
+  const float ra = a * cs.x - b * cs.y;
+  const float rb = a * cs.y + b * cs.x;
+  a = ra;
+  b = rb;
+}
+
+// Destination of features [f, f+n) of token m, n <= 16 and inside one head.
+// Returns null (and records the error) when the token's position is invalid.
+__device__ __forceinline__ __nv_bfloat16* proj_dst(const ProjParams& p, int m, int f, int& pos) {
+  if (!p.qkv) {
+    pos = 0;
+    return p.out + static_cast<size_t>(m) * p.N + f;
+  }
+  const int b = m / p.T;
+  const int t = m - b * p.T;
+  const int start = p.sp.get(b);
+  if (!p.sp.ok(start)) {
+    if (t == 0 && (f & 127) == 0) report(p.status, DEV_BAD_POSITION);
+    return nullptr;
+  }
+  pos = start + t;
+  if (f < D_MODEL) return p.out + static_cast<size_t>(m) * D_MODEL + f;
+  const size_t row = (static_cast<size_t>(b) * p.s_max + pos) * KV_ROW;
+  if (f < D_MODEL + KV_ROW) return p.cache_k + row + (f - D_MODEL);
+  return p.cache_v + row + (f - D_MODEL - KV_ROW);
+}
+
+// Epilogue for 16 consecutive features f..f+15 (f multiple of 16) of token m.
+__device__ __forceinline__ void proj_store16(const ProjParams& p, int m, int f, float (&v)[16]) {
+  int pos;
+  __nv_bfloat16* dst = proj_dst(p, m, f, pos);
+  if (!dst) return;
+  if (p.qkv && f < D_MODEL + KV_ROW) {
+    const float4* cs = reinterpret_cast<const float4*>(
+        p.rope + (static_cast<size_t>(pos) * ROPE_PAIRS + ((f & (HEAD_DIM - 1)) >> 1)) * 2);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 c = cs[j];  // pairs 2j, 2j+1: (cos, sin, cos, sin)
+      float a = v[4 * j], b = v[4 * j + 1];
+      v[4 * j] = a * c.x - b * c.y;
+      v[4 * j + 1] = a * c.y + b * c.x;
+      a = v[4 * j + 2];
+      b = v[4 * j + 3];
+      v[4 * j + 2] = a * c.z - b * c.w;
+      v[4 * j + 3] = a * c.w + b * c.z;
+    }
+  }
+  uint4 lo, hi;
+  lo.x = pack_bf16(v[0], v[1]);
+  lo.y = pack_bf16(v[2], v[3]);
+  lo.z = pack_bf16(v[4], v[5]);
+  lo.w = pack_bf16(v[6], v[7]);
+  hi.x = pack_bf16(v[8], v[9]);
+  hi.y = pack_bf16(v[10], v[11]);
+  hi.z = pack_bf16(v[12], v[13]);
+  hi.w = pack_bf16(v[14], v[15]);
+  reinterpret_cast<uint4*>(dst)[0] = lo;
+  reinterpret_cast<uint4*>(dst)[1] = hi;
+}
+
+// Epilogue for the feature pair (f, f+1), f even.
+__device__ __forceinline__ void proj_store2(const ProjParams& p, int m, int f, float a, float b) {
+  int pos;
+  __nv_bfloat16* dst = proj_dst(p, m, f, pos);
+  if (!dst) return;
+  if (p.qkv && f < D_MODEL + KV_ROW) rope_pair(p.rope, pos, f, a, b);
+  *reinterpret_cast<uint32_t*>(dst) = pack_bf16(a, b);
+}
+
+// ----------------------------------------------------------------- launches
+// Split-K weight-streaming projection on mma.sync for M <= 64 tokens.
+// acc: fp32 [N][mp] zero-filled scratch, tickets: int [N/16] zero-filled;
+// both are left zero-filled on return.
+cudaError_t launch_gemv(const ProjParams& p, float* acc, int* tickets, int num_sms, cudaStream_t s);
+int gemv_padded_m(int M);  // acc row stride used for M tokens (0 if unsupported)
+
+// tcgen05 GEMM for M > 64 tokens. Maps are created by the caller.
+struct GemmMaps {
+  CUtensorMap a;      // activations [M][4096]
+  CUtensorMap b[3];   // w0, w1, w2
+};
+cudaError_t launch_gemm_tc(const GemmMaps& maps, const ProjParams& p, cudaStream_t s);
+constexpr int GEMM_BN = 256;
+constexpr int GEMM_BM = 128;
+
+// Decode attention (one new token per sequence), split over the key axis.
+struct DecodeAttnParams {
+  const __nv_bfloat16* q;  // [B][4096] rotated queries
+  int B;
+  StartPos sp;             // keys 0..sp(b) are read
+  int chunk;               // keys per split (multiple of 64)
+  int nsplit;              // splits allocated per (b, g)
+  float* part_o;           // [B*8*nsplit*4][128]
+  float* part_ml;          // [B*8*nsplit*4][2] (running max in log2 units, sum)
+  int* tickets;            // [B*8], zero-filled, left zero-filled
+  __nv_bfloat16* o;        // [B][4096]
+  int* status;
+};
+cudaError_t launch_attn_decode(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeAttnParams& a,
+                               cudaStream_t s);
+int decode_chunk(int B, int max_keys, int num_sms);
+
+// Causal prefill attention.
+struct PrefillAttnParams {
+  const __nv_bfloat16* q;  // [B*T][4096] rotated queries
+  int B, T;
+  StartPos sp;             // common start position (chunked prefill when > 0)
+  __nv_bfloat16* o;        // [B*T][4096]
+  int* status;
+};
+cudaError_t launch_attn_prefill(const CUtensorMap& mk, const CUtensorMap& mv, const PrefillAttnParams& a,
+                                cudaStream_t s);
+
+cudaError_t launch_rope_table(float* rope, int rows, double theta, int scaled, double factor, double lo,
+                              double hi, double ctx, cudaStream_t s);
+
+}  // namespace gqa

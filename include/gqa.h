@@ -1,0 +1,162 @@
+/*
+ * gqa.h — C ABI of the GB300 grouped-query attention block library (libgqa.so).
+ *
+ * One call runs the attention half of a Llama-3.1-8B transformer block on one
+ * GPU: x [B,T,4096] -> delta_attn [B,T,4096], updating the KV cache in place.
+ * The operation is the one the page "Llama 3.1 8B · Grouped-query attention"
+ * states in its header ("in: x [B batch, T positions, 4096 d], R [positions,
+ * 64 pairs]; out: delta_attn; state: KV cache, writes the new rows, reads rows
+ * 0..start_pos+T-1") and spells out in its Attention.forward excerpts:
+ *
+ *   q = x Wq^T, k = x Wk^T, v = x Wv^T                    (bias-free linears,
+ *                                                         weights stored [out,in])
+ *   q, k rotated by RoPE at position start_pos + t        (apply_rotary_emb)
+ *   cache_k/v[b, start_pos + t] = k, v   (bf16)           (the KV-cache state)
+ *   o_h = softmax(q_h K_g^T / sqrt(128) + causal mask) V_g, g = h / 4  (repeat_kv)
+ *   delta = o Wo^T, o features ordered h*128 + d          (head merge + wo)
+ *
+ * Fixed dimensions (the Llama 3.1 8B catalogue entry): d_model 4096, 32 query
+ * heads, 8 KV heads, head_dim 128.
+ *
+ * Conventions shared by every entry point
+ *   - bf16 tensors are raw 16-bit bfloat16 storage (gqa_bf16); all tensors are
+ *     dense row-major with the shapes given; device pointers unless stated.
+ *   - Every device pointer must be 16-byte aligned (128-bit loads and TMA).
+ *   - The caller owns all memory. The library never allocates, frees or
+ *     synchronises: it validates the arguments on the host, then enqueues
+ *     kernels on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *     returns. Results are ready when the stream reaches that point.
+ *   - Validation happens before any launch; on a non-zero return nothing was
+ *     enqueued (except GQA_ECUDA, which reports a failed launch).
+ *   - Conditions only the device can see (a per-sequence start position out of
+ *     range, a bounded wait that gave up) are recorded in the workspace status
+ *     word; read it with gqa_device_status().
+ *   - One workspace may serve one call at a time: calls that overlap on the
+ *     GPU must use different workspaces.
+ */
+#ifndef GQA_H
+#define GQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t gqa_bf16;
+
+#define GQA_D_MODEL 4096
+#define GQA_N_HEADS 32
+#define GQA_N_KV_HEADS 8
+#define GQA_HEAD_DIM 128
+#define GQA_ROPE_PAIRS 64
+
+/* Return codes (0 = success). */
+#define GQA_OK 0
+#define GQA_EINVAL (-1)      /* null pointer, non-positive size, position beyond cache/table */
+#define GQA_EALIGN (-2)      /* a pointer is not 16-byte aligned */
+#define GQA_EWORKSPACE (-3)  /* workspace smaller than gqa_workspace_bytes() */
+#define GQA_ECUDA (-4)       /* a CUDA runtime call or launch failed (see gqa_strerror) */
+#define GQA_EDEVICE (-5)     /* gqa_device_status(): a kernel recorded an error */
+
+/* Device status codes stored in the workspace status word. */
+#define GQA_DEV_OK 0
+#define GQA_DEV_BAD_POSITION 1  /* a start position < 0 or >= S_max / rope rows */
+#define GQA_DEV_WAIT_TIMEOUT 2  /* a bounded barrier wait gave up */
+
+/* Bytes of workspace a call with batch B, T new tokens per sequence and at
+ * most max_keys = start_pos + T cache rows read per sequence needs. The
+ * workspace holds the rotated queries, the attention output, split-K
+ * partials and tickets. It must be zero-filled before its first use (for
+ * example with gqa_workspace_init); every successful call leaves it ready
+ * for the next one. Returns 0 for invalid sizes. */
+size_t gqa_workspace_bytes(int B, int T, int max_keys);
+
+/* Zero-fill a workspace on `stream` (cudaMemsetAsync). */
+int gqa_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronously read the workspace status word into *status (GQA_DEV_*).
+ * Returns GQA_EDEVICE when it is non-zero, GQA_OK otherwise. Resets it to 0
+ * when `clear` is non-zero. Blocks until all prior work on the device is done. */
+int gqa_device_status(void* workspace, int* status, int clear);
+
+/* RoPE table R for positions 0..rows-1: rope[p][i] = (cos, sin) of p * f_i,
+ * fp32, shape [rows, 64, 2]. f_i = theta^(-2i/128); with `scaled` non-zero
+ * the Llama 3.1 frequency rescaling is applied (pairs whose wavelength
+ * 2*pi/f_i exceeds original_context/low_freq_factor are divided by
+ * `factor`, those shorter than original_context/high_freq_factor are kept,
+ * the band between is interpolated linearly in
+ * mu = (original_context/wavelength - low_freq_factor) /
+ *      (high_freq_factor - low_freq_factor)).
+ * The page "Prepare Q, K, V · Key heads" names the rule; the pages do not
+ * print it, and this reading is stated in the design notes. Angles are
+ * formed and evaluated in fp64 on the device, then stored as fp32. */
+int gqa_rope_table(float* rope, int rows, double theta, int scaled, double factor,
+                   double low_freq_factor, double high_freq_factor,
+                   double original_context, void* stream);
+
+/* The block for one batch with a common start position (the pages'
+ * forward(x, start_pos, freqs_cis, mask)).
+ *   x        [B, T, 4096] bf16, the (normalised) block input
+ *   wq       [4096, 4096], wk [1024, 4096], wv [1024, 4096], wo [4096, 4096] bf16
+ *   rope     [rope_rows, 64, 2] fp32 table from gqa_rope_table (row = position)
+ *   cache_k, cache_v  [B, s_max, 8, 128] bf16; rows start_pos..start_pos+T-1
+ *            are overwritten with the new rotated keys / values, rows
+ *            0..start_pos+T-1 are read, every other row is left untouched
+ *   out      [B, T, 4096] bf16, delta_attn
+ * Requires start_pos >= 0, start_pos + T <= s_max and <= rope_rows.
+ * T == 1 runs the decode path, T > 1 the causal prefill path (the mask of
+ * Transformer.forward: query t sees keys 0..start_pos+t). */
+int gqa_block_forward(const gqa_bf16* x, int B, int T, int start_pos,
+                      const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv,
+                      const gqa_bf16* wo, const float* rope, int rope_rows,
+                      gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max, gqa_bf16* out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* One decode step (T = 1) with a start position per sequence.
+ *   start_pos  device int32 [B]: sequence b has start_pos[b] cached rows,
+ *              writes row start_pos[b] and attends over rows 0..start_pos[b]
+ *   max_start_pos  a host-side bound with start_pos[b] <= max_start_pos for
+ *              every b; it sizes the split-K work and must satisfy
+ *              max_start_pos + 1 <= s_max and <= rope_rows.
+ * A start_pos[b] outside [0, max_start_pos] is reported as
+ * GQA_DEV_BAD_POSITION in the status word and sequence b is skipped: its
+ * cache rows are not written and its output row is unspecified. Other
+ * arguments as in
+ * gqa_block_forward with x [B, 1, 4096] and out [B, 1, 4096]. */
+int gqa_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos,
+               const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo,
+               const float* rope, int rope_rows, gqa_bf16* cache_k, gqa_bf16* cache_v,
+               int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
+               void* stream);
+
+/* Causal prefill of T >= 1 new tokens per sequence after start_pos cached
+ * rows (start_pos > 0 is a chunked prefill over an existing prefix).
+ * Arguments as in gqa_block_forward. */
+int gqa_prefill(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* wq,
+                const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo,
+                const float* rope, int rope_rows, gqa_bf16* cache_k, gqa_bf16* cache_v,
+                int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/* Static description of a return code (GQA_ECUDA appends the last CUDA
+ * error name seen by this library on the calling thread). */
+const char* gqa_strerror(int status);
+
+/* Number of kernels the most recent successful call on this thread enqueued. */
+int gqa_last_launch_count(void);
+
+/* Measurement hook; it changes nothing the block computes. While set, every
+ * block call on the calling thread records events[0] on its stream before its
+ * first kernel and events[i] right after its i-th kernel (for i < count), so
+ * a profiler can time each kernel with cudaEventElapsedTime. `events` holds
+ * caller-created cudaEvent_t handles and must stay valid while set;
+ * count = 0 (or events = NULL) stops the recording. */
+int gqa_set_profile_events(void* const* events, int count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_H */

@@ -188,12 +188,14 @@ def sequence_forward(x: np.ndarray, wq: np.ndarray, wk: np.ndarray, wv: np.ndarr
     visible = np.arange(L)[None, :] <= (start_pos + rows)[:, None]      # [R, L]
     o = np.empty((len(rows), n_heads, head_dim))
     scale = 1.0 / math.sqrt(head_dim)
+    R = len(rows)
     for g in range(n_kv_heads):
         heads = slice(g * n_rep, (g + 1) * n_rep)                 # KV head g serves h // n_rep == g
-        s = np.einsum("rhd,jd->rhj", q[:, heads, :], keys[:, g, :]) * scale
+        qg = q[:, heads, :].reshape(R * n_rep, head_dim)          # (row, head) pairs
+        s = (qg @ keys[:, g, :].T).reshape(R, n_rep, L) * scale
         s = np.where(visible[:, None, :], s, -np.inf)
         p = softmax(s, axis=-1)
-        o[:, heads, :] = np.einsum("rhj,jd->rhd", p, values[:, g, :])
+        o[:, heads, :] = (p.reshape(R * n_rep, L) @ values[:, g, :]).reshape(R, n_rep, head_dim)
 
     # 5: merge heads (feature h*d_h + d) and project
     delta = o.reshape(len(rows), n_heads * head_dim) @ wo.T

@@ -1,0 +1,130 @@
+"""Test harness: run the CUDA library and the CPU oracle on the same seeded
+inputs and compare. Used by the GPU parity tests, ``__graft_entry__.smoke``
+and the bench's oracle leg; it is test infrastructure (it imports the oracle).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+import gqa_inputs as I
+from oracle import gqa as O
+
+# Parity bar for delta_attn (bf16 I/O, fp32 accumulation).
+REL_L2_TOL = 1e-2
+MAX_ABS_TOL = 3e-2
+
+
+@dataclass
+class Case:
+    B: int
+    T: int
+    start: list               # per-sequence start positions
+    s_max: int
+    seed: int = 0
+    rope: I.RopeConfig = I.LLAMA31_ROPE
+    dev: dict = field(default_factory=dict)     # device tensors
+    host: dict = field(default_factory=dict)    # CPU copies of the inputs
+
+
+def make_case(B: int, T: int, start: Sequence[int], s_max: int, seed: int = 0,
+              rope: I.RopeConfig = I.LLAMA31_ROPE, weights=None, cache_device=None) -> Case:
+    """Seeded inputs on cuda:0 (weights may be shared between cases)."""
+    start = [int(s) for s in start]
+    c = Case(B, T, start, s_max, seed, rope)
+    if weights is None:
+        gen, w = I.draw_weights(seed=seed)
+    else:
+        gen, w = weights
+    x = I.draw_x(gen, B, T)
+    ck, cv = I.draw_cache(B, s_max, start, seed=seed, device=cache_device)
+    c.host = {"x": x, **w}
+    c.dev = {k: v.to("cuda") for k, v in c.host.items()}
+    c.dev["cache_k"] = ck.to("cuda")
+    c.dev["cache_v"] = cv.to("cuda")
+    c.dev["cache_k0"] = c.dev["cache_k"].clone()   # untouched copies for the canary check
+    c.dev["cache_v0"] = c.dev["cache_v"].clone()
+    return c
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+_W64 = {}
+
+
+def weights64(c: Case):
+    key = id(c.host["wq"])
+    if key not in _W64:
+        _W64.clear()
+        _W64[key] = {k: f64(c.host[k]) for k in ("wq", "wk", "wv", "wo")}
+    return _W64[key]
+
+
+def oracle_sequence(c: Case, b: int, query_rows=None):
+    """Oracle delta / new cache rows of sequence b, from the untouched cache."""
+    r = c.rope
+    freqs = O.rope_frequencies(128, r.theta, r.scaled, r.factor, r.low_freq_factor,
+                               r.high_freq_factor, r.original_context)
+    w = weights64(c)
+    sp = c.start[b]
+    ck = f64(c.dev["cache_k0"][b, :sp])
+    cv = f64(c.dev["cache_v0"][b, :sp])
+    return O.sequence_forward(f64(c.host["x"][b]), w["wq"], w["wk"], w["wv"], w["wo"], sp, ck, cv,
+                              freqs, 32, 8, query_rows)
+
+
+def rel_l2(got: np.ndarray, ref: np.ndarray) -> float:
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+
+
+def ordered_bf16(t: torch.Tensor) -> np.ndarray:
+    """bf16 bit patterns mapped to integers that order like the values."""
+    bits = t.contiguous().view(torch.int16).to(torch.int32).numpy()
+    mag = bits & 0x7FFF
+    return np.where(bits < 0, -mag, mag)
+
+
+def check_rows_within_one_ulp(got_bf16: torch.Tensor, ref64: np.ndarray, what: str):
+    ref = torch.from_numpy(np.ascontiguousarray(ref64)).to(torch.bfloat16)   # exact: ref is bf16-valued
+    d = np.abs(ordered_bf16(got_bf16.cpu()) - ordered_bf16(ref))
+    assert d.max() <= 1, f"{what}: {int((d > 1).sum())} values differ by more than 1 bf16 ulp (max {d.max()})"
+
+
+def compare_sequence(c: Case, out: torch.Tensor, b: int, query_rows=None, check_cache=True):
+    """Oracle vs GPU for sequence b; returns (rel_l2, max_abs)."""
+    dl, nk, nv = oracle_sequence(c, b, query_rows)
+    rows = slice(None) if query_rows is None else list(query_rows)
+    got = f64(out[b])[rows]
+    r2 = rel_l2(got, dl)
+    ma = float(np.abs(got - dl).max())
+    assert np.isfinite(got).all(), f"non-finite output in sequence {b}"
+    assert r2 <= REL_L2_TOL, f"sequence {b}: rel L2 {r2:.3e} > {REL_L2_TOL}"
+    assert ma <= MAX_ABS_TOL, f"sequence {b}: max abs {ma:.3e} > {MAX_ABS_TOL}"
+    if check_cache:
+        sp, T = c.start[b], c.T
+        check_rows_within_one_ulp(c.dev["cache_k"][b, sp:sp + T], nk, f"cache_k rows of sequence {b}")
+        check_rows_within_one_ulp(c.dev["cache_v"][b, sp:sp + T], nv, f"cache_v rows of sequence {b}")
+    return r2, ma
+
+
+def check_canaries(c: Case, seqs=None):
+    """Cache rows outside [start_b, start_b + T) must be bit-identical."""
+    for b in (range(c.B) if seqs is None else seqs):
+        sp = c.start[b]
+        for name in ("cache_k", "cache_v"):
+            now, before = c.dev[name][b], c.dev[name + "0"][b]
+            assert torch.equal(now[:sp], before[:sp]), f"{name}[{b}] rows before start_pos changed"
+            assert torch.equal(now[sp + c.T:], before[sp + c.T:]), f"{name}[{b}] rows after the new ones changed"
+
+
+def rope_for(c: Case, rows: Optional[int] = None):
+    import grouped_query_attention_gemv_gb300 as G
+    r = c.rope
+    return G.rope_table(rows or c.s_max, r.theta, r.scaled, r.factor, r.low_freq_factor,
+                        r.high_freq_factor, r.original_context)

@@ -1,0 +1,97 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads,
+exports every function include/gqa.h declares, sizes workspaces, and rejects
+bad arguments on the host before anything is launched.
+
+Every call below fails validation by construction (the pointers are fake
+but are never dereferenced, because validation runs before any launch)."""
+import ctypes
+
+import pytest
+
+import grouped_query_attention_gemv_gb300 as G
+from grouped_query_attention_gemv_gb300 import build as gbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return G.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = G.exported_symbols()
+    assert set(names) >= {"gqa_block_forward", "gqa_decode", "gqa_prefill", "gqa_workspace_bytes",
+                          "gqa_strerror", "gqa_rope_table"}
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in gqa.h but not exported"
+
+
+def test_strerror_covers_codes(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.gqa_strerror(code)
+    assert b"unknown" in lib.gqa_strerror(-99)
+
+
+def test_workspace_sizes(lib):
+    ws = G.workspace_bytes
+    assert ws(0, 1, 1) == 0 and ws(1, 0, 1) == 0 and ws(1, 4, 3) == 0   # max_keys < T
+    a, b = ws(16, 1, 1001), ws(16, 1, 131072)
+    assert 0 < a < b                                   # split-K partials grow with context
+    assert ws(1, 2048, 2048) >= 2 * 2048 * 4096 * 2    # rotated q + attention output, bf16
+    assert ws(64, 1, 32769) % 256 == 0
+
+
+FAKE = 1 << 20   # aligned, never dereferenced
+
+
+def call_block(lib, **kw):
+    a = dict(x=FAKE, B=2, T=1, start_pos=5, wq=FAKE, wk=FAKE, wv=FAKE, wo=FAKE, rope=FAKE, rope_rows=64,
+             ck=FAKE, cv=FAKE, s_max=64, out=FAKE, ws=FAKE, ws_bytes=1 << 40, stream=None)
+    a.update(kw)
+    return lib.gqa_block_forward(a["x"], a["B"], a["T"], a["start_pos"], a["wq"], a["wk"], a["wv"], a["wo"],
+                                 a["rope"], a["rope_rows"], a["ck"], a["cv"], a["s_max"], a["out"], a["ws"],
+                                 a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), -1), (dict(wo=None), -1), (dict(ws=None), -1), (dict(rope=None), -1),
+    (dict(B=0), -1), (dict(T=0), -1), (dict(start_pos=-1), -1),
+    (dict(start_pos=60, T=5), -1),          # start_pos + T > s_max
+    (dict(start_pos=60, T=4, rope_rows=63), -1),   # beyond the rope table
+    (dict(x=FAKE + 2), -2), (dict(ck=FAKE + 8), -2), (dict(out=FAKE + 4), -2),
+    (dict(ws_bytes=16), -3),
+])
+def test_block_forward_rejects_bad_arguments(lib, kw, code):
+    assert call_block(lib, **kw) == code
+
+
+def test_decode_rejects_bad_arguments(lib):
+    d = lib.gqa_decode
+    args = [FAKE, 4, FAKE, 10, FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, FAKE, 64, FAKE, FAKE, 1 << 40, None]
+    bad = list(args)
+    bad[2] = None          # start_pos array
+    assert d(*bad) == -1
+    bad = list(args)
+    bad[3] = 64            # max_start_pos + 1 > s_max
+    assert d(*bad) == -1
+    bad = list(args)
+    bad[2] = FAKE + 2      # start_pos array misaligned
+    assert d(*bad) == -2
+    bad = list(args)
+    bad[15] = 100          # workspace too small
+    assert d(*bad) == -3
+
+
+def test_rope_table_rejects_bad_arguments(lib):
+    f = lib.gqa_rope_table
+    assert f(None, 16, 5e5, 1, 8.0, 1.0, 4.0, 8192.0, None) == -1
+    assert f(FAKE, 0, 5e5, 1, 8.0, 1.0, 4.0, 8192.0, None) == -1
+    assert f(FAKE, 16, 5e5, 1, 8.0, 4.0, 1.0, 8192.0, None) == -1   # high <= low
+    assert f(FAKE + 4, 16, 5e5, 1, 8.0, 1.0, 4.0, 8192.0, None) == -2
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(G, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(G, "_lib", None)
+    with pytest.raises(ImportError):
+        G.lib()

@@ -1,0 +1,210 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle on
+the same seeded inputs. Bar: delta_attn within rel-L2 1e-2 and max-abs 3e-2
+(bf16 I/O, fp32 accumulation), written cache rows within 1 bf16 ulp, every
+other cache row bit-identical, workspace status word clear."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_inputs as I
+from oracle import gqa as O
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+G = pytest.importorskip("grouped_query_attention_gemv_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from grouped_query_attention_gemv_gb300 import build
+    build.build()
+
+
+@pytest.fixture(scope="module")
+def weights():
+    return I.draw_weights(seed=0)
+
+
+def run_decode(c, max_start=None, ws=None, rope=None):
+    d = c.dev
+    sp = torch.tensor(c.start, dtype=torch.int32, device="cuda")
+    max_start = max(c.start) if max_start is None else max_start
+    ws = G.make_workspace(c.B, 1, max_start + 1) if ws is None else ws
+    rope = H.rope_for(c) if rope is None else rope
+    out = G.decode(d["x"], sp, max_start, d["wq"], d["wk"], d["wv"], d["wo"], rope, d["cache_k"], d["cache_v"],
+                   workspace=ws)
+    torch.cuda.synchronize()
+    assert G.device_status(ws) == 0
+    return out, ws
+
+
+def run_prefill(c, ws=None, entry="prefill"):
+    d = c.dev
+    assert len(set(c.start)) == 1
+    sp = c.start[0]
+    ws = G.make_workspace(c.B, c.T, sp + c.T) if ws is None else ws
+    fn = G.prefill if entry == "prefill" else G.block_forward
+    out = fn(d["x"], sp, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"], workspace=ws)
+    torch.cuda.synchronize()
+    assert G.device_status(ws) == 0
+    return out, ws
+
+
+# ------------------------------------------------------------------ RoPE table
+
+@pytest.mark.parametrize("scaled", [True, False])
+def test_rope_table_matches_oracle(scaled):
+    rows = 131072
+    t = G.rope_table(rows, scaled=scaled).cpu().double().numpy()
+    f = O.rope_frequencies(128, 500000.0, scaled)
+    for lo in (0, 4097, rows - 2048):
+        c, s = O.rope_cos_sin(np.arange(lo, lo + 2048), f)
+        np.testing.assert_allclose(t[lo:lo + 2048, :, 0], c, rtol=0, atol=2e-7)
+        np.testing.assert_allclose(t[lo:lo + 2048, :, 1], s, rtol=0, atol=2e-7)
+
+
+# ------------------------------------------------------------------ decode
+
+@pytest.mark.parametrize("B,starts,s_max", [
+    (1, [0], 4),                          # one key: o_h = v_{h//4}
+    (3, [0, 5, 130], 160),                # ragged tails, several splits
+    (2, [63, 64], 80),                    # tile edges
+    (16, list(range(0, 1600, 100)), 1600),
+    (40, None, 700),                      # M = 40 token projection (n-tile padding)
+    (64, None, 520),                      # largest few-token projection
+    (80, None, 300),                      # tensor-core projection (M > 64)
+])
+def test_decode_small_matches_oracle(weights, B, starts, s_max):
+    if starts is None:
+        g = torch.Generator().manual_seed(B)
+        starts = torch.randint(0, s_max, (B,), generator=g).tolist()
+    c = H.make_case(B, 1, starts, s_max, weights=weights)
+    out, _ = run_decode(c)
+    for b in range(B):
+        H.compare_sequence(c, out, b)
+    H.check_canaries(c)
+
+
+def test_decode_is_repeatable_with_a_reused_workspace(weights):
+    c = H.make_case(5, 1, [700, 10, 333, 1024, 1], 1100, weights=weights)
+    out1, ws = run_decode(c)
+    out1 = out1.clone()
+    out2, _ = run_decode(c, ws=ws)
+    assert torch.equal(out1, out2)
+    for b in range(5):
+        H.compare_sequence(c, out2, b)
+
+
+def test_decode_bad_start_position_is_reported_and_skipped(weights):
+    c = H.make_case(3, 1, [5, 9, 7], 16, weights=weights)
+    d = c.dev
+    sp = torch.tensor([5, 12, 7], dtype=torch.int32, device="cuda")   # 12 > max_start_pos 9
+    ws = G.make_workspace(3, 1, 10)
+    out = torch.full_like(d["x"], float("nan"))
+    G.decode(d["x"], sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"],
+             out=out, workspace=ws)
+    assert G.device_status(ws, clear=True) == 1
+    assert torch.equal(d["cache_k"][1], d["cache_k0"][1])   # skipped sequence untouched
+    c.start = [5, 9, 7]
+    for b in (0, 2):
+        H.compare_sequence(c, out, b)
+
+
+@pytest.mark.parametrize("name", ["decode_b1_p15", "decode_b16_p1000"])
+def test_decode_workloads_full(weights, name):
+    w = I.workload(name)
+    c = H.make_case(w.B, 1, w.start_positions().tolist(), w.cache_rows(), weights=weights)
+    out, _ = run_decode(c)
+    worst = 0.0
+    for b in range(w.B):
+        worst = max(worst, H.compare_sequence(c, out, b)[0])
+    H.check_canaries(c)
+
+
+def test_block_forward_decode_matches_oracle(weights):
+    c = H.make_case(4, 1, [37, 37, 37, 37], 40, weights=weights)
+    d = c.dev
+    ws = G.make_workspace(4, 1, 38)
+    out = G.block_forward(d["x"], 37, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"],
+                          d["cache_v"], workspace=ws)
+    torch.cuda.synchronize()
+    assert G.device_status(ws) == 0
+    assert G.last_launch_count() == 3
+    for b in range(4):
+        H.compare_sequence(c, out, b)
+
+
+# ------------------------------------------------------------------ prefill
+
+@pytest.mark.parametrize("B,T,start,s_max", [
+    (1, 5, 0, 8),          # few tokens: few-token projection path with T > 1
+    (2, 37, 0, 40),        # M = 74: tensor-core projection, ragged M tile and query tile
+    (1, 50, 70, 130),      # chunked prefill over a cached prefix
+    (1, 300, 0, 300),      # three M tiles, ragged
+    (3, 129, 200, 400),    # chunked, several sequences
+])
+def test_prefill_small_matches_oracle(weights, B, T, start, s_max):
+    c = H.make_case(B, T, [start] * B, s_max, weights=weights)
+    out, _ = run_prefill(c)
+    for b in range(B):
+        H.compare_sequence(c, out, b)
+    H.check_canaries(c)
+
+
+def test_prefill_then_decode_equals_longer_prefill(weights):
+    c = H.make_case(1, 9, [0], 16, weights=weights)
+    out9, _ = run_prefill(c)
+    # decode the 10th token on top of the cache the prefill wrote
+    x10 = I.draw_x(torch.Generator().manual_seed(99), 1, 1).cuda()
+    d = c.dev
+    sp = torch.tensor([9], dtype=torch.int32, device="cuda")
+    o10 = G.decode(x10, sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"])
+    c2 = H.make_case(1, 10, [0], 16, weights=weights)
+    c2.dev["x"][:, :9] = c.dev["x"]
+    c2.dev["x"][:, 9:] = x10
+    c2.host["x"] = c2.dev["x"].cpu()
+    out10, _ = run_prefill(c2)
+    torch.cuda.synchronize()
+    ref = H.f64(out10[0, 9])
+    got = H.f64(o10[0, 0])
+    assert H.rel_l2(got, ref) < 1e-2
+    for name in ("cache_k", "cache_v"):
+        d1 = H.ordered_bf16(c.dev[name][0, :10].cpu()) - H.ordered_bf16(c2.dev[name][0, :10].cpu())
+        assert np.abs(d1).max() <= 1
+
+
+@pytest.mark.parametrize("name,rows", [("prefill_b1_t2048", None), ("prefill_b4_t2048", 192)])
+def test_prefill_workloads_full(weights, name, rows):
+    w = I.workload(name)
+    c = H.make_case(w.B, w.T, w.start_positions().tolist(), w.cache_rows(), weights=weights)
+    out, _ = run_prefill(c, entry="block_forward")
+    g = np.random.default_rng(0)
+    for b in range(w.B):
+        q = None if rows is None else sorted(set(g.choice(w.T, rows, replace=False).tolist()) | {0, w.T - 1})
+        H.compare_sequence(c, out, b, query_rows=q)
+    H.check_canaries(c)
+
+
+@pytest.mark.parametrize("name,sample", [("batched_decode_b64_p512_32768", 4), ("long_decode_b8_p131071", 2)])
+def test_large_decode_workloads_sampled(weights, name, sample):
+    w = I.workload(name)
+    starts = w.start_positions().tolist()
+    c = H.make_case(w.B, 1, starts, w.cache_rows(), weights=weights, cache_device="cuda")
+    out, _ = run_decode(c)
+    order = np.argsort(starts)
+    seqs = sorted({int(order[0]), int(order[-1])} | set(list(range(0, w.B, max(1, w.B // sample)))[:sample]))
+    for b in seqs:
+        H.compare_sequence(c, out, b)
+    # every written row and the rows around it, for all sequences
+    for b in range(w.B):
+        sp = starts[b]
+        for name_ in ("cache_k", "cache_v"):
+            now, before = c.dev[name_][b], c.dev[name_ + "0"][b]
+            lo = max(0, sp - 64)
+            assert torch.equal(now[lo:sp], before[lo:sp])
+            assert torch.equal(now[sp + 1:sp + 65], before[sp + 1:sp + 65])

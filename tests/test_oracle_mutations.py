@@ -28,7 +28,7 @@ MUTANTS = {
                      "np.where(wavelength < short_edge, f / factor, np.where(wavelength > long_edge, f, mid))"),
     "rope_on_values": ("v = (x @ wv.T).reshape(T, n_kv_heads, head_dim)",
                        "v = rope_rotate((x @ wv.T).reshape(T, n_kv_heads, head_dim), cos[:, None, :], sin[:, None, :])"),
-    "softmax_no_max_shift_and_wrong_axis": ("return e / np.sum(e, axis=axis, keepdims=True)",
+    "softmax_wrong_axis": ("return e / np.sum(e, axis=axis, keepdims=True)",
                                             "return e / np.sum(e, axis=0, keepdims=True)"),
 }
 
