@@ -363,6 +363,9 @@ def main():
     # kernel, with a device-side backlog so host gaps do not enter the intervals
     ksteps = min(a.steps, 200)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(ksteps)]
+    for e4 in evs:          # torch only times events it has recorded once itself
+        for e in e4:
+            e.record(stream)
     torch.cuda.synchronize()
     torch.cuda._sleep(int(3e8))
     for i in range(ksteps):

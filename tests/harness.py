@@ -90,10 +90,30 @@ def ordered_bf16(t: torch.Tensor) -> np.ndarray:
     return np.where(bits < 0, -mag, mag)
 
 
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |v| (8 significant bits, fp32 exponent range)."""
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, 2.0 ** (np.maximum(e, -126) - 7), 2.0 ** -133)
+
+
+# Absolute floor of the cache-row check, relative to the RMS of the 128-value
+# head row: an fp32 dot product of 4096 terms carries an error of order
+# 2^-24 * sqrt(4096) = 2^-18 of the row scale, so values that cancel to
+# nearly zero cannot be pinned to their own (tiny) bf16 ulp.
+CACHE_FLOOR = 2.0 ** -16
+
+
 def check_rows_within_one_ulp(got_bf16: torch.Tensor, ref64: np.ndarray, what: str):
-    ref = torch.from_numpy(np.ascontiguousarray(ref64)).to(torch.bfloat16)   # exact: ref is bf16-valued
-    d = np.abs(ordered_bf16(got_bf16.cpu()) - ordered_bf16(ref))
-    assert d.max() <= 1, f"{what}: {int((d > 1).sum())} values differ by more than 1 bf16 ulp (max {d.max()})"
+    """|got - ref| <= ulp_bf16(ref) + CACHE_FLOOR * rms(head row of ref)."""
+    got = got_bf16.detach().to("cpu", torch.float64).numpy()
+    rms = np.sqrt(np.mean(ref64 ** 2, axis=-1, keepdims=True))
+    tol = bf16_ulp(ref64) + CACHE_FLOOR * rms
+    err = np.abs(got - ref64)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} values beyond 1 bf16 ulp "
+                           f"(worst excess {float((err - tol).max()):.3e}, at ref "
+                           f"{float(ref64.reshape(-1)[np.argmax((err - tol).reshape(-1))]):.3e})")
 
 
 def compare_sequence(c: Case, out: torch.Tensor, b: int, query_rows=None, check_cache=True):
