@@ -23,9 +23,11 @@ __all__ = [
     "GQAError", "D_MODEL", "N_HEADS", "N_KV_HEADS", "HEAD_DIM", "library_path", "lib",
     "exported_symbols", "workspace_bytes", "make_workspace", "rope_table", "block_forward",
     "decode", "prefill", "device_status", "last_launch_count", "set_profile_events",
+    "decode_static", "static_device_status", "STATIC_SCRATCH_BYTES",
 ]
 
 D_MODEL, N_HEADS, N_KV_HEADS, HEAD_DIM = 4096, 32, 8, 128
+STATIC_SCRATCH_BYTES = 8 << 20
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "lib", "libgqa.so")
 _HEADER = os.path.join(os.path.dirname(_PKG), "include", "gqa.h")
@@ -42,6 +44,8 @@ _SIGNATURES = {
     "gqa_strerror": (ctypes.c_char_p, [_i]),
     "gqa_last_launch_count": (_i, []),
     "gqa_set_profile_events": (_i, [ctypes.POINTER(_vp), _i]),
+    "gqa_decode_static": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp]),
+    "gqa_static_device_status": (_i, [ctypes.POINTER(_i), _i]),
 }
 
 
@@ -226,3 +230,28 @@ def set_profile_events(events) -> None:
     r = lib().gqa_set_profile_events(arr, len(events))
     if r:
         raise GQAError(r, "gqa_set_profile_events")
+
+
+def decode_static(x, start_pos: torch.Tensor, max_start_pos: int, wq, wk, wv, wo, rope, cache_k, cache_v,
+                  out=None, stream=None) -> torch.Tensor:
+    """``decode`` without a workspace: the library's own static device scratch
+    (``STATIC_SCRATCH_BYTES``) is used, so nothing is allocated for scratch.
+    For callers that must not allocate device memory per step. Calls share
+    that scratch: do not overlap them on the GPU."""
+    B, out = _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, 1)
+    _check(start_pos, "start_pos", torch.int32, (B,))
+    r = lib().gqa_decode_static(_p(x), B, _p(start_pos), int(max_start_pos), _p(wq), _p(wk), _p(wv), _p(wo),
+                                _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
+                                _s(stream))
+    if r:
+        raise GQAError(r, "gqa_decode_static")
+    return out
+
+
+def static_device_status(clear: bool = False) -> int:
+    """Status word of the static scratch on the current device (synchronises)."""
+    st = ctypes.c_int(0)
+    r = lib().gqa_static_device_status(ctypes.byref(st), int(clear))
+    if r not in (0, -5):
+        raise GQAError(r, "gqa_static_device_status")
+    return st.value

@@ -367,6 +367,9 @@ const char* gqa_strerror(int status) {
     case GQA_EALIGN: return "pointer not 16-byte aligned";
     case GQA_EWORKSPACE: return "workspace smaller than gqa_workspace_bytes()";
     case GQA_EDEVICE: return "a kernel recorded an error in the workspace status word";
+    case GQA_ESCRATCH:
+      return "call needs more scratch than gqa_decode_static's static array (GQA_STATIC_SCRATCH_BYTES = 8 MiB); "
+             "use gqa_decode with a workspace";
     case GQA_ECUDA:
       snprintf(t_msg, sizeof(t_msg), "CUDA error: %s", cudaGetErrorName(t_last_cuda));
       return t_msg;
@@ -384,3 +387,69 @@ int gqa_set_profile_events(void* const* events, int count) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gqa_decode_static: the decode step with its scratch in a static device array
+// instead of a caller-provided workspace, for callers that cannot allocate.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[GQA_STATIC_SCRATCH_BYTES];
+
+std::mutex g_static_mu;
+void* g_static_ptr[64] = {};
+
+// Device address of g_static_scratch on the current device. In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device with that device current.
+int static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= 64) return fail_cuda(cudaErrorInvalidDevice);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return fail_cuda(e);
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" int gqa_decode_static(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos,
+                                 const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo,
+                                 const float* rope, int rope_rows, gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max,
+                                 gqa_bf16* out, void* stream) {
+  if (!start_pos || max_start_pos < 0 || max_start_pos > (1 << 30) || B <= 0) return GQA_EINVAL;
+  Layout need;
+  if (!make_layout(B, 1, max_start_pos + 1, &need)) return GQA_EINVAL;
+  if (need.total > GQA_STATIC_SCRATCH_BYTES) return GQA_ESCRATCH;
+  if (!x || !wq || !wk || !wv || !wo || !rope || !cache_k || !cache_v || !out) return GQA_EINVAL;
+  void* scratch = nullptr;
+  int r = static_scratch(&scratch);
+  if (r != GQA_OK) return r;
+  // everything gqa_decode checks, checked before the clear is enqueued
+  Layout L;
+  r = check_common(x, B, 1, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, out, scratch,
+                   max_start_pos + 1, GQA_STATIC_SCRATCH_BYTES, &L);
+  if (r != GQA_OK) return r;
+  if ((reinterpret_cast<uintptr_t>(start_pos) & 3u) != 0) return GQA_EALIGN;
+  cudaError_t e = cudaMemsetAsync(scratch, 0, L.total, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return gqa_decode(x, B, start_pos, max_start_pos, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, out,
+                    scratch, GQA_STATIC_SCRATCH_BYTES, stream);
+}
+
+extern "C" int gqa_static_device_status(int* status, int clear) {
+  if (!status) return GQA_EINVAL;
+  void* scratch = nullptr;
+  int r = static_scratch(&scratch);
+  if (r != GQA_OK) return r;
+  return gqa_device_status(scratch, status, clear);
+}

@@ -59,6 +59,7 @@ typedef uint16_t gqa_bf16;
 #define GQA_EWORKSPACE (-3)  /* workspace smaller than gqa_workspace_bytes() */
 #define GQA_ECUDA (-4)       /* a CUDA runtime call or launch failed (see gqa_strerror) */
 #define GQA_EDEVICE (-5)     /* gqa_device_status(): a kernel recorded an error */
+#define GQA_ESCRATCH (-6)    /* gqa_decode_static: call needs more than GQA_STATIC_SCRATCH_BYTES */
 
 /* Device status codes stored in the workspace status word. */
 #define GQA_DEV_OK 0
@@ -154,6 +155,43 @@ int gqa_last_launch_count(void);
  * caller-created cudaEvent_t handles and must stay valid while set;
  * count = 0 (or events = NULL) stops the recording. */
 int gqa_set_profile_events(void* const* events, int count);
+
+/* Size of the scratch array gqa_decode_static works in (8 MiB). */
+#define GQA_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* gqa_decode without a workspace argument, for callers that cannot allocate
+ * device memory when they run a step: for instance an engine plugin whose
+ * enqueue hook must not call cudaMalloc, or a real-time serving loop where a
+ * synchronous allocation would stall the device. The pages have no
+ * counterpart to this; it only changes where the scratch memory lives.
+ *
+ * The scratch (rotated queries, attention output, split-K partials, tickets,
+ * status word) is a file-scope __device__ array of GQA_STATIC_SCRATCH_BYTES
+ * inside libgqa, so every GPU that loads the library holds it until the
+ * process exits. Arguments and results are exactly those of gqa_decode; the
+ * caller still passes every input and output buffer.
+ *   - A call whose workspace (gqa_workspace_bytes(B, 1, max_start_pos + 1))
+ *     exceeds GQA_STATIC_SCRATCH_BYTES returns GQA_ESCRATCH and enqueues
+ *     nothing; e.g. B = 16 fits up to about 50,000 cached positions.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.
+ *   - Each call clears the part of the array it uses (cudaMemsetAsync on
+ *     `stream`) before its kernels; it allocates and frees nothing.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents: calls that overlap on the GPU (different streams, or several
+ *     host threads) race and must be serialised by the caller.
+ *   - Device-side errors go to the array's status word; read them with
+ *     gqa_static_device_status. */
+int gqa_decode_static(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos,
+                      const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv,
+                      const gqa_bf16* wo, const float* rope, int rope_rows,
+                      gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max, gqa_bf16* out,
+                      void* stream);
+
+/* Status word of the gqa_decode_static scratch on the current device (as
+ * gqa_device_status: synchronises, returns GQA_EDEVICE when non-zero). */
+int gqa_static_device_status(int* status, int clear);
 
 #ifdef __cplusplus
 }

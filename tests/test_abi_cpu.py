@@ -95,3 +95,14 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(G, "_lib", None)
     with pytest.raises(ImportError):
         G.lib()
+
+
+def test_decode_static_rejects_requests_beyond_its_scratch(lib):
+    # B = 64 at 131,072 cached positions needs far more than the 8 MiB static
+    # scratch: rejected on the host before any device work
+    assert G.workspace_bytes(64, 1, 131072) > G.STATIC_SCRATCH_BYTES
+    r = lib.gqa_decode_static(FAKE, 64, FAKE, 131071, FAKE, FAKE, FAKE, FAKE, FAKE, 131072, FAKE, FAKE, 131072,
+                              FAKE, None)
+    assert r == -6
+    assert b"static" in lib.gqa_strerror(-6)
+    assert lib.gqa_decode_static(FAKE, 0, FAKE, 10, FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, FAKE, 64, FAKE, None) == -1
