@@ -56,6 +56,8 @@ def args_():
     ap.add_argument("--workload", default="decode_b16_p1000")
     ap.add_argument("--replicas", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-kernels", choices=["fused", "three"], default="fused",
+                    help="decode step as one persistent grid (default) or as three kernels")
     return ap.parse_args()
 
 
@@ -74,6 +76,7 @@ def step_bytes(B: int, starts) -> dict:
         "decode_attention": kv_read + B * 8192 + B * 8192,           # cache rows 0..P, q, o
         "o_projection": 33554432 + B * 8192 + B * 8192,              # Wo, o, delta
         "step": WEIGHT_BYTES + kv_read + B * 4096 + 2 * B * 8192,    # the roofline's byte count
+        "decode_step": WEIGHT_BYTES + kv_read + B * 4096 + 2 * B * 8192,  # the fused kernel: the whole step
     }
 
 
@@ -246,6 +249,8 @@ def config_dict(w: I.Workload, a, starts):
          "n_kv_heads": 8, "head_dim": 128,
          "l2": f"inputs larger than L2: {a.replicas} rotating replicas of weights+cache+x, one per step",
          "parallelism": "replicas"}
+    if w.T == 1:
+        c["decode_kernels"] = a.decode_kernels
     if w.start_pos is not None:
         c["start_pos"] = w.start_pos
     else:
@@ -289,7 +294,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     decode = w.T == 1
-    kernels = KERNELS if decode else ("qkv_projection", "prefill_attention", "o_projection")
+    G.set_decode_fusion(a.decode_kernels == "fused")
 
     starts = w.start_positions().tolist()
     s_max = w.cache_rows()
@@ -320,6 +325,10 @@ def main():
         step(i)
     torch.cuda.synchronize()
     per_step_launches = G.last_launch_count()
+    if decode:
+        kernels = ("decode_step",) if per_step_launches == 1 else KERNELS
+    else:
+        kernels = ("qkv_projection", "prefill_attention", "o_projection")
     for r in reps:
         assert G.device_status(r["ws"]) == 0, "device status set during warm-up"
 
@@ -362,7 +371,7 @@ def main():
     # ---- per-kernel attribution: events recorded by the library around each
     # kernel, with a device-side backlog so host gaps do not enter the intervals
     ksteps = min(a.steps, 200)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(ksteps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)] for _ in range(ksteps)]
     for e4 in evs:          # torch only times events it has recorded once itself
         for e in e4:
             e.record(stream)

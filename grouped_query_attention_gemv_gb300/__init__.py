@@ -23,11 +23,11 @@ __all__ = [
     "GQAError", "D_MODEL", "N_HEADS", "N_KV_HEADS", "HEAD_DIM", "library_path", "lib",
     "exported_symbols", "workspace_bytes", "make_workspace", "rope_table", "block_forward",
     "decode", "prefill", "device_status", "last_launch_count", "set_profile_events",
-    "decode_static", "static_device_status", "STATIC_SCRATCH_BYTES",
+    "set_decode_fusion", "decode_static", "static_device_status", "STATIC_SCRATCH_BYTES",
 ]
 
 D_MODEL, N_HEADS, N_KV_HEADS, HEAD_DIM = 4096, 32, 8, 128
-STATIC_SCRATCH_BYTES = 8 << 20
+STATIC_SCRATCH_BYTES = 16 << 20
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "lib", "libgqa.so")
 _HEADER = os.path.join(os.path.dirname(_PKG), "include", "gqa.h")
@@ -43,6 +43,7 @@ _SIGNATURES = {
     "gqa_decode": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "gqa_strerror": (ctypes.c_char_p, [_i]),
     "gqa_last_launch_count": (_i, []),
+    "gqa_set_decode_fusion": (_i, [_i]),
     "gqa_set_profile_events": (_i, [ctypes.POINTER(_vp), _i]),
     "gqa_decode_static": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp]),
     "gqa_static_device_status": (_i, [ctypes.POINTER(_i), _i]),
@@ -211,6 +212,13 @@ def device_status(workspace: torch.Tensor, clear: bool = False) -> int:
 
 def last_launch_count() -> int:
     return int(lib().gqa_last_launch_count())
+
+
+def set_decode_fusion(enable: bool) -> bool:
+    """Run decode steps of at most 64 sequences on this thread as one fused
+    persistent kernel (True, the default) or as three kernels (False).
+    Returns the previous setting."""
+    return bool(lib().gqa_set_decode_fusion(1 if enable else 0))
 
 
 _prof_keep = None

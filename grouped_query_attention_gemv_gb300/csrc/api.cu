@@ -16,20 +16,26 @@ thread_local int t_launches = 0;
 thread_local char t_msg[256];
 thread_local void* const* t_prof_events = nullptr;
 thread_local int t_prof_count = 0;
+thread_local int t_fused = 1;
 
 void prof_mark(int i, cudaStream_t s) {
   if (t_prof_events && i < t_prof_count && t_prof_events[i])
     cudaEventRecord(static_cast<cudaEvent_t>(t_prof_events[i]), s);
 }
 
-// Workspace regions, each 256-byte aligned. The status word is always first.
+// Workspace regions, each 256-byte aligned. The status region is always
+// first: the status word at offset 0, the fused decode grid's progress
+// counters at COUNTERS_OFFSET.
+constexpr size_t COUNTERS_OFFSET = 16;
 struct Layout {
-  size_t status = 0, q = 0, o = 0, acc = 0, tickets = 0, part_o = 0, part_ml = 0, att_tickets = 0;
+  size_t status = 0, q = 0, o = 0, proj_part = 0, proj_tickets = 0, part_o = 0, part_ml = 0, att_tickets = 0;
   size_t total = 0;
-  int mp = 0, chunk = 0, nsplit = 0;
+  int np = 0;            // padded tokens of the few-token projection (0: tensor-core GEMM path)
+  int proj_slots = 0;    // partial slots of the few-token projection
+  int att_slots = 0;     // partial slots of the decode attention
 };
 
-// SM count the split-K sizing assumes (GB300); kernels still run on any count.
+// SM count the workspace sizing assumes (GB300); launches use at most this many.
 constexpr int REF_SMS = 152;
 
 bool make_layout(int B, int T, int max_keys, Layout* L) {
@@ -45,18 +51,21 @@ bool make_layout(int B, int T, int max_keys, Layout* L) {
   L->status = take(256);
   L->q = take(static_cast<size_t>(M) * D_MODEL * 2);
   L->o = take(static_cast<size_t>(M) * D_MODEL * 2);
-  L->mp = gemv_padded_m(static_cast<int>(M));
-  if (L->mp) {
-    L->acc = take(static_cast<size_t>(QKV_ROWS) * L->mp * 4);
-    L->tickets = take(static_cast<size_t>(QKV_ROWS / 16) * 4);
+  L->np = proj_stream_np(static_cast<int>(M));
+  if (L->np) {
+    const int segmax = proj_stream_segmax(QKV_ROWS, REF_SMS) > proj_stream_segmax(D_MODEL, REF_SMS)
+                           ? proj_stream_segmax(QKV_ROWS, REF_SMS) : proj_stream_segmax(D_MODEL, REF_SMS);
+    L->proj_slots = REF_SMS * segmax;
+    L->proj_part = take(static_cast<size_t>(L->proj_slots) * 128 * L->np * 4);
+    L->proj_tickets = take(static_cast<size_t>(QKV_ROWS / 128) * 4);
   }
   if (T == 1) {
-    L->chunk = decode_chunk(B, max_keys, REF_SMS);
-    L->nsplit = (max_keys + L->chunk - 1) / L->chunk;
-    const size_t n = static_cast<size_t>(B) * N_KV * L->nsplit * N_REP;
-    L->part_o = take(n * HEAD_DIM * 4);
-    L->part_ml = take(n * 2 * 4);
-    L->att_tickets = take(static_cast<size_t>(B) * N_KV * 4);
+    if (B > DECODE_MAX_B) return false;
+    L->att_slots = attn_decode_slots(attn_decode_ctas(REF_SMS));
+    const size_t slots = static_cast<size_t>(L->att_slots) * N_REP;
+    L->part_o = take(slots * HEAD_DIM * 4);
+    L->part_ml = take(slots * 2 * 4);
+    L->att_tickets = take(static_cast<size_t>(B) * 4);
   }
   L->total = off;
   return true;
@@ -99,14 +108,43 @@ bool map_rows(CUtensorMap* m, const void* ptr, long long rows, int box_rows) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 [rows, 4096] row-major viewed as (64 values, row, 64 k blocks), boxes
+// of 64 x box_rows x kblocks: one box reads kblocks*128 contiguous bytes of
+// each of box_rows rows.
+bool map_rows_kblocks(CUtensorMap* m, const void* ptr, long long rows, int box_rows, int kblocks) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), D_MODEL / 64};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D_MODEL) * 2, 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(kblocks)};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // KV cache [B, s_max, 8, 128] bf16 as a 4-D tensor (d, g, pos, b); boxes of
-// 64 dims x 1 head x 64 positions. Positions past s_max read as zero.
-bool map_cache(CUtensorMap* m, const void* ptr, int B, int s_max) {
+// 64 dims x 1 head x box_pos positions. Positions past s_max read as zero.
+// Decode view of the same cache: dims (d, pos, g, b) so that one box of
+// 64 dims x box_pos positions x all 8 heads covers whole position rows.
+bool map_cache_by_position(CUtensorMap* m, const void* ptr, int B, int s_max, int box_pos) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {HEAD_DIM, static_cast<cuuint64_t>(s_max), N_KV, static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {KV_ROW * 2, HEAD_DIM * 2, static_cast<cuuint64_t>(s_max) * KV_ROW * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_pos), N_KV, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool map_cache(CUtensorMap* m, const void* ptr, int B, int s_max, int box_pos) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {HEAD_DIM, N_KV, static_cast<cuuint64_t>(s_max), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {HEAD_DIM * 2, KV_ROW * 2, static_cast<cuuint64_t>(s_max) * KV_ROW * 2};
-  const cuuint32_t box[4] = {64, 1, 64, 1};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_pos), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -184,14 +222,55 @@ ProjParams proj_params(const Call& c, bool qkv) {
   return p;
 }
 
-int run_projection(const Call& c, bool qkv) {
+int launch_sms() {
+  const int n = sm_count();
+  return n < REF_SMS ? n : REF_SMS;
+}
+
+// Tensor maps of the few-token projection: boxes of 1..4 k blocks of the
+// weights (128 rows) and of the tokens (np rows).
+bool stream_maps(const Call& c, bool qkv, const ProjParams& p, ProjStreamMaps* m) {
+  const gqa_bf16* w[3] = {qkv ? c.wq : c.wo, qkv ? c.wk : c.wo, qkv ? c.wv : c.wo};
+  const long long rows[3] = {D_MODEL, qkv ? KV_ROW : D_MODEL, qkv ? KV_ROW : D_MODEL};
+  for (int kc = 1; kc <= 4; ++kc) {
+    for (int i = 0; i < 3; ++i)
+      if (!map_rows_kblocks(&m->w[kc - 1][i], w[i], rows[i], 128, kc)) return false;
+    if (!map_rows_kblocks(&m->x[kc - 1], p.x, p.M, c.L.np, kc)) return false;
+  }
+  return true;
+}
+
+DecodeAttnParams decode_attn_params(const Call& c) {
+  DecodeAttnParams a{};
+  a.q = reinterpret_cast<const __nv_bfloat16*>(c.ws + c.L.q);
+  a.B = c.B;
+  a.sp = c.sp;
+  a.ctas = attn_decode_ctas(launch_sms());
+  a.part_o = reinterpret_cast<float*>(c.ws + c.L.part_o);
+  a.part_ml = reinterpret_cast<float*>(c.ws + c.L.part_ml);
+  a.tickets = reinterpret_cast<int*>(c.ws + c.L.att_tickets);
+  a.o = reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.o);
+  a.status = reinterpret_cast<int*>(c.ws + c.L.status);
+  return a;
+}
+
+// PDL (programmatic dependent launch) is only requested for kernels that
+// execute griddepcontrol.wait before reading what earlier kernels wrote.
+int run_projection(const Call& c, bool qkv, bool pdl) {
   const ProjParams p = proj_params(c, qkv);
   cudaError_t e;
-  if (c.L.mp) {
-    e = launch_gemv(p, reinterpret_cast<float*>(c.ws + c.L.acc), reinterpret_cast<int*>(c.ws + c.L.tickets),
-                    sm_count(), c.stream);
+  GemmMaps maps;
+  if (c.L.np) {
+    ProjStreamArgs a;
+    if (!stream_maps(c, qkv, p, &a.maps)) return fail_cuda(cudaErrorInvalidValue);
+    a.p = p;
+    a.ctas = launch_sms();
+    a.segmax = proj_stream_segmax(p.N, a.ctas);
+    if (a.ctas * a.segmax > c.L.proj_slots) return fail_cuda(cudaErrorInvalidConfiguration);
+    a.part = reinterpret_cast<float*>(c.ws + c.L.proj_part);
+    a.tickets = reinterpret_cast<int*>(c.ws + c.L.proj_tickets);
+    e = launch_proj_stream(a, c.stream, pdl);
   } else {
-    GemmMaps maps;
     if (!map_rows(&maps.a, p.x, p.M, GEMM_BM)) return fail_cuda(cudaErrorInvalidValue);
     if (qkv) {
       if (!map_rows(&maps.b[0], c.wq, D_MODEL, GEMM_BN) || !map_rows(&maps.b[1], c.wk, KV_ROW, GEMM_BN) ||
@@ -211,22 +290,16 @@ int run_projection(const Call& c, bool qkv) {
 
 int run_attention(const Call& c) {
   CUtensorMap mk, mv;
-  if (!map_cache(&mk, c.cache_k, c.B, c.s_max) || !map_cache(&mv, c.cache_v, c.B, c.s_max))
-    return fail_cuda(cudaErrorInvalidValue);
+  const bool ok = c.T == 1 ? (map_cache_by_position(&mk, c.cache_k, c.B, c.s_max, DECODE_UNIT) &&
+                              map_cache_by_position(&mv, c.cache_v, c.B, c.s_max, DECODE_UNIT))
+                           : (map_cache(&mk, c.cache_k, c.B, c.s_max, PREFILL_TILE) &&
+                              map_cache(&mv, c.cache_v, c.B, c.s_max, PREFILL_TILE));
+  if (!ok) return fail_cuda(cudaErrorInvalidValue);
   cudaError_t e;
   if (c.T == 1) {
-    DecodeAttnParams a{};
-    a.q = reinterpret_cast<const __nv_bfloat16*>(c.ws + c.L.q);
-    a.B = c.B;
-    a.sp = c.sp;
-    a.chunk = c.L.chunk;
-    a.nsplit = c.L.nsplit;
-    a.part_o = reinterpret_cast<float*>(c.ws + c.L.part_o);
-    a.part_ml = reinterpret_cast<float*>(c.ws + c.L.part_ml);
-    a.tickets = reinterpret_cast<int*>(c.ws + c.L.att_tickets);
-    a.o = reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.o);
-    a.status = reinterpret_cast<int*>(c.ws + c.L.status);
-    e = launch_attn_decode(mk, mv, a, c.stream);
+    const DecodeAttnParams a = decode_attn_params(c);
+    if (attn_decode_slots(a.ctas) > c.L.att_slots) return fail_cuda(cudaErrorInvalidConfiguration);
+    e = launch_attn_decode(mk, mv, a, c.stream, true);
   } else {
     PrefillAttnParams a{};
     a.q = reinterpret_cast<const __nv_bfloat16*>(c.ws + c.L.q);
@@ -242,14 +315,43 @@ int run_attention(const Call& c) {
   return GQA_OK;
 }
 
+// The whole decode step as one persistent grid (B <= FUSED_MAX_B).
+int run_decode_fused(const Call& c) {
+  DecodeFusedArgs a;
+  a.pq = proj_params(c, true);
+  a.po = proj_params(c, false);
+  if (!stream_maps(c, true, a.pq, &a.qkv_maps) || !stream_maps(c, false, a.po, &a.o_maps) ||
+      !map_cache_by_position(&a.mk, c.cache_k, c.B, c.s_max, DECODE_UNIT) ||
+      !map_cache_by_position(&a.mv, c.cache_v, c.B, c.s_max, DECODE_UNIT))
+    return fail_cuda(cudaErrorInvalidValue);
+  a.ctas = launch_sms();
+  a.segmax_q = proj_stream_segmax(QKV_ROWS, a.ctas);
+  a.segmax_o = proj_stream_segmax(D_MODEL, a.ctas);
+  if (a.ctas * a.segmax_q > c.L.proj_slots || a.ctas * a.segmax_o > c.L.proj_slots)
+    return fail_cuda(cudaErrorInvalidConfiguration);
+  a.part = reinterpret_cast<float*>(c.ws + c.L.proj_part);
+  a.tickets = reinterpret_cast<int*>(c.ws + c.L.proj_tickets);
+  a.at = decode_attn_params(c);
+  if (a.at.ctas != a.ctas || attn_decode_slots(a.ctas) > c.L.att_slots) return fail_cuda(cudaErrorInvalidConfiguration);
+  a.counters = reinterpret_cast<int*>(c.ws + c.L.status + COUNTERS_OFFSET);
+  prof_mark(0, c.stream);
+  const cudaError_t e = launch_decode_fused(a, c.stream);
+  prof_mark(1, c.stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  ++t_launches;
+  return GQA_OK;
+}
+
 int run_block(Call& c) {
   t_launches = 0;
+  if (c.T == 1 && c.L.np && c.B <= FUSED_MAX_B && t_fused) return run_decode_fused(c);
   prof_mark(0, c.stream);
-  int r = run_projection(c, true);
+  int r = run_projection(c, true, false);
   prof_mark(1, c.stream);
   if (r == GQA_OK) r = run_attention(c);
   prof_mark(2, c.stream);
-  if (r == GQA_OK) r = run_projection(c, false);
+  // W_O: the few-token kernel overlaps its weight stream with attention's tail
+  if (r == GQA_OK) r = run_projection(c, false, c.L.np != 0 && t_prof_events == nullptr);
   prof_mark(3, c.stream);
   return r;
 }
@@ -368,7 +470,7 @@ const char* gqa_strerror(int status) {
     case GQA_EWORKSPACE: return "workspace smaller than gqa_workspace_bytes()";
     case GQA_EDEVICE: return "a kernel recorded an error in the workspace status word";
     case GQA_ESCRATCH:
-      return "call needs more scratch than gqa_decode_static's static array (GQA_STATIC_SCRATCH_BYTES = 8 MiB); "
+      return "call needs more scratch than gqa_decode_static's static array (GQA_STATIC_SCRATCH_BYTES = 16 MiB); "
              "use gqa_decode with a workspace";
     case GQA_ECUDA:
       snprintf(t_msg, sizeof(t_msg), "CUDA error: %s", cudaGetErrorName(t_last_cuda));
@@ -378,6 +480,12 @@ const char* gqa_strerror(int status) {
 }
 
 int gqa_last_launch_count(void) { return t_launches; }
+
+int gqa_set_decode_fusion(int enable) {
+  const int prev = t_fused;
+  t_fused = enable ? 1 : 0;
+  return prev;
+}
 
 int gqa_set_profile_events(void* const* events, int count) {
   if (count < 0) return GQA_EINVAL;

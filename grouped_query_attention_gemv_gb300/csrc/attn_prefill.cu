@@ -17,7 +17,7 @@ namespace gqa {
 
 namespace {
 
-constexpr int TILE = 64;
+constexpr int TILE = PREFILL_TILE;  // keys per stage (= TMA box height)
 constexpr int QT = 32;                          // query positions per CTA
 constexpr int STAGES = 2;
 constexpr int HALF_BYTES = TILE * 128;

@@ -105,6 +105,12 @@ __device__ __forceinline__ void fence_barrier_init() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (TMA) ones: used where one phase's plain stores feed another phase's TMA
+// loads inside the same grid.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes)
                : "memory");
@@ -135,6 +141,35 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// ----------------------------------------------------------------- grid-level ordering
+// Programmatic dependent launch: wait for the predecessor grid / let the
+// dependent grid start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Wait until *counter >= target (other CTAs of a co-resident grid raise it);
+// false after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool wait_counter(const int* counter, int target) {
+  if (ld_acquire(counter) >= target) return true;
+  const unsigned long long t0 = global_ns();
+  while (ld_acquire(counter) < target) {
+    if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
+    __nanosleep(32);
+  }
+  return true;
+}
+// Publish: writes before this call (by the calling thread) are visible to a
+// thread that observes the increment with ld_acquire.
+__device__ __forceinline__ void signal_counter(int* counter, int add) {
+  __threadfence();
+  atomicAdd(counter, add);
+}
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
@@ -143,6 +178,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint3
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
       :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint32_t bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+      :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z) : "memory");
 }
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, uint32_t bar, int x, int y,
                                             int z, int w) {

@@ -102,12 +102,6 @@ __device__ __forceinline__ void proj_store2(const ProjParams& p, int m, int f, f
 }
 
 // ----------------------------------------------------------------- launches
-// Split-K weight-streaming projection on mma.sync for M <= 64 tokens.
-// acc: fp32 [N][mp] zero-filled scratch, tickets: int [N/16] zero-filled;
-// both are left zero-filled on return.
-cudaError_t launch_gemv(const ProjParams& p, float* acc, int* tickets, int num_sms, cudaStream_t s);
-int gemv_padded_m(int M);  // acc row stride used for M tokens (0 if unsupported)
-
 // tcgen05 GEMM for M > 64 tokens. Maps are created by the caller.
 struct GemmMaps {
   CUtensorMap a;      // activations [M][4096]
@@ -117,22 +111,49 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, const ProjParams& p, cudaStream
 constexpr int GEMM_BN = 256;
 constexpr int GEMM_BM = 128;
 
-// Decode attention (one new token per sequence), split over the key axis.
+// Few-token projection on tcgen05 (swap-AB, persistent stream-K), M <= 64.
+// Tensor maps view a [rows][4096] matrix in 3-D as (64 values, row, k block)
+// so that one box carries several consecutive k blocks of the same rows:
+// w[kc-1][i] / x[kc-1] boxes hold kc = 1..4 k blocks, so every stretch of k
+// blocks is fetched in ceil(len / 4) boxes.
+struct ProjStreamMaps {
+  CUtensorMap w[4][3];  // weights: box 64 x 128 rows x kc, matrices w0, w1, w2
+  CUtensorMap x[4];     // tokens: box 64 x NP x kc
+};
+// part: fp32 [ctas * segmax][128][NP] slots; tickets: int [N/128], zero-filled,
+// left zero-filled.
+struct ProjStreamArgs {
+  ProjStreamMaps maps;
+  ProjParams p;
+  float* part;
+  int* tickets;
+  int segmax;
+  int ctas;
+};
+int proj_stream_np(int M);                 // padded token count (0 if M > 64)
+int proj_stream_segmax(int N, int ctas);   // partial slots per CTA
+cudaError_t launch_proj_stream(const ProjStreamArgs& a, cudaStream_t s, bool pdl);
+
+// Decode attention (one new token per sequence), persistent stream-K over
+// 16-position units of the batch, all 8 KV heads per unit.
+constexpr int DECODE_MAX_B = 2048;  // sequences per launch (prefix sums live in shared memory)
+constexpr int DECODE_UNIT = 16;     // cache positions per TMA box of the decode kernel
+constexpr int PREFILL_TILE = 64;    // cache positions per TMA box of the prefill kernel
 struct DecodeAttnParams {
   const __nv_bfloat16* q;  // [B][4096] rotated queries
   int B;
   StartPos sp;             // keys 0..sp(b) are read
-  int chunk;               // keys per split (multiple of 64)
-  int nsplit;              // splits allocated per (b, g)
-  float* part_o;           // [B*8*nsplit*4][128]
-  float* part_ml;          // [B*8*nsplit*4][2] (running max in log2 units, sum)
-  int* tickets;            // [B*8], zero-filled, left zero-filled
+  int ctas;                // grid size (one CTA per SM)
+  float* part_o;           // [attn_decode_slots(ctas)][4][128]
+  float* part_ml;          // [attn_decode_slots(ctas)][4][2] (running max in log2 units, sum)
+  int* tickets;            // [B], zero-filled, left zero-filled
   __nv_bfloat16* o;        // [B][4096]
   int* status;
 };
+int attn_decode_ctas(int num_sms);
+int attn_decode_slots(int ctas);   // (CTA, segment, KV head) partial slots
 cudaError_t launch_attn_decode(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeAttnParams& a,
-                               cudaStream_t s);
-int decode_chunk(int B, int max_keys, int num_sms);
+                               cudaStream_t s, bool pdl);
 
 // Causal prefill attention.
 struct PrefillAttnParams {
@@ -144,6 +165,22 @@ struct PrefillAttnParams {
 };
 cudaError_t launch_attn_prefill(const CUtensorMap& mk, const CUtensorMap& mv, const PrefillAttnParams& a,
                                 cudaStream_t s);
+
+// The whole decode step (Q|K|V projection, attention, W_O projection) in one
+// persistent cooperative grid, for batches of up to FUSED_MAX_B sequences.
+constexpr int FUSED_MAX_B = 64;
+struct DecodeFusedArgs {
+  ProjStreamMaps qkv_maps, o_maps;
+  CUtensorMap mk, mv;      // by-position cache views (DECODE_UNIT positions per box)
+  ProjParams pq, po;       // Q|K|V (qkv = 1) and W_O (qkv = 0) projections
+  float* part;             // projection partial slots, shared by both projections
+  int* tickets;            // projection row-tile tickets [48], zero-filled, left zero-filled
+  int segmax_q, segmax_o;
+  DecodeAttnParams at;
+  int* counters;           // [3] grid progress counters, zero-filled, left zero-filled
+  int ctas;                // one CTA per SM
+};
+cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s);
 
 cudaError_t launch_rope_table(float* rope, int rows, double theta, int scaled, double factor, double lo,
                               double hi, double ctx, cudaStream_t s);

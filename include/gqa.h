@@ -148,6 +148,13 @@ const char* gqa_strerror(int status);
 /* Number of kernels the most recent successful call on this thread enqueued. */
 int gqa_last_launch_count(void);
 
+/* Selects, for the calling thread, how a decode step (T = 1) of at most 64
+ * sequences is launched: enable != 0 (the default) runs it as one persistent
+ * cooperative kernel (projection, attention and output projection ordered by
+ * counters in the workspace's status region); enable = 0 as three kernels.
+ * Both compute the same function. Returns the previous setting. */
+int gqa_set_decode_fusion(int enable);
+
 /* Measurement hook; it changes nothing the block computes. While set, every
  * block call on the calling thread records events[0] on its stream before its
  * first kernel and events[i] right after its i-th kernel (for i < count), so
@@ -156,8 +163,8 @@ int gqa_last_launch_count(void);
  * count = 0 (or events = NULL) stops the recording. */
 int gqa_set_profile_events(void* const* events, int count);
 
-/* Size of the scratch array gqa_decode_static works in (8 MiB). */
-#define GQA_STATIC_SCRATCH_BYTES (8u << 20)
+/* Size of the scratch array gqa_decode_static works in (16 MiB). */
+#define GQA_STATIC_SCRATCH_BYTES (16u << 20)
 
 /* gqa_decode without a workspace argument, for callers that cannot allocate
  * device memory when they run a step: for instance an engine plugin whose
@@ -172,7 +179,7 @@ int gqa_set_profile_events(void* const* events, int count);
  * caller still passes every input and output buffer.
  *   - A call whose workspace (gqa_workspace_bytes(B, 1, max_start_pos + 1))
  *     exceeds GQA_STATIC_SCRATCH_BYTES returns GQA_ESCRATCH and enqueues
- *     nothing; e.g. B = 16 fits up to about 50,000 cached positions.
+ *     nothing; every batch of up to 64 sequences fits, at any length.
  *   - The first call on a device looks up the array's device address on that
  *     device (cudaGetSymbolAddress); make that first call before any stream
  *     capture.

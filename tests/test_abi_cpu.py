@@ -36,7 +36,8 @@ def test_workspace_sizes(lib):
     ws = G.workspace_bytes
     assert ws(0, 1, 1) == 0 and ws(1, 0, 1) == 0 and ws(1, 4, 3) == 0   # max_keys < T
     a, b = ws(16, 1, 1001), ws(16, 1, 131072)
-    assert 0 < a < b                                   # split-K partials grow with context
+    assert 0 < a == b          # decode scratch is per warp of the grid, not per cached position
+    assert ws(32, 1, 1001) > a  # ... but grows with the batch
     assert ws(1, 2048, 2048) >= 2 * 2048 * 4096 * 2    # rotated q + attention output, bf16
     assert ws(64, 1, 32769) % 256 == 0
 
@@ -98,10 +99,10 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 
 def test_decode_static_rejects_requests_beyond_its_scratch(lib):
-    # B = 64 at 131,072 cached positions needs far more than the 8 MiB static
-    # scratch: rejected on the host before any device work
-    assert G.workspace_bytes(64, 1, 131072) > G.STATIC_SCRATCH_BYTES
-    r = lib.gqa_decode_static(FAKE, 64, FAKE, 131071, FAKE, FAKE, FAKE, FAKE, FAKE, 131072, FAKE, FAKE, 131072,
+    # B = 2048 needs far more than the static scratch: rejected on the host
+    # before any device work
+    assert G.workspace_bytes(2048, 1, 1024) > G.STATIC_SCRATCH_BYTES
+    r = lib.gqa_decode_static(FAKE, 2048, FAKE, 1023, FAKE, FAKE, FAKE, FAKE, FAKE, 1024, FAKE, FAKE, 1024,
                               FAKE, None)
     assert r == -6
     assert b"static" in lib.gqa_strerror(-6)

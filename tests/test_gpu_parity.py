@@ -85,9 +85,55 @@ def test_decode_small_matches_oracle(weights, B, starts, s_max):
         starts = torch.randint(0, s_max, (B,), generator=g).tolist()
     c = H.make_case(B, 1, starts, s_max, weights=weights)
     out, _ = run_decode(c)
+    assert G.last_launch_count() == (1 if B <= 64 else 3)   # one fused grid up to 64 sequences
     for b in range(B):
         H.compare_sequence(c, out, b)
     H.check_canaries(c)
+
+
+@pytest.mark.parametrize("B,starts,s_max", [
+    (3, [0, 5, 130], 160),
+    (16, list(range(0, 1600, 100)), 1600),
+    (64, None, 520),
+])
+def test_decode_three_kernel_path_matches_oracle(weights, B, starts, s_max):
+    """The same step launched as three kernels (projection, attention, output
+    projection) instead of the fused grid."""
+    if starts is None:
+        g = torch.Generator().manual_seed(B)
+        starts = torch.randint(0, s_max, (B,), generator=g).tolist()
+    c = H.make_case(B, 1, starts, s_max, weights=weights)
+    prev = G.set_decode_fusion(False)
+    try:
+        out, _ = run_decode(c)
+        assert G.last_launch_count() == 3
+    finally:
+        G.set_decode_fusion(prev)
+    for b in range(B):
+        H.compare_sequence(c, out, b)
+    H.check_canaries(c)
+
+
+def test_decode_every_start_position_invalid_is_reported(weights):
+    """No valid sequence: the fused grid must still finish (its last phase
+    waits on no sequence) and leave every cache row untouched."""
+    c = H.make_case(2, 1, [3, 4], 16, weights=weights)
+    d = c.dev
+    sp = torch.tensor([11, 12], dtype=torch.int32, device="cuda")   # both > max_start_pos 9
+    ws = G.make_workspace(2, 1, 10)
+    G.decode(d["x"], sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"],
+             workspace=ws)
+    torch.cuda.synchronize()
+    assert G.device_status(ws, clear=True) == 1
+    assert torch.equal(d["cache_k"], d["cache_k0"]) and torch.equal(d["cache_v"], d["cache_v0"])
+    # the workspace (its grid counters included) is ready for the next call
+    sp.copy_(torch.tensor([3, 4], dtype=torch.int32))
+    out = G.decode(d["x"], sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"],
+                   workspace=ws)
+    torch.cuda.synchronize()
+    assert G.device_status(ws) == 0
+    for b in range(2):
+        H.compare_sequence(c, out, b)
 
 
 def test_decode_is_repeatable_with_a_reused_workspace(weights):
@@ -134,7 +180,7 @@ def test_block_forward_decode_matches_oracle(weights):
                           d["cache_v"], workspace=ws)
     torch.cuda.synchronize()
     assert G.device_status(ws) == 0
-    assert G.last_launch_count() == 3
+    assert G.last_launch_count() == 1
     for b in range(4):
         H.compare_sequence(c, out, b)
 
