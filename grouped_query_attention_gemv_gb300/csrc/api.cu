@@ -28,7 +28,7 @@ void prof_mark(int i, cudaStream_t s) {
 // counters at COUNTERS_OFFSET.
 constexpr size_t COUNTERS_OFFSET = 16;
 struct Layout {
-  size_t status = 0, q = 0, o = 0, proj_part = 0, proj_tickets = 0, part_o = 0, part_ml = 0, att_tickets = 0;
+  size_t status = 0, q = 0, o = 0, proj_part = 0, proj_tickets = 0, part_o = 0, part_ml = 0;
   size_t total = 0;
   int np = 0;            // padded tokens of the few-token projection (0: tensor-core GEMM path)
   int proj_slots = 0;    // partial slots of the few-token projection
@@ -65,7 +65,6 @@ bool make_layout(int B, int T, int max_keys, Layout* L) {
     const size_t slots = static_cast<size_t>(L->att_slots) * N_REP;
     L->part_o = take(slots * HEAD_DIM * 4);
     L->part_ml = take(slots * 2 * 4);
-    L->att_tickets = take(static_cast<size_t>(B) * 4);
   }
   L->total = off;
   return true;
@@ -123,10 +122,9 @@ bool map_rows_kblocks(CUtensorMap* m, const void* ptr, long long rows, int box_r
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// KV cache [B, s_max, 8, 128] bf16 as a 4-D tensor (d, g, pos, b); boxes of
-// 64 dims x 1 head x box_pos positions. Positions past s_max read as zero.
-// Decode view of the same cache: dims (d, pos, g, b) so that one box of
-// 64 dims x box_pos positions x all 8 heads covers whole position rows.
+// Decode view of the KV cache [B, s_max, 8, 128] bf16: dims (d, pos, g, b) so
+// that one box of 64 dims x box_pos positions x all 8 heads covers whole
+// position rows. Positions past s_max read as zero.
 bool map_cache_by_position(CUtensorMap* m, const void* ptr, int B, int s_max, int box_pos) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
@@ -139,6 +137,8 @@ bool map_cache_by_position(CUtensorMap* m, const void* ptr, int B, int s_max, in
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// KV cache [B, s_max, 8, 128] bf16 as a 4-D tensor (d, g, pos, b); boxes of
+// 64 dims x 1 head x box_pos positions. Positions past s_max read as zero.
 bool map_cache(CUtensorMap* m, const void* ptr, int B, int s_max, int box_pos) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
@@ -248,10 +248,18 @@ DecodeAttnParams decode_attn_params(const Call& c) {
   a.ctas = attn_decode_ctas(launch_sms());
   a.part_o = reinterpret_cast<float*>(c.ws + c.L.part_o);
   a.part_ml = reinterpret_cast<float*>(c.ws + c.L.part_ml);
-  a.tickets = reinterpret_cast<int*>(c.ws + c.L.att_tickets);
+  a.counters = reinterpret_cast<int*>(c.ws + c.L.status + COUNTERS_OFFSET);
   a.o = reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.o);
   a.status = reinterpret_cast<int*>(c.ws + c.L.status);
+  a.cache_k = reinterpret_cast<const __nv_bfloat16*>(c.cache_k);
+  a.cache_v = reinterpret_cast<const __nv_bfloat16*>(c.cache_v);
+  a.s_max = c.s_max;
   return a;
+}
+
+bool decode_cache_maps(const Call& c, DecodeCacheMaps* m) {
+  return map_cache_by_position(&m->k, c.cache_k, c.B, c.s_max, DECODE_UNIT) &&
+         map_cache_by_position(&m->v, c.cache_v, c.B, c.s_max, DECODE_UNIT);
 }
 
 // PDL (programmatic dependent launch) is only requested for kernels that
@@ -289,18 +297,17 @@ int run_projection(const Call& c, bool qkv, bool pdl) {
 }
 
 int run_attention(const Call& c) {
-  CUtensorMap mk, mv;
-  const bool ok = c.T == 1 ? (map_cache_by_position(&mk, c.cache_k, c.B, c.s_max, DECODE_UNIT) &&
-                              map_cache_by_position(&mv, c.cache_v, c.B, c.s_max, DECODE_UNIT))
-                           : (map_cache(&mk, c.cache_k, c.B, c.s_max, PREFILL_TILE) &&
-                              map_cache(&mv, c.cache_v, c.B, c.s_max, PREFILL_TILE));
-  if (!ok) return fail_cuda(cudaErrorInvalidValue);
   cudaError_t e;
   if (c.T == 1) {
+    DecodeCacheMaps maps;
+    if (!decode_cache_maps(c, &maps)) return fail_cuda(cudaErrorInvalidValue);
     const DecodeAttnParams a = decode_attn_params(c);
     if (attn_decode_slots(a.ctas) > c.L.att_slots) return fail_cuda(cudaErrorInvalidConfiguration);
-    e = launch_attn_decode(mk, mv, a, c.stream, true);
+    e = launch_attn_decode(maps, a, c.stream);
   } else {
+    CUtensorMap mk, mv;
+    if (!map_cache(&mk, c.cache_k, c.B, c.s_max, PREFILL_TILE) || !map_cache(&mv, c.cache_v, c.B, c.s_max, PREFILL_TILE))
+      return fail_cuda(cudaErrorInvalidValue);
     PrefillAttnParams a{};
     a.q = reinterpret_cast<const __nv_bfloat16*>(c.ws + c.L.q);
     a.B = c.B;
@@ -315,22 +322,34 @@ int run_attention(const Call& c) {
   return GQA_OK;
 }
 
-// The whole decode step as one persistent grid (B <= FUSED_MAX_B).
+// Tensor maps of a row-owner projection: per matrix, boxes of its two row counts.
+bool row_maps(const gqa_bf16* const* w, const RowPlan& plan, const void* x, int M, int np, RowMaps* m) {
+  for (int i = 0; i < 3; ++i) {
+    const int mi = i < plan.nmat ? i : 0;
+    for (int hi = 0; hi < 2; ++hi)
+      if (!map_rows_kblocks(&m->w[i][hi], w[mi], plan.rows[mi], plan.h_lo[mi] + 2 * hi, 4)) return false;
+  }
+  return map_rows_kblocks(&m->x, x, M, np, 4);
+}
+
+// The whole decode step as one persistent grid (B <= FUSED_MAX_B). Returns
+// GQA_EINVAL without launching anything when this GPU cannot run it (too few
+// SMs for the row split); the caller then takes the three-kernel path.
 int run_decode_fused(const Call& c) {
   DecodeFusedArgs a;
+  a.ctas = launch_sms();
+  const int qkv_rows[3] = {D_MODEL, KV_ROW, KV_ROW};
+  const int o_rows[1] = {D_MODEL};
+  if (!make_row_plan(3, qkv_rows, a.ctas, &a.qkv_plan) || !make_row_plan(1, o_rows, a.ctas, &a.o_plan))
+    return GQA_EINVAL;
   a.pq = proj_params(c, true);
   a.po = proj_params(c, false);
-  if (!stream_maps(c, true, a.pq, &a.qkv_maps) || !stream_maps(c, false, a.po, &a.o_maps) ||
-      !map_cache_by_position(&a.mk, c.cache_k, c.B, c.s_max, DECODE_UNIT) ||
-      !map_cache_by_position(&a.mv, c.cache_v, c.B, c.s_max, DECODE_UNIT))
+  const gqa_bf16* wqkv[3] = {c.wq, c.wk, c.wv};
+  const gqa_bf16* wo[1] = {c.wo};
+  if (!row_maps(wqkv, a.qkv_plan, a.pq.x, a.pq.M, c.L.np, &a.qkv_maps) ||
+      !row_maps(wo, a.o_plan, a.po.x, a.po.M, c.L.np, &a.o_maps) ||
+      !decode_cache_maps(c, &a.cache))
     return fail_cuda(cudaErrorInvalidValue);
-  a.ctas = launch_sms();
-  a.segmax_q = proj_stream_segmax(QKV_ROWS, a.ctas);
-  a.segmax_o = proj_stream_segmax(D_MODEL, a.ctas);
-  if (a.ctas * a.segmax_q > c.L.proj_slots || a.ctas * a.segmax_o > c.L.proj_slots)
-    return fail_cuda(cudaErrorInvalidConfiguration);
-  a.part = reinterpret_cast<float*>(c.ws + c.L.proj_part);
-  a.tickets = reinterpret_cast<int*>(c.ws + c.L.proj_tickets);
   a.at = decode_attn_params(c);
   if (a.at.ctas != a.ctas || attn_decode_slots(a.ctas) > c.L.att_slots) return fail_cuda(cudaErrorInvalidConfiguration);
   a.counters = reinterpret_cast<int*>(c.ws + c.L.status + COUNTERS_OFFSET);
@@ -344,7 +363,10 @@ int run_decode_fused(const Call& c) {
 
 int run_block(Call& c) {
   t_launches = 0;
-  if (c.T == 1 && c.L.np && c.B <= FUSED_MAX_B && t_fused) return run_decode_fused(c);
+  if (c.T == 1 && c.L.np && c.B <= FUSED_MAX_B && t_fused) {
+    const int r = run_decode_fused(c);
+    if (r != GQA_EINVAL) return r;
+  }
   prof_mark(0, c.stream);
   int r = run_projection(c, true, false);
   prof_mark(1, c.stream);

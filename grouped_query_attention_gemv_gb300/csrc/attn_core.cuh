@@ -10,21 +10,27 @@
 //
 // Work decomposition (persistent, stream-K over position chunks):
 //   * the cache rows of every sequence are cut into 16-position units; all
-//     units of the batch, in (b, chunk) order, are split into equal contiguous
-//     ranges, one per CTA (one CTA per SM), so every SM streams the same bytes
-//     whatever the mix of sequence lengths;
-//   * a producer warp fetches each unit for all 8 KV heads at once: a TMA box
-//     of 16 positions x 8 heads x 64 dims over a transposed view of the cache
-//     (K and V, two halves each: 64 KB per unit, 3-stage mbarrier ring), so
-//     every 2 KB position row is read in one burst;
-//   * compute warp g (of 8) owns KV head g: QK^T and PV on mma.sync m16n8k16
-//     with its 4 query heads as the (zero-padded) M = 16 rows, online softmax
-//     in fp32 (base-2, scale folded in);
+//     units of the batch, in (sequence, chunk) order, are split into equal
+//     contiguous ranges, one per CTA (one CTA per SM), so every SM streams
+//     the same bytes whatever the mix of sequence lengths;
+//   * a producer lane fetches each unit for all 8 KV heads at once: TMA boxes
+//     of 16 positions x 8 heads x 64 dims over a (dim, position, head,
+//     sequence) view of the cache, K and V in two halves each (64 KB per
+//     unit, 3 units in flight), so every 2 KB position row is read whole;
+//   * compute warp g (of 8) owns KV head g. Its 16 keys go on the M side of
+//     mma.sync m16n8k16 and its 4 query heads (padded to 8) on the N side:
+//     S^T = K Q^T, online softmax per head in fp32 (base 2, scale folded in),
+//     O^T += V^T P^T with P^T moved into B-operand layout by movmatrix: half
+//     the tensor instructions of the query-rows-as-M form, whose 16 rows
+//     would hold 4 heads;
 //   * a sequence wholly inside one CTA's range is finished in registers; one
-//     split between CTAs leaves fp32 partials (max, sum, o) in two slots per
-//     CTA, and the CTA whose ticket completes the sequence merges them with
-//     the log-sum-exp rule in CTA order (deterministic). Nothing waits on
-//     another CTA;
+//     split between CTAs leaves an fp32 partial (running max, sum, o) in one
+//     of the CTA's two slots;
+//   * after every CTA's last unit the grid meets once (a counter), and every
+//     warp of the grid merges one (sequence, query head) of the split
+//     sequences over its slots by the log-sum-exp rule, in CTA order
+//     (deterministic). All slot loads of a merge are issued together, so the
+//     merge costs one round trip however many CTAs shared the sequence;
 //   * units are requested before `gate` (the queries and the new rows may
 //     still be in the making) except a sequence's last unit, which holds the
 //     row the projection writes; queries are read after it.
@@ -37,14 +43,16 @@
 namespace gqa {
 namespace attnk {
 
-constexpr int UNIT = DECODE_UNIT;              // positions per unit (= TMA box height)
+constexpr int UNIT = DECODE_UNIT;             // positions per unit
+constexpr int COMPUTE_WARPS = N_KV;           // warps 0..7 (KV head = warp); warp 8 lane 0 produces
 constexpr int STAGES = 3;
-constexpr int BOX_BYTES = UNIT * N_KV * 128;   // 16 positions x 8 heads x 64 dims x bf16 = 16 KB
-constexpr int UNIT_BYTES = 4 * BOX_BYTES;      // K lo | K hi | V lo | V hi
+constexpr int HEAD_BYTES = UNIT * 128;        // one head's 16 positions x 64 dims
+constexpr int BOX_BYTES = N_KV * HEAD_BYTES;  // 16 positions x 8 heads x 64 dims = 16 KB
+constexpr int UNIT_BYTES = 4 * BOX_BYTES;     // K lo | K hi | V lo | V hi
 constexpr int RING = STAGES * UNIT_BYTES;
-constexpr int HEAD_BYTES = UNIT * 128;         // one head's slice of a box
-constexpr int COMPUTE_WARPS = N_KV;            // warps 0..7; warp 8 is the producer
+constexpr int STAGE_OUT_BYTES = COMPUTE_WARPS * N_REP * HEAD_DIM * 4;  // per-warp o staging
 constexpr float SCALE_LOG2 = 0.08838834764831845f * 1.4426950408889634f;
+constexpr int MERGE_SLOTS = 16;               // slots whose loads are in flight together in a merge
 
 struct Cursor {
   int b, j;  // sequence, unit within it
@@ -112,22 +120,43 @@ __device__ __forceinline__ bool compute_all(bool v) {
 }
 
 struct Shared {
-  uint8_t* ring;    // RING bytes, 1024-aligned
-  uint64_t* full;   // [STAGES], count 1
-  uint64_t* empty;  // [STAGES], count COMPUTE_WARPS
-  int* flags;       // [0] abort, [1] ticket, [2] issued
-  const int* pre;   // [B + 1] from build_prefix
+  uint8_t* ring;     // RING bytes, 1024-aligned
+  uint64_t* full;    // [STAGES], count 1
+  uint64_t* empty;   // [STAGES], count COMPUTE_WARPS
+  int* flags;        // [0] abort, [2] units issued
+  const int* pre;    // [B + 1] from build_prefix
+  float* stage_out;  // STAGE_OUT_BYTES
 };
 
-// This CTA's range of units. Roles: warps 0..7 compute (KV head = warp), warp 8
-// lane 0 produces. gate_lane() is called by the producer lane before the units
-// that need the projection's output, gate_warp() by every lane of each compute
-// warp before it reads queries; false = give up. seq_done(b) runs on thread 0
-// once sequence b's attention output is written.
-template <class GateLane, class GateWarp, class SeqDone>
-__device__ __forceinline__ void attn_phase(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeAttnParams& a,
-                                           const Shared& sh, GateLane gate_lane, GateWarp gate_warp,
-                                           SeqDone seq_done) {
+// Ask L2 for this CTA's units [u0 + first, u0 + first + count). One thread.
+__device__ __forceinline__ void prefetch_units(const CUtensorMap* mk, const CUtensorMap* mv, const DecodeAttnParams& a,
+                                               const int* pre, int first, int count) {
+  const long long U = pre[a.B], C = gridDim.x;
+  const long long u0 = range_start(blockIdx.x, U, C), u1 = range_start(blockIdx.x + 1, U, C);
+  const long long from = u0 + first, to = min(u1, u0 + first + count);
+  if (from >= to) return;
+  Cursor cur = locate(from, pre, a.B);
+  for (long long u = from; u < to; ++u) {
+    const int pos = cur.j * UNIT;
+    tma_prefetch_4d(mk, 0, pos, 0, cur.b);
+    tma_prefetch_4d(mk, 64, pos, 0, cur.b);
+    tma_prefetch_4d(mv, 0, pos, 0, cur.b);
+    tma_prefetch_4d(mv, 64, pos, 0, cur.b);
+    advance(cur, pre, a.B);
+  }
+}
+
+// This CTA's range of units: outputs of the sequences it holds whole,
+// partials of the others. Every thread of the CTA calls this. Roles: warps
+// 0..7 compute, warp 8 lane 0 produces. gate_lane() is called by the producer
+// lane before the units that need the projection's output, gate_warp() by
+// every lane of each compute warp before it reads queries; false = give up.
+// issued() runs on the producer lane once all its loads are requested.
+// Returns false (on the compute threads) when the phase gave up; on return
+// every unit is consumed and the ring is free.
+template <class GateLane, class GateWarp, class Issued>
+__device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeAttnParams& a,
+                                           const Shared& sh, GateLane gate_lane, GateWarp gate_warp, Issued issued) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = a.B;
   const int* pre = sh.pre;
@@ -136,10 +165,9 @@ __device__ __forceinline__ void attn_phase(const CUtensorMap& mk, const CUtensor
   const long long C = gridDim.x;
   const long long u0 = range_start(blockIdx.x, U, C), u1 = range_start(blockIdx.x + 1, U, C);
   const int n = static_cast<int>(u1 - u0);
-  if (n <= 0) return;
 
   if (warp == COMPUTE_WARPS) {
-    if (lane != 0) return;
+    if (lane != 0 || n <= 0) return true;
     tma_prefetch_desc(&mk);
     tma_prefetch_desc(&mv);
     Cursor iss = locate(u0, pre, B);
@@ -168,209 +196,237 @@ __device__ __forceinline__ void attn_phase(const CUtensorMap& mk, const CUtensor
     }
     if (!ok) atomicExch(&flags[0], 1);
     flags[2] = i;
-    return;
+    if (ok) issued();
+    return true;
   }
-  if (warp > COMPUTE_WARPS) return;
+  if (warp > COMPUTE_WARPS) return true;
 
-  if (!compute_all(gate_warp())) {
-    if (lane == 0) atomicExch(&flags[0], 1);
-    return;
-  }
-  const int g = warp;               // KV head of this warp
+  const int g = warp;  // KV head of this warp
   const int gr = lane >> 2, t = lane & 3;
-  const bool real_row = gr < N_REP;
-  Cursor cur = locate(u0, pre, B);
-  uint32_t qa[8][2];
-  float m_run = -INFINITY, l_run = 0.f;
-  float oacc[16][4];
-  int seg_units = 0;
-  long long seg_start = u0;
-
-  for (int i = 0; i < n; ++i) {
-    const long long u = u0 + i;
-    const int L = a.sp.get(cur.b) + 1;
-    if (i == 0 || cur.j == 0) {
-      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(
-          a.q + static_cast<size_t>(cur.b) * D_MODEL + static_cast<size_t>(g * N_REP + (gr & 3)) * HEAD_DIM);
+  bool ok = true;
+  if (n > 0) ok = compute_all(gate_warp());
+  if (n > 0 && ok) {
+    Cursor cur = locate(u0, pre, B);
+    uint32_t qb[8][2];         // Q^T as B fragments: dims 16s + 2t (+1) | +8, query head gr (0-3 real)
+    float m_run[2], l_run[2];  // query heads 2t, 2t+1
+    float oacc[8][4];          // O^T tile d: (dim 16d + gr (+8), heads 2t, 2t+1)
+    int seg_units = 0;
+    long long seg_start = u0;
+    float* so = sh.stage_out + g * N_REP * HEAD_DIM;  // this warp's [4][128] staging
+    for (int i = 0; i < n; ++i) {
+      const long long u = u0 + i;
+      const int L = a.sp.get(cur.b) + 1;
+      if (i == 0 || cur.j == 0) {
+        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(
+            a.q + static_cast<size_t>(cur.b) * D_MODEL + static_cast<size_t>(g * N_REP + (gr & 3)) * HEAD_DIM);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          qb[s][0] = gr < N_REP ? q32[s * 8 + t] : 0u;
+          qb[s][1] = gr < N_REP ? q32[s * 8 + 4 + t] : 0u;
+        }
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) oacc[d][0] = oacc[d][1] = oacc[d][2] = oacc[d][3] = 0.f;
+        seg_units = 0;
+        seg_start = u;
+      }
+      const int s = i % STAGES;
+      const bool landed = mbar_wait(smem_u32(&sh.full[s]), (i / STAGES) & 1);
+      if (!compute_all(landed && !*reinterpret_cast<volatile int*>(&flags[0]))) {
+        ok = false;
+        break;
+      }
+      // this warp's head inside the four boxes: rows g*16 + r (r = key within the unit)
+      const uint32_t kt = smem_u32(sh.ring + s * UNIT_BYTES) + g * HEAD_BYTES;
+      const uint32_t vt = kt + 2 * BOX_BYTES;
+      const int key0 = cur.j * UNIT;
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        qa[ks][0] = real_row ? q32[ks * 8 + t] : 0u;
-        qa[ks][1] = real_row ? q32[ks * 8 + 4 + t] : 0u;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(kt + (ks >> 2) * BOX_BYTES + sw128(lane & 15, 2 * (ks & 3) + (lane >> 4)), a0, a1, a2, a3);
+        mma16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
       }
-      m_run = -INFINITY;
-      l_run = 0.f;
+      // sc: (key gr, heads 2t, 2t+1), (key gr + 8, heads 2t, 2t+1)
+      const bool v0 = key0 + gr < L, v1 = key0 + gr + 8 < L;
+      sc[0] = v0 ? sc[0] * SCALE_LOG2 : -INFINITY;
+      sc[1] = v0 ? sc[1] * SCALE_LOG2 : -INFINITY;
+      sc[2] = v1 ? sc[2] * SCALE_LOG2 : -INFINITY;
+      sc[3] = v1 ? sc[3] * SCALE_LOG2 : -INFINITY;
+      float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.f;
-      seg_units = 0;
-      seg_start = u;
-    }
-    const int s = i % STAGES;
-    const bool landed = mbar_wait(smem_u32(&sh.full[s]), (i / STAGES) & 1);
-    if (!compute_all(landed && !*reinterpret_cast<volatile int*>(&flags[0]))) {
-      if (lane == 0) atomicExch(&flags[0], 1);
-      break;
-    }
-    // this warp's head inside the four boxes: rows g*16 + r (r = key within the unit)
-    const uint32_t kt = smem_u32(sh.ring + s * UNIT_BYTES) + g * HEAD_BYTES;
-    const uint32_t vt = kt + 2 * BOX_BYTES;
-    const int key0 = cur.j * UNIT;
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);  // finite: key0 < L
+      const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
+      const float p0 = exp2f(sc[0] - mn0), p1 = exp2f(sc[1] - mn1);
+      const float p2 = exp2f(sc[2] - mn0), p3 = exp2f(sc[3] - mn1);
+      float ps0 = p0 + p2, ps1 = p1 + p3;
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        ps0 += __shfl_xor_sync(0xffffffffu, ps0, o);
+        ps1 += __shfl_xor_sync(0xffffffffu, ps1, o);
+      }
+      l_run[0] = l_run[0] * al0 + ps0;
+      l_run[1] = l_run[1] * al1 + ps1;
+      m_run[0] = mn0;
+      m_run[1] = mn1;
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        oacc[d][0] *= al0;
+        oacc[d][1] *= al1;
+        oacc[d][2] *= al0;
+        oacc[d][3] *= al1;
+      }
+      // P^T as the B operand: (head gr, keys 2t, 2t+1) and (head gr, keys 2t+8, 2t+9)
+      const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
+      const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
+      uint32_t mask_a = 0xffffffffu, mask_b = 0xffffffffu;
+      if (key0 + UNIT > L) {  // value rows past the sequence may hold anything
+        const int ka = key0 + 2 * t, kb = ka + 8;
+        mask_a = (ka < L ? 0x0000ffffu : 0u) | (ka + 1 < L ? 0xffff0000u : 0u);
+        mask_b = (kb < L ? 0x0000ffffu : 0u) | (kb + 1 < L ? 0xffff0000u : 0u);
+      }
+      const int vr = (lane & 7) + ((lane >> 4) << 3);  // key row of this lane's ldmatrix address
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vt + (d >> 2) * BOX_BYTES + sw128(vr, 2 * (d & 3) + ((lane >> 3) & 1)), a0, a1, a2, a3);
+        mma16816(oacc[d], a0 & mask_a, a1 & mask_a, a2 & mask_b, a3 & mask_b, pb0, pb1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
+      ++seg_units;
 
-    float sc[2][4];
-#pragma unroll
-    for (int jn = 0; jn < 2; ++jn) {
-      sc[jn][0] = sc[jn][1] = sc[jn][2] = sc[jn][3] = 0.f;
-      const int r = jn * 8 + (lane & 7);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int ch = 4 * c + (lane >> 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kt + (ch >> 3) * BOX_BYTES + sw128(r, ch & 7), b0, b1, b2, b3);
-        mma16816(sc[jn], qa[2 * c][0], 0u, qa[2 * c][1], 0u, b0, b1);
-        mma16816(sc[jn], qa[2 * c + 1][0], 0u, qa[2 * c + 1][1], 0u, b2, b3);
-      }
-    }
-    float mx = -INFINITY;
-#pragma unroll
-    for (int jn = 0; jn < 2; ++jn) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = key0 + 8 * jn + 2 * t + e;
-        const float v = key < L ? sc[jn][e] * SCALE_LOG2 : -INFINITY;
-        sc[jn][e] = v;
-        mx = fmaxf(mx, v);
-      }
-    }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
-    const float m_use = m_new == -INFINITY ? 0.f : m_new;
-    const float alpha = exp2f(m_run - m_use);
-    float p[2][2];
-    float psum = 0.f;
-#pragma unroll
-    for (int jn = 0; jn < 2; ++jn) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        p[jn][e] = exp2f(sc[jn][e] - m_use);
-        psum += p[jn][e];
-      }
-    }
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      oacc[nt][0] *= alpha;
-      oacc[nt][1] *= alpha;
-    }
-    const uint32_t pa0 = real_row ? pack_bf16(p[0][0], p[0][1]) : 0u;
-    const uint32_t pa2 = real_row ? pack_bf16(p[1][0], p[1][1]) : 0u;
-    uint32_t mask_a = 0xffffffffu, mask_b = 0xffffffffu;
-    if (key0 + UNIT > L) {  // value rows past the sequence may hold anything
-      const int ka = key0 + 2 * t, kb = ka + 8;
-      mask_a = (ka < L ? 0x0000ffffu : 0u) | (ka + 1 < L ? 0xffff0000u : 0u);
-      mask_b = (kb < L ? 0x0000ffffu : 0u) | (kb + 1 < L ? 0xffff0000u : 0u);
-    }
-    const int vr = (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      const int ch = 2 * dp + (lane >> 4);
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(vt + (ch >> 3) * BOX_BYTES + sw128(vr, ch & 7), v0, v1, v2, v3);
-      mma16816(oacc[2 * dp], pa0, 0u, pa2, 0u, v0 & mask_a, v1 & mask_b);
-      mma16816(oacc[2 * dp + 1], pa0, 0u, pa2, 0u, v2 & mask_a, v3 & mask_b);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
-    ++seg_units;
+      const Cursor here = cur;
+      advance(cur, pre, B);
+      if (i + 1 < n && cur.j != 0) continue;
 
-    const Cursor here = cur;
-    advance(cur, pre, B);
-    if (i + 1 < n && cur.j != 0) continue;
-
-    // ---- end of this CTA's part of sequence `here.b`
-    float lsum = l_run;
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-    const int nu = units_of(pre, here.b);
-    __nv_bfloat16* out = a.o + static_cast<size_t>(here.b) * D_MODEL + static_cast<size_t>(g * N_REP) * HEAD_DIM;
-    if (seg_units == nu) {
-      if (real_row) {
-        const float inv = 1.f / lsum;
+      // ---- end of this CTA's part of sequence here.b: stage o (this warp's 4 heads) as [4][128]
+      const bool whole = seg_units == units_of(pre, here.b);
+      const float inv0 = whole ? 1.f / l_run[0] : 1.f, inv1 = whole ? 1.f / l_run[1] : 1.f;
+      if (t < 2) {
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt)
-          *reinterpret_cast<uint32_t*>(out + gr * HEAD_DIM + nt * 8 + 2 * t) =
-              pack_bf16(oacc[nt][0] * inv, oacc[nt][1] * inv);
+        for (int d = 0; d < 8; ++d) {
+          float* o0 = so + 2 * t * HEAD_DIM + 16 * d + gr;
+          o0[0] = oacc[d][0] * inv0;
+          o0[HEAD_DIM] = oacc[d][1] * inv1;
+          o0[8] = oacc[d][2] * inv0;
+          o0[HEAD_DIM + 8] = oacc[d][3] * inv1;
+        }
       }
-      fence_proxy_async_global();  // a later phase of the same grid reads o by TMA
-      __threadfence();
-      asm volatile("bar.sync 2, 256;" ::: "memory");   // the 8 compute warps
-      if (threadIdx.x == 0) seq_done(here.b);
-      continue;
-    }
-    const long long slot = (2LL * blockIdx.x + (seg_start == u0 ? 0 : 1)) * N_KV + g;
-    if (real_row) {
-      float* po = a.part_o + (slot * N_REP + gr) * HEAD_DIM;
+      __syncwarp();
+      // lane -> head lane / 8, dims 16 (lane % 8) .. + 15
+      const int hh = lane >> 3, d0 = (lane & 7) * 16;
+      const float4* src = reinterpret_cast<const float4*>(so + hh * HEAD_DIM + d0);
+      if (whole) {
+        __nv_bfloat16* out = a.o + static_cast<size_t>(here.b) * D_MODEL + static_cast<size_t>(g * N_REP + hh) * HEAD_DIM + d0;
+        uint32_t w[8];
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt)
-        __stcg(reinterpret_cast<float2*>(po + nt * 8 + 2 * t), make_float2(oacc[nt][0], oacc[nt][1]));
-      if (t == 0) __stcg(reinterpret_cast<float2*>(a.part_ml + (slot * N_REP + gr) * 2), make_float2(m_run, lsum));
-    }
-    __threadfence();
-    asm volatile("bar.sync 2, 256;" ::: "memory");
-    if (threadIdx.x == 0) flags[1] = atomicAdd(a.tickets + here.b, seg_units);
-    asm volatile("bar.sync 2, 256;" ::: "memory");
-    if (flags[1] + seg_units != nu) continue;
-
-    // last contribution to sequence here.b: warp g merges KV head g over every CTA's slot
-    __threadfence();
-    const long long ub = pre[here.b];
-    const int cf = cta_of(ub, U, C), cl = cta_of(ub + nu - 1, U, C);
-    const int hh = lane >> 3;        // query head within the group
-    const int d0 = (lane & 7) * 16;  // 16 dims per lane
-    float gmax = -INFINITY;
-    for (int cc = cf; cc <= cl; ++cc) {
-      const long long sl = (2LL * cc + (range_start(cc, U, C) >= ub ? 0 : 1)) * N_KV + g;
-      gmax = fmaxf(gmax, __ldcg(a.part_ml + (sl * N_REP + hh) * 2));
-    }
-    float gl = 0.f;
-    float go[16];
+        for (int e = 0; e < 4; ++e) {
+          const float4 v = src[e];
+          w[2 * e] = pack_bf16(v.x, v.y);
+          w[2 * e + 1] = pack_bf16(v.z, v.w);
+        }
+        reinterpret_cast<uint4*>(out)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(out)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      } else {
+        const long long slot = 2LL * blockIdx.x + (seg_start == u0 ? 0 : 1);
+        float4* dst = reinterpret_cast<float4*>(a.part_o + (slot * N_HEADS + g * N_REP + hh) * HEAD_DIM + d0);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) go[e] = 0.f;
-    for (int cc = cf; cc <= cl; ++cc) {
-      const long long sl = (2LL * cc + (range_start(cc, U, C) >= ub ? 0 : 1)) * N_KV + g;
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml + (sl * N_REP + hh) * 2));
-      const float sc2 = exp2f(ml.x - gmax);
-      gl += ml.y * sc2;
-      const float4* po = reinterpret_cast<const float4*>(a.part_o + (sl * N_REP + hh) * HEAD_DIM + d0);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float4 v = __ldcg(po + e);
-        go[4 * e] += v.x * sc2;
-        go[4 * e + 1] += v.y * sc2;
-        go[4 * e + 2] += v.z * sc2;
-        go[4 * e + 3] += v.w * sc2;
+        for (int e = 0; e < 4; ++e) __stcg(dst + e, src[e]);
+        // (max, sum) of query head g*4 + q is held by the lanes with t = q / 2
+        const int srcl = (lane >> 1) & 1;
+        const float mq0 = __shfl_sync(0xffffffffu, m_run[0], srcl), mq1 = __shfl_sync(0xffffffffu, m_run[1], srcl);
+        const float lq0 = __shfl_sync(0xffffffffu, l_run[0], srcl), lq1 = __shfl_sync(0xffffffffu, l_run[1], srcl);
+        if (lane < N_REP)
+          __stcg(reinterpret_cast<float2*>(a.part_ml + (slot * N_HEADS + g * N_REP + lane) * 2),
+                 (lane & 1) ? make_float2(mq1, lq1) : make_float2(mq0, lq0));
       }
-    }
-    const float inv = 1.f / gl;
-    uint4 lo, hi2;
-    lo.x = pack_bf16(go[0] * inv, go[1] * inv);
-    lo.y = pack_bf16(go[2] * inv, go[3] * inv);
-    lo.z = pack_bf16(go[4] * inv, go[5] * inv);
-    lo.w = pack_bf16(go[6] * inv, go[7] * inv);
-    hi2.x = pack_bf16(go[8] * inv, go[9] * inv);
-    hi2.y = pack_bf16(go[10] * inv, go[11] * inv);
-    hi2.z = pack_bf16(go[12] * inv, go[13] * inv);
-    hi2.w = pack_bf16(go[14] * inv, go[15] * inv);
-    reinterpret_cast<uint4*>(out + hh * HEAD_DIM + d0)[0] = lo;
-    reinterpret_cast<uint4*>(out + hh * HEAD_DIM + d0)[1] = hi2;
-    fence_proxy_async_global();
-    __threadfence();
-    asm volatile("bar.sync 2, 256;" ::: "memory");
-    if (threadIdx.x == 0) {
-      a.tickets[here.b] = 0;
-      seq_done(here.b);
+      __syncwarp();  // the staging area is reused by the next sequence
     }
   }
+  // its outputs and partials are out
+  fence_proxy_async_global();  // a later phase of the same grid reads o by TMA
+  __threadfence();
+  return ok;
+}
+
+// The merges, after every CTA's units: the grid meets once on `meet` (a
+// zero-filled counter, left equal to the grid size: the caller resets it),
+// then every warp merges one (sequence, query head) of the split sequences.
+// Called by the 256 compute threads of every CTA with `ok` from attn_units
+// (a CTA that gave up still meets, so that no other CTA waits in vain).
+// Returns false when any thread of the CTA gave up or the meeting timed out.
+__device__ __forceinline__ bool attn_merge(const DecodeAttnParams& a, const Shared& sh, int* meet, bool ok) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int B = a.B;
+  const int* pre = sh.pre;
+  int* flags = sh.flags;
+  const long long U = pre[B];
+  const long long C = gridDim.x;
+  const bool all_ok = compute_all(ok);
+  if (threadIdx.x == 0) {
+    atomicAdd(meet, 1);
+    flags[3] = wait_counter(meet, static_cast<int>(C)) ? 1 : 0;
+  }
+  asm volatile("bar.sync 2, 256;" ::: "memory");
+  if (!all_ok || flags[3] == 0) {
+    if (lane == 0) atomicExch(&flags[0], 1);
+    return false;
+  }
+  // merges: one warp per (sequence, query head) of every split sequence,
+  // spread over the SMs first (warp w of CTA c takes task w * C + c)
+  const int hh4 = lane * 4;  // dims of this lane
+  for (long long task = static_cast<long long>(warp) * C + blockIdx.x; task < static_cast<long long>(B) * N_HEADS;
+       task += C * COMPUTE_WARPS) {
+    const int b = static_cast<int>(task / N_HEADS), h = static_cast<int>(task % N_HEADS);
+    const int nu = units_of(pre, b);
+    if (nu == 0) continue;
+    const long long ub = pre[b];
+    const int cf = cta_of(ub, U, C), cl = cta_of(ub + nu - 1, U, C);
+    if (cf == cl) continue;  // finished by its CTA
+    float GM = -INFINITY, GL = 0.f;
+    float4 go = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = cf; c0 <= cl; c0 += MERGE_SLOTS) {
+      float2 mlv[MERGE_SLOTS];
+      float4 ov[MERGE_SLOTS];
+#pragma unroll
+      for (int k = 0; k < MERGE_SLOTS; ++k) {
+        const int cc = c0 + k;
+        if (cc <= cl) {
+          const long long sl = 2LL * cc + (range_start(cc, U, C) >= ub ? 0 : 1);
+          mlv[k] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + (sl * N_HEADS + h) * 2));
+          ov[k] = __ldcg(reinterpret_cast<const float4*>(a.part_o + (sl * N_HEADS + h) * HEAD_DIM + hh4));
+        } else {
+          mlv[k] = make_float2(-INFINITY, 0.f);
+          ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < MERGE_SLOTS; ++k) {
+        if (mlv[k].x == -INFINITY) continue;
+        const float mn = fmaxf(GM, mlv[k].x);
+        const float sa = GM == -INFINITY ? 0.f : exp2f(GM - mn), sb = exp2f(mlv[k].x - mn);
+        GL = GL * sa + mlv[k].y * sb;
+        go.x = go.x * sa + ov[k].x * sb;
+        go.y = go.y * sa + ov[k].y * sb;
+        go.z = go.z * sa + ov[k].z * sb;
+        go.w = go.w * sa + ov[k].w * sb;
+        GM = mn;
+      }
+    }
+    const float inv = 1.f / GL;
+    __nv_bfloat16* out = a.o + static_cast<size_t>(b) * D_MODEL + static_cast<size_t>(h) * HEAD_DIM + hh4;
+    *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(go.x * inv, go.y * inv), pack_bf16(go.z * inv, go.w * inv));
+  }
+  fence_proxy_async_global();
+  __threadfence();
+  asm volatile("bar.sync 2, 256;" ::: "memory");
+  return true;
 }
 
 // After an aborted phase: let loads that were issued but never consumed land

@@ -1,6 +1,7 @@
 // Standalone decode attention kernel (the decode path for batches above the
 // few-token projection size): the attention phase of attn_core.cuh in its own
-// grid, ordered after the projection by programmatic dependent launch.
+// persistent grid, launched cooperatively because its CTAs meet before the
+// merges.
 #include "attn_core.cuh"
 
 namespace gqa {
@@ -8,19 +9,18 @@ namespace gqa {
 namespace {
 
 constexpr int THREADS = (attnk::COMPUTE_WARPS + 1) * 32;
-constexpr int FIXED_SMEM = attnk::RING + 1024 + 2 * attnk::STAGES * 8 + 4 * 4;
+constexpr int FIXED_SMEM = attnk::RING + attnk::STAGE_OUT_BYTES + 1024 + 2 * attnk::STAGES * 8 + 4 * 4;
 
-__global__ void __launch_bounds__(THREADS, 1)
-    attn_decode_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                       DecodeAttnParams a) {
+__global__ void __launch_bounds__(THREADS, 1) attn_decode_kernel(const __grid_constant__ DecodeCacheMaps maps,
+                                                                 DecodeAttnParams a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + attnk::RING);
+  float* stage_out = reinterpret_cast<float*>(smem + attnk::RING);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + attnk::RING + attnk::STAGE_OUT_BYTES);
   uint64_t* empty = full + attnk::STAGES;
   int* flags = reinterpret_cast<int*>(empty + attnk::STAGES);
   int* pre = flags + 4;
 
-  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == attnk::COMPUTE_WARPS) {
     attnk::build_prefix(a, pre);
@@ -34,17 +34,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
   __syncthreads();
-  const attnk::Shared sh{smem, full, empty, flags, pre};
-  auto gate = []() {
-    pdl_wait();
-    return true;
-  };
-  attnk::attn_phase(mk, mv, a, sh, gate, gate, [](int) {});
-  pdl_wait();  // never complete before the predecessor grid: the next kernel relies on it
+  const attnk::Shared sh{smem, full, empty, flags, pre, stage_out};
+  // the projection that wrote the queries and the new rows ran before this grid
+  auto pass = []() { return true; };
+  const bool ok = attnk::attn_units(maps.k, maps.v, a, sh, pass, pass, []() {});
+  if (warp < attnk::COMPUTE_WARPS) attnk::attn_merge(a, sh, &a.counters[0], ok);
   __syncthreads();
-  if (flags[0] && threadIdx.x == attnk::COMPUTE_WARPS * 32) {
-    report(a.status, DEV_WAIT_TIMEOUT);
-    attnk::attn_drain(sh);
+  if (threadIdx.x == 0) {
+    if (flags[0]) {
+      report(a.status, DEV_WAIT_TIMEOUT);
+      attnk::attn_drain(sh);
+    }
+    // the last CTA out resets the grid counters for the next call
+    __threadfence();
+    if (atomicAdd(&a.counters[1], 1) == static_cast<int>(gridDim.x) - 1) {
+      a.counters[0] = 0;
+      a.counters[1] = 0;
+      __threadfence();
+    }
   }
 }
 
@@ -53,8 +60,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 int attn_decode_ctas(int num_sms) { return num_sms; }
 int attn_decode_slots(int ctas) { return 2 * ctas * N_KV; }
 
-cudaError_t launch_attn_decode(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeAttnParams& a,
-                               cudaStream_t s, bool pdl) {
+cudaError_t launch_attn_decode(const DecodeCacheMaps& maps, const DecodeAttnParams& a, cudaStream_t s) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -73,11 +79,11 @@ cudaError_t launch_attn_decode(const CUtensorMap& mk, const CUtensorMap& mv, con
   cfg.dynamicSmemBytes = FIXED_SMEM + (a.B + 1) * 4;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel, mk, mv, a);
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel, maps, a);
 }
 
 }  // namespace gqa

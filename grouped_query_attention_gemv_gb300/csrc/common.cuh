@@ -79,6 +79,14 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
+// Transpose of an 8x8 b16 matrix held one row pair per lane (lane 4r + c
+// holds elements (r, 2c), (r, 2c+1)): afterwards the lane holds (2c, r),
+// (2c+1, r) of the original.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
 // D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col)
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -153,6 +161,28 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   return v;
 }
 // Wait until *counter >= target (other CTAs of a co-resident grid raise it);
+// Shared-memory flag handed from one thread of a CTA to the others: the
+// writer's earlier accesses (and what it acquired) happen before the reader's
+// later ones.
+__device__ __forceinline__ void st_release_cta(int* flag, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" :: "r"(smem_u32(flag)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int* flag) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(flag)) : "memory");
+  return v;
+}
+// Wait until a shared-memory flag is non-zero; returns it (0 after WAIT_LIMIT_NS).
+__device__ __forceinline__ int wait_flag_cta(const int* flag) {
+  int v = ld_acquire_cta(flag);
+  if (v) return v;
+  const unsigned long long t0 = global_ns();
+  while (!(v = ld_acquire_cta(flag))) {
+    if (global_ns() - t0 > WAIT_LIMIT_NS) return 0;
+  }
+  return v;
+}
+
 // false after WAIT_LIMIT_NS.
 __device__ __forceinline__ bool wait_counter(const int* counter, int target) {
   if (ld_acquire(counter) >= target) return true;
@@ -171,6 +201,17 @@ __device__ __forceinline__ void signal_counter(int* counter, int add) {
 }
 
 // ----------------------------------------------------------------- TMA
+// Ask L2 to fetch [p, p + bytes) from HBM (no data moves to the SM). p and
+// bytes multiples of 16. Used to start the next phase's stream while the
+// current phase's epilogue, merges and grid waits leave HBM idle.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  constexpr uint32_t CHUNK = 32768;
+  const char* c = static_cast<const char*>(p);
+  for (uint32_t off = 0; off < bytes; off += CHUNK) {
+    const uint32_t n = bytes - off < CHUNK ? bytes - off : CHUNK;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(c + off), "r"(n) : "memory");
+  }
+}
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
 }
@@ -183,6 +224,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
       :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z) : "memory");
+}
+// Ask L2 for the box of a 2-D tensor map at the given coordinates.
+__device__ __forceinline__ void tma_prefetch_2d(const void* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" :: "l"(map), "r"(x), "r"(y) : "memory");
+}
+// Ask L2 for the box of a 3-D tensor map at the given coordinates.
+__device__ __forceinline__ void tma_prefetch_3d(const void* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" :: "l"(map), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+// Ask L2 for the box of a 4-D tensor map at the given coordinates.
+__device__ __forceinline__ void tma_prefetch_4d(const void* map, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+               :: "l"(map), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, uint32_t bar, int x, int y,
                                             int z, int w) {

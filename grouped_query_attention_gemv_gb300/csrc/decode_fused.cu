@@ -8,76 +8,119 @@
 // 34 MB at B = 16, P = 1000). Run as separate kernels, every boundary costs
 // the slowest CTA's tail plus the teardown and launch of the next grid, all
 // with HBM idle. Here phases are ordered by grid-wide counters instead:
+//   * both projections are row-owner phases (proj_rows.cuh): a CTA finishes
+//     its rows without waiting on any other CTA;
 //   * phase B needs the rotated queries and the new K/V rows: a CTA leaving
 //     phase A at once requests its first KV units (all but a sequence's last
-//     one) and waits until all 48 row tiles of phase A are published;
+//     one) and waits until every CTA has published its phase A rows;
 //   * phase C needs every sequence's attention output: a CTA leaving phase B
-//     at once requests its first W_O tiles and waits until all valid
-//     sequences are published.
+//     (whose CTAs meet once before their merges) at once requests its first
+//     W_O stages and waits until every CTA has published its outputs.
 // Waits are bounded (DEV_WAIT_TIMEOUT in the status word, then a clean exit).
 // The last CTA out resets the counters, so the workspace is ready for the
 // next call.
 #include "attn_core.cuh"
-#include "proj_core.cuh"
+#include "proj_rows.cuh"
 
 namespace gqa {
 
+bool make_row_plan(int nmat, const int* rows, int ctas, RowPlan* plan) {
+  if (nmat < 1 || nmat > 3 || ctas < nmat) return false;
+  long long total = 0;
+  for (int i = 0; i < nmat; ++i) {
+    if (rows[i] <= 0 || (rows[i] & 1)) return false;
+    total += rows[i];
+  }
+  *plan = RowPlan{};
+  plan->nmat = nmat;
+  int given = 0;
+  for (int i = nmat - 1; i >= 1; --i) {  // the smaller matrices first, the rest to matrix 0
+    plan->ctas[i] = static_cast<int>((static_cast<long long>(ctas) * rows[i] + total / 2) / total);
+    if (plan->ctas[i] < 1) plan->ctas[i] = 1;
+    given += plan->ctas[i];
+  }
+  plan->ctas[0] = ctas - given;
+  for (int i = 0; i < nmat; ++i) {
+    if (plan->ctas[i] < 1) return false;
+    const int pairs = rows[i] / 2;
+    plan->rows[i] = rows[i];
+    plan->h_lo[i] = 2 * (pairs / plan->ctas[i]);
+    const int h_hi = 2 * ((pairs + plan->ctas[i] - 1) / plan->ctas[i]);
+    if (plan->h_lo[i] < 2 || h_hi > ROWS_MAX_H) return false;
+  }
+  return true;
+}
+
 namespace {
 
-constexpr int THREADS = (attnk::COMPUTE_WARPS + 1) * 32;  // 9 warps: attention needs them all
-constexpr int QKV_TILES = QKV_ROWS / projk::TILE_ROWS;
+// warps 0-7 compute; 8 loads (weights in the projections, the cache in the
+// attention); 9 loads the projections' token rows
+constexpr int THREADS = (rowsk::WARPS + 2) * 32;
+static_assert(attnk::COMPUTE_WARPS == rowsk::WARPS, "phases share the compute warps");
+// KV units per CTA that phase A asks L2 for (beyond the ones phase B loads
+// before its gate): 152 x 4 x 64 KB = 39 MB at most, so that a long context
+// does not flush L2
+constexpr int KV_PREFETCH_UNITS = 4;
 
 struct FusedMaps {
-  ProjStreamMaps qkv, o;
-  CUtensorMap mk, mv;
+  RowMaps qkv, o;
+  DecodeCacheMaps cache;
 };
 
 struct FusedParams {
   ProjParams pq, po;
-  float* part;     // projection partial slots
-  int* tickets;    // projection row-tile tickets
-  int segmax_q, segmax_o;
+  RowPlan qkv_plan, o_plan;
   DecodeAttnParams at;
-  int* counters;   // [0] Q|K|V row tiles published, [1] sequences published, [2] CTAs done
+  int* counters;   // [0] CTAs whose Q|K|V rows are published, [1] CTAs whose attention outputs are published,
+                   // [2] CTAs done, [3] the attention's meeting before its merges
 };
+
+// Phase A streams its weights from HBM as soon as the grid starts: the
+// default (short) token ring. Phase C requests its first weight stages while
+// the grid merges the attention outputs and asks L2 for the rest, so W_O is
+// on chip by its gate; its tokens, the attention output, only become ready
+// at the gate: a deep token ring (128 KB).
+template <int NP>
+using CfgA = rowsk::Cfg<NP>;
+template <int NP>
+using CfgC = rowsk::Cfg<NP, NP == 16 ? 16 : (NP == 32 ? 8 : 3), true>;
 
 template <int NP>
 struct Layout {
-  static constexpr int RING = projk::Cfg<NP>::RING > attnk::RING ? projk::Cfg<NP>::RING : attnk::RING;
-  static constexpr int S = projk::Cfg<NP>::STAGES;
-  static constexpr int BARS = 2 * (2 * S + 4) + 2 * attnk::STAGES;  // two projection sets + attention
-  static constexpr int FIXED = RING + projk::Cfg<NP>::OUT_BYTES + BARS * 8 + 16 * 4 + 1024;
+  static constexpr int RING = rowsk::RING_BYTES > attnk::RING ? rowsk::RING_BYTES : attnk::RING;
+  static constexpr int PSET = 2 * rowsk::MAX_STAGES + 2 * rowsk::XS_MAX;   // barriers of one projection
+  static constexpr int BARS = 2 * PSET + 2 * attnk::STAGES;                // two projections + attention
+  static constexpr int FIXED = RING + BARS * 8 + 16 * 4 + 1024;
+  // the attention's output staging lies past its ring, inside the projections' ring
+  static_assert(attnk::RING + attnk::STAGE_OUT_BYTES <= RING, "attention staging fits");
 };
 
 template <int NP>
 __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_constant__ FusedMaps m, FusedParams fp) {
   using L = Layout<NP>;
-  constexpr int S = L::S;
+  constexpr int MS = rowsk::MAX_STAGES, XS = rowsk::XS_MAX;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + L::RING);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::RING + projk::Cfg<NP>::OUT_BYTES);
-  uint64_t* a_bars = bars;                       // phase A: full[S] empty[S] acc_full[2] acc_empty[2]
-  uint64_t* c_bars = bars + (2 * S + 4);         // phase C: same
-  uint64_t* b_bars = bars + 2 * (2 * S + 4);     // phase B: full[3] empty[3]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::RING);
+  uint64_t* a_bars = bars;                // phase A: full[MS] empty[MS] xfull[XS] xempty[XS]
+  uint64_t* c_bars = bars + L::PSET;      // phase C: same
+  uint64_t* b_bars = bars + 2 * L::PSET;  // phase B: full[3] empty[3]
   int* ints = reinterpret_cast<int*>(bars + L::BARS);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ints);
   int* flags_a = ints + 4;
   int* flags_b = ints + 8;
   int* flags_c = ints + 12;
-  int* n_valid_s = ints + 1;
   int* pre = ints + 16;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (uint64_t* set : {a_bars, c_bars}) {
-      for (int s = 0; s < S; ++s) {
+      for (int s = 0; s < MS; ++s) {
         mbar_init(smem_u32(&set[s]), 1);
-        mbar_init(smem_u32(&set[S + s]), 1);
+        mbar_init(smem_u32(&set[MS + s]), rowsk::WARPS);
       }
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(smem_u32(&set[2 * S + b]), 1);
-        mbar_init(smem_u32(&set[2 * S + 2 + b]), 4);
+      for (int s = 0; s < XS; ++s) {
+        mbar_init(smem_u32(&set[2 * MS + s]), 1);
+        mbar_init(smem_u32(&set[2 * MS + XS + s]), rowsk::WARPS);
       }
     }
     for (int s = 0; s < attnk::STAGES; ++s) {
@@ -87,92 +130,92 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
     for (int i = 0; i < 4; ++i) flags_a[i] = flags_b[i] = flags_c[i] = 0;
     fence_barrier_init();
   }
-  if (warp == attnk::COMPUTE_WARPS) {
-    const int valid = attnk::build_prefix(fp.at, pre);
-    if (lane == 0) *n_valid_s = valid;
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), projk::Cfg<NP>::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
+  if (warp == attnk::COMPUTE_WARPS) attnk::build_prefix(fp.at, pre);
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const int n_valid = *n_valid_s;
+  const int grid = static_cast<int>(gridDim.x);
   int* const cnt = fp.counters;
 
   // ---------------- phase A: Q|K|V projection, RoPE, cache append
-  const projk::Shared<NP> sha{smem, a_bars, a_bars + S, a_bars + 2 * S, a_bars + 2 * S + 2, stage, flags_a, tmem};
-  projk::proj_phase<NP, true>(
-      m.qkv, fp.pq, fp.part, fp.tickets, fp.segmax_q, sha, []() { return true; },
-      [cnt](int) { signal_counter(&cnt[0], 1); });
-  tc_fence_before();
+  const rowsk::Shared sha{smem, a_bars, a_bars + MS, a_bars + 2 * MS, a_bars + 2 * MS + XS, flags_a};
+  // once its weight stream is requested, the CTA asks L2 for its first KV
+  // stages after the ones phase B loads before its gate: HBM would otherwise
+  // idle through this phase's epilogue and the grid wait
+  rowsk::rows_phase<CfgA<NP>, true>(
+      m.qkv, fp.pq, fp.qkv_plan, sha, []() { return true; }, []() { return true; },
+      [&fp, &m, pre]() {
+        attnk::prefetch_units(&m.cache.k, &m.cache.v, fp.at, pre, attnk::STAGES, KV_PREFETCH_UNITS);
+      },
+      [cnt]() { signal_counter(&cnt[0], 1); });
+  fence_proxy_async_smem();  // the ring's generic reads and writes precede phase B's TMA writes into it
   __syncthreads();
-  tc_fence_after();
   bool aborted = flags_a[0] != 0;
 
-  // ---------------- phase B: attention (waits for every Q|K|V row tile)
-  const attnk::Shared shb{smem, b_bars, b_bars + attnk::STAGES, flags_b, pre};
+  // ---------------- phase B: attention units (waits for every CTA's Q|K|V rows)
+  const attnk::Shared shb{smem, b_bars, b_bars + attnk::STAGES, flags_b, pre,
+                          reinterpret_cast<float*>(smem + attnk::RING)};
+  bool units_ok = true;
   if (!aborted) {
-    attnk::attn_phase(
-        m.mk, m.mv, fp.at, shb,
-        [cnt]() {
-          const bool ok = wait_counter(&cnt[0], QKV_TILES);
+    units_ok = attnk::attn_units(
+        m.cache.k, m.cache.v, fp.at, shb,
+        // one poller per CTA: the producer lane waits on the grid counter and
+        // hands the outcome to the compute warps through shared memory
+        [cnt, grid, flags_b]() {
+          const bool ok = wait_counter(&cnt[0], grid);
           fence_proxy_async_global();  // the new K/V rows were written by plain stores
+          st_release_cta(&flags_b[1], ok ? 1 : 2);
           return ok;
         },
-        [cnt]() {
-          int ok = 0;
-          if ((threadIdx.x & 31) == 0) ok = wait_counter(&cnt[0], QKV_TILES);
-          return __shfl_sync(0xffffffffu, ok, 0) != 0;
+        [flags_b]() {
+          int v = 0;
+          if ((threadIdx.x & 31) == 0) v = wait_flag_cta(&flags_b[1]);
+          return __shfl_sync(0xffffffffu, v, 0) == 1;
         },
-        [cnt](int) { signal_counter(&cnt[1], 1); });
+        []() {});
     fence_proxy_async_smem();  // ldmatrix reads of the ring precede phase C's TMA writes into it
   }
   __syncthreads();
-  aborted = aborted || flags_b[0] != 0;
 
-  // ---------------- phase C: W_O projection (waits for every valid sequence)
-  const projk::Shared<NP> shc{smem, c_bars, c_bars + S, c_bars + 2 * S, c_bars + 2 * S + 2, stage, flags_c, tmem};
-  if (!aborted) {
-    tc_fence_after();
-    // The partial slots and tickets are phase A's as well. The producer's gate
-    // below orders this phase's loads after every phase A merge; the epilogue
-    // warps, which write the slots and take tickets, acquire the same counter
-    // themselves (their first barrier passes it on to all four warps).
-    if (threadIdx.x == 64) wait_counter(&cnt[0], QKV_TILES);
-    projk::proj_phase<NP, false>(
-        m.o, fp.po, fp.part, fp.tickets, fp.segmax_o, shc,
-        [cnt, n_valid]() {
-          // every Q|K|V tile as well: with no valid sequence phase B waits on
-          // nothing, and the partial slots and tickets are shared with phase A
-          const bool ok = wait_counter(&cnt[0], QKV_TILES) && wait_counter(&cnt[1], n_valid);
-          fence_proxy_async_global();  // o was written by plain stores
-          return ok;
-        },
-        [](int) {});
+  // ---------------- phase C: W_O projection. Its weight loads start at once;
+  // meanwhile the compute warps meet the grid and merge the attention
+  // outputs of split sequences; its token loads wait for every CTA's outputs.
+  const rowsk::Shared shc{smem, c_bars, c_bars + MS, c_bars + 2 * MS, c_bars + 2 * MS + XS, flags_c};
+  if (!aborted && flags_b[0]) {
+    // this CTA's units gave up: it still meets the grid (no other CTA waits in vain)
+    if (warp < attnk::COMPUTE_WARPS) {
+      attnk::attn_merge(fp.at, shb, &cnt[3], false);
+      if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
+    }
+  } else if (!aborted) {
+    rowsk::rows_phase<CfgC<NP>, false>(m.o, fp.po, fp.o_plan, shc,
+                                       [cnt, grid]() {
+                                         const bool ok = wait_counter(&cnt[1], grid);
+                                         fence_proxy_async_global();  // o was written by plain stores
+                                         return ok;
+                                       },
+                                       [&fp, &shb, cnt, units_ok]() {
+                                         const bool ok = attnk::attn_merge(fp.at, shb, &cnt[3], units_ok);
+                                         // this CTA's attention outputs (whole sequences, merges) are fenced
+                                         if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
+                                         return ok;
+                                       },
+                                       []() {}, []() {});
   }
-  tc_fence_before();
+  aborted = aborted || flags_b[0] != 0;
   __syncthreads();
   if (threadIdx.x == 0 && (aborted || flags_c[0])) {
     report(fp.pq.status, DEV_WAIT_TIMEOUT);
-    if (flags_a[0]) projk::proj_drain(sha);
+    if (flags_a[0]) rowsk::rows_drain<CfgA<NP>>(sha, fp.qkv_plan);
     if (flags_b[0]) attnk::attn_drain(shb);
-    if (flags_c[0]) projk::proj_drain(shc);
-  }
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, projk::Cfg<NP>::TMEM_COLS);
+    if (flags_c[0]) rowsk::rows_drain<CfgC<NP>>(shc, fp.o_plan);
   }
   if (threadIdx.x == 0) {
     // the last CTA out resets the grid counters for the next call
     __threadfence();
-    if (atomicAdd(&cnt[2], 1) == static_cast<int>(gridDim.x) - 1) {
+    if (atomicAdd(&cnt[2], 1) == grid - 1) {
       cnt[0] = 0;
       cnt[1] = 0;
       cnt[2] = 0;
+      cnt[3] = 0;
       __threadfence();
     }
   }
@@ -193,18 +236,18 @@ cudaError_t launch_fused_np(const DecodeFusedArgs& a, cudaStream_t s) {
     attr_set[dev] = true;
   }
   if (a.at.B <= 0 || a.at.B > FUSED_MAX_B) return cudaErrorInvalidValue;
+  int planned = 0;
+  for (int i = 0; i < a.qkv_plan.nmat; ++i) planned += a.qkv_plan.ctas[i];
+  if (planned != a.ctas || a.o_plan.nmat != 1 || a.o_plan.ctas[0] != a.ctas) return cudaErrorInvalidValue;
   FusedMaps m;
   m.qkv = a.qkv_maps;
   m.o = a.o_maps;
-  m.mk = a.mk;
-  m.mv = a.mv;
+  m.cache = a.cache;
   FusedParams fp;
   fp.pq = a.pq;
   fp.po = a.po;
-  fp.part = a.part;
-  fp.tickets = a.tickets;
-  fp.segmax_q = a.segmax_q;
-  fp.segmax_o = a.segmax_o;
+  fp.qkv_plan = a.qkv_plan;
+  fp.o_plan = a.o_plan;
   fp.at = a.at;
   fp.counters = a.counters;
   cudaLaunchConfig_t cfg = {};

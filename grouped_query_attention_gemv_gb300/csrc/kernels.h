@@ -137,23 +137,31 @@ cudaError_t launch_proj_stream(const ProjStreamArgs& a, cudaStream_t s, bool pdl
 // Decode attention (one new token per sequence), persistent stream-K over
 // 16-position units of the batch, all 8 KV heads per unit.
 constexpr int DECODE_MAX_B = 2048;  // sequences per launch (prefix sums live in shared memory)
-constexpr int DECODE_UNIT = 16;     // cache positions per TMA box of the decode kernel
+constexpr int DECODE_UNIT = 16;     // cache positions per unit (TMA box) of the decode attention
 constexpr int PREFILL_TILE = 64;    // cache positions per TMA box of the prefill kernel
 struct DecodeAttnParams {
   const __nv_bfloat16* q;  // [B][4096] rotated queries
   int B;
   StartPos sp;             // keys 0..sp(b) are read
   int ctas;                // grid size (one CTA per SM)
-  float* part_o;           // [attn_decode_slots(ctas)][4][128]
-  float* part_ml;          // [attn_decode_slots(ctas)][4][2] (running max in log2 units, sum)
-  int* tickets;            // [B], zero-filled, left zero-filled
+  float* part_o;           // [attn_decode_slots(ctas) / 8][32 query heads][128]
+  float* part_ml;          // [attn_decode_slots(ctas) / 8][32][2] (running max in log2 units, sum)
+  int* counters;           // [2] grid counters (meeting, exit), zero-filled, left zero-filled
   __nv_bfloat16* o;        // [B][4096]
   int* status;
+  const __nv_bfloat16* cache_k;  // [B][s_max][8][128], for L2 prefetches only
+  const __nv_bfloat16* cache_v;
+  int s_max;
 };
 int attn_decode_ctas(int num_sms);
-int attn_decode_slots(int ctas);   // (CTA, segment, KV head) partial slots
-cudaError_t launch_attn_decode(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeAttnParams& a,
-                               cudaStream_t s, bool pdl);
+int attn_decode_slots(int ctas);   // (CTA, first or last stretch, KV head) partial slots
+// Cache tensor maps of the decode attention: (dim, position, KV head,
+// sequence) with boxes of 64 dims x 16 positions x 8 heads.
+struct DecodeCacheMaps {
+  CUtensorMap k, v;
+};
+// Cooperative launch: the CTAs meet once before the merges.
+cudaError_t launch_attn_decode(const DecodeCacheMaps& maps, const DecodeAttnParams& a, cudaStream_t s);
 
 // Causal prefill attention.
 struct PrefillAttnParams {
@@ -166,16 +174,36 @@ struct PrefillAttnParams {
 cudaError_t launch_attn_prefill(const CUtensorMap& mk, const CUtensorMap& mv, const PrefillAttnParams& a,
                                 cudaStream_t s);
 
+// Row-owner projection of the fused decode grid: the rows of matrix i are
+// split over ctas[i] CTAs in row pairs; a CTA owns h_lo[i] or h_lo[i] + 2
+// rows. CTAs of matrix 0 come first, then 1, then 2.
+struct RowPlan {
+  int nmat;
+  int rows[3];
+  int ctas[3];
+  int h_lo[3];
+};
+constexpr int ROWS_MAX_H = 48;   // rows one CTA can own (3 row tiles of 16)
+// Tensor maps over (64 k, row, k block) views of [rows][4096] matrices:
+// w[i][0] / w[i][1] are matrix i with boxes of 64 x h_lo[i] (or h_lo[i] + 2)
+// rows x 4 k blocks; x is the [M][4096] token matrix with boxes of 64 x NP
+// rows x 4 k blocks.
+struct RowMaps {
+  CUtensorMap w[3][2];
+  CUtensorMap x;
+};
+// Splits nmat matrices of the given row counts over `ctas` CTAs; false if a
+// CTA would own more than ROWS_MAX_H rows or a matrix gets no CTA.
+bool make_row_plan(int nmat, const int* rows, int ctas, RowPlan* plan);
+
 // The whole decode step (Q|K|V projection, attention, W_O projection) in one
 // persistent cooperative grid, for batches of up to FUSED_MAX_B sequences.
 constexpr int FUSED_MAX_B = 64;
 struct DecodeFusedArgs {
-  ProjStreamMaps qkv_maps, o_maps;
-  CUtensorMap mk, mv;      // by-position cache views (DECODE_UNIT positions per box)
+  RowMaps qkv_maps, o_maps;
+  RowPlan qkv_plan, o_plan;
+  DecodeCacheMaps cache;
   ProjParams pq, po;       // Q|K|V (qkv = 1) and W_O (qkv = 0) projections
-  float* part;             // projection partial slots, shared by both projections
-  int* tickets;            // projection row-tile tickets [48], zero-filled, left zero-filled
-  int segmax_q, segmax_o;
   DecodeAttnParams at;
   int* counters;           // [3] grid progress counters, zero-filled, left zero-filled
   int ctas;                // one CTA per SM

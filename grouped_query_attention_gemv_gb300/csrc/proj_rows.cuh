@@ -1,0 +1,327 @@
+// Few-token projection y = x W^T (W stored [out, in]) in which every CTA owns
+// whole output rows: the projection phases of the fused decode grid
+// (decode_fused.cu). "Llama 3.1 8B · Query projection" and the K, V and
+// output projections of "Grouped-query attention".
+//
+// At decode sizes a projection is a stream of its weights (50 MB for Q|K|V,
+// 34 MB for W_O at bf16) against a handful of token rows, and in a grid that
+// runs several phases back to back its end matters as much as its rate:
+//   * the rows of each weight matrix are split over a share of the grid
+//     proportional to its size (Q|K|V: 102 + 25 + 25 CTAs of 40 or 42 rows on
+//     152 SMs; W_O: 152 CTAs of 26 or 28 rows), in pairs so that RoPE partners
+//     stay together. Every CTA reads all 64 k blocks of its rows, so every CTA
+//     streams the same bytes to within one row pair, and no CTA waits on
+//     another: there is no cross-CTA reduction (the stream-K projection of
+//     proj_core.cuh pays a chain of global round trips per row tile for it);
+//   * a weight stage holds 4 k blocks of the CTA's h rows, fetched as ONE TMA
+//     box of (64 k x h rows x 4 blocks) over a (k, row, k block) view of W: a
+//     TMA request has a fixed cost, and four smaller boxes per stage measured
+//     a lower rate per SM than the weight stream needs. The box lands dense,
+//     row R = block * h + r at R * 128 bytes with the 128-byte swizzle of R,
+//     which ldmatrix addresses directly (the MMAs here need no tensor-core
+//     descriptor layout). The token rows of the same 4 k blocks (one box of 64
+//     k x NP tokens x 4 blocks) go to a separate ring: they come from L2;
+//   * CTAs walk the 16 stages from different starting points: were they in
+//     step, every request in flight would fall in the same 512-byte window of
+//     the 8 KB weight rows;
+//   * the arithmetic is mma.sync m16n8k16 (bf16 in, fp32 accumulate) on the 8
+//     compute warps: warp w takes k block w % 4 of every stage, up to 3 row
+//     tiles of 16, and either half of that block's 64 k and every token (up
+//     to 32 tokens: each weight fragment is read from shared memory once) or
+//     all of its k and half of the tokens (64 tokens: the accumulators of all
+//     tokens would not fit in registers). The step is bound by HBM, and with
+//     so few tokens the cost per tensor instruction, not FLOPs, decides
+//     whether the arithmetic keeps up: with 40-42 rows per CTA a tcgen05.mma
+//     covers 16 k of a 64-row tile, and the 256 of them a CTA needs measured
+//     slower than the weight stream itself, while 8 warps of mma.sync keep up;
+//   * at the end the 8 warps' partials of every (row, token) are added in
+//     shared memory, the pair (f, f+1) is rotated (Q|K|V), written as bf16
+//     and published with one counter increment.
+#pragma once
+
+#include "kernels.h"
+
+namespace gqa {
+namespace rowsk {
+
+constexpr int KBLK = 64;
+constexpr int NKB = D_MODEL / KBLK;      // 64 k blocks
+constexpr int KC = 4;                    // k blocks per stage (= k-block groups of warps)
+constexpr int NST = NKB / KC;            // 16 stages per CTA
+constexpr int MT_MAX = ROWS_MAX_H / 16;  // row tiles of 16
+constexpr int WARPS = 8;                 // compute warps 0-7; warp 8 lane 0 loads W, warp 9 lane 0 loads x
+constexpr int MAX_STAGES = 12;           // weight stages (barrier pairs)
+constexpr int RING_BYTES = 216 * 1024;   // weight ring + token ring
+constexpr int OVERREAD = 1024;           // the last row tile may read up to 15 rows past a stage
+
+constexpr int XS_MAX = NST;              // token stages at most (all of a phase's tokens)
+
+// NP padded tokens; XS token stages in flight. A phase whose weights come
+// from HBM wants most of shared memory for them (few token stages); one whose
+// weights are already in L2 but whose tokens only become ready when it starts
+// wants the tokens in flight instead.
+// L2_REST: once the weight ring is full, ask L2 for the rest of the CTA's
+// weights (for a phase whose first loads go out long before its tokens are
+// ready, so that HBM works through the wait).
+template <int NP_, int XS_ = (NP_ == 16 ? 4 : (NP_ == 32 ? 3 : 2)), bool L2_REST_ = false>
+struct Cfg {
+  static constexpr int NP = NP_;
+  static constexpr bool L2_REST = L2_REST_;
+  static constexpr int B_BYTES = NP * KBLK * 2;      // one k block of the token tile
+  static constexpr int X_STAGE = KC * B_BYTES;       // the token rows of one weight stage
+  static constexpr int XS = XS_;                     // token stages
+  static_assert(XS >= 1 && XS <= XS_MAX, "token stages");
+  static constexpr int X_RING = XS * X_STAGE;
+  static constexpr int W_RING = RING_BYTES - X_RING;
+  static constexpr bool TOKEN_SPLIT = NP > 32;      // warps split the tokens (else the k of a block)
+  static constexpr int NT = TOKEN_SPLIT ? NP / 16 : NP / 8;  // n8 token tiles per warp
+  static constexpr int RED_BYTES = WARPS * ROWS_MAX_H * NP * 4;  // per-warp partials, reuse the weight ring
+  static_assert(RED_BYTES <= W_RING, "the reduction fits in the weight ring");
+};
+
+// Weight stage: 4 k blocks of the phase's largest row count, rounded up to
+// whole 1 KB swizzle atoms (so that every stage starts 1024-byte aligned).
+__device__ __forceinline__ int wstage_bytes(const RowPlan& plan) {
+  int hmax = 0;
+  for (int i = 0; i < plan.nmat; ++i) hmax = max(hmax, plan.h_lo[i] + 2);
+  return ((KC * hmax * 128 + 1023) / 1024) * 1024;
+}
+
+// This CTA's rows: matrix `mat`, rows [row0, row0 + h), map index hi (0: h_lo, 1: h_lo + 2).
+struct MyRows {
+  int mat, row0, h, hi;
+};
+__device__ __forceinline__ MyRows my_rows(const RowPlan& plan, int c) {
+  int mat = 0;
+  while (mat + 1 < plan.nmat && c >= plan.ctas[mat]) c -= plan.ctas[mat++];
+  const int pairs = plan.rows[mat] / 2, n = plan.ctas[mat];
+  const int p0 = static_cast<int>(static_cast<long long>(pairs) * c / n);
+  const int p1 = static_cast<int>(static_cast<long long>(pairs) * (c + 1) / n);
+  MyRows r;
+  r.mat = mat;
+  r.row0 = 2 * p0;
+  r.h = 2 * (p1 - p0);
+  r.hi = r.h == plan.h_lo[mat] ? 0 : 1;
+  return r;
+}
+
+// AND of `v` over the 256 compute threads (warps 0-7), with a barrier.
+__device__ __forceinline__ bool compute_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 4, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r) : "r"(static_cast<uint32_t>(v)) : "memory");
+  return r != 0;
+}
+
+struct Shared {
+  uint8_t* ring;    // RING_BYTES, 1024-aligned: weight ring, then token ring
+  uint64_t* full;   // [MAX_STAGES], count 1
+  uint64_t* empty;  // [MAX_STAGES], count WARPS
+  uint64_t* xfull;  // [XS_MAX], count 1
+  uint64_t* xempty; // [XS_MAX], count WARPS
+  int* flags;       // [0] abort, [2] weight stages issued, [3] token stages issued
+};
+
+// One projection phase. Roles: warps 0-7 compute, warp 8 lane 0 loads the
+// weights, warp 9 lane 0 the token rows; other lanes return at once. gate()
+// runs on the token producer before its first load (false = give up);
+// prologue() runs on the 256 compute threads before they consume anything
+// (other work of the grid that may overlap the first weight loads; false =
+// give up); w_issued() runs on the weight producer once all its loads are
+// requested; rows_done() runs on thread 0 once this CTA's rows are written
+// and fenced.
+template <class C_, bool QKV, class Gate, class Prologue, class WIssued, class RowsDone>
+__device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams& p, const RowPlan& plan,
+                                           const Shared& sh, Gate gate, Prologue prologue, WIssued w_issued,
+                                           RowsDone rows_done) {
+  constexpr int NP = C_::NP;
+  constexpr int XS = C_::XS;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const MyRows mr = my_rows(plan, blockIdx.x);
+  const int rot = (blockIdx.x * 7) % NST;  // this CTA's first k stage
+  const int wstage = wstage_bytes(plan);
+  const int S = min(MAX_STAGES, (C_::W_RING - OVERREAD) / wstage);
+  uint8_t* const xring = sh.ring + C_::W_RING;
+  int* flags = sh.flags;
+
+  if (warp == WARPS) {
+    if (lane != 0) return;
+    // ---------------- weight producer: needs nothing from earlier phases
+    const CUtensorMap* wmap = &maps.w[mr.mat][mr.hi];
+    tma_prefetch_desc(wmap);
+    const uint32_t bytes = KC * mr.h * 128;
+    int i = 0;
+    for (; i < NST; ++i) {
+      const int s = i % S, ks = (i + rot) % NST;
+      if (C_::L2_REST && i == S) {
+        for (int r = S; r < NST; ++r) tma_prefetch_3d(wmap, 0, mr.row0, ((r + rot) % NST) * KC);
+      }
+      if (i >= S && !mbar_wait(smem_u32(&sh.empty[s]), ((i / S) & 1) ^ 1)) {
+        atomicExch(&flags[0], 1);
+        break;
+      }
+      const uint32_t fb = smem_u32(&sh.full[s]);
+      mbar_expect_tx(fb, bytes);
+      tma_load_3d(smem_u32(sh.ring + s * wstage), wmap, fb, 0, mr.row0, ks * KC);
+    }
+    flags[2] = i;
+    if (i == NST) w_issued();
+    return;
+  }
+  if (warp == WARPS + 1) {
+    if (lane != 0) return;
+    // ---------------- token producer: the token rows may come from an earlier phase
+    tma_prefetch_desc(&maps.x);
+    bool ok = gate();
+    int i = 0;
+    for (; ok && i < NST; ++i) {
+      const int s = i % XS, ks = (i + rot) % NST;
+      if (i >= XS && !mbar_wait(smem_u32(&sh.xempty[s]), ((i / XS) & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb = smem_u32(&sh.xfull[s]);
+      mbar_expect_tx(fb, C_::X_STAGE);
+      tma_load_3d(smem_u32(xring + s * C_::X_STAGE), &maps.x, fb, 0, 0, ks * KC);
+    }
+    if (!ok) atomicExch(&flags[0], 1);
+    flags[3] = i;
+    return;
+  }
+  if (warp > WARPS + 1) return;
+
+  // ---------------- compute warps: k block kb of every stage; k16 steps [ks0, ks0 + KS) of it and
+  // tokens [tok0, tok0 + 8 NT)
+  const int kb = warp & (KC - 1);
+  constexpr int KS = C_::TOKEN_SPLIT ? 4 : 2;
+  const int ks0 = C_::TOKEN_SPLIT ? 0 : 2 * (warp / KC);
+  const int tok0 = C_::TOKEN_SPLIT ? (warp / KC) * (NP / 2) : 0;
+  const int mtc = (mr.h + 15) >> 4;  // row tiles holding this CTA's rows
+  float acc[MT_MAX][C_::NT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT_MAX; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < C_::NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+
+  bool ok = prologue();
+  for (int i = 0; ok && i < NST; ++i) {
+    const int s = i % S, xs = i % XS;
+    bool landed = mbar_wait(smem_u32(&sh.full[s]), (i / S) & 1);
+    landed = landed && mbar_wait(smem_u32(&sh.xfull[xs]), (i / XS) & 1);
+    if (!compute_all(landed && !*reinterpret_cast<volatile int*>(&flags[0]))) {
+      ok = false;
+      break;
+    }
+    const uint32_t wa = smem_u32(sh.ring + s * wstage);
+    const int rb = kb * mr.h;  // this warp's k block starts at row rb of the stage
+    const uint32_t xb = smem_u32(xring + xs * C_::X_STAGE + kb * C_::B_BYTES);
+#pragma unroll
+    for (int ks = ks0; ks < ks0 + KS; ks += 2) {
+      // token fragments of two k16 steps: matrices (tokens, 16-byte chunks 2ks .. 2ks+3)
+      uint32_t b[C_::NT][4];
+#pragma unroll
+      for (int nt = 0; nt < C_::NT; ++nt) {
+        const int tr = tok0 + nt * 8 + (lane & 7);
+        ldsm_x4(xb + sw128(tr, 2 * ks + (lane >> 3)), b[nt][0], b[nt][1], b[nt][2], b[nt][3]);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+        for (int mt = 0; mt < MT_MAX; ++mt) {
+          if (mt < mtc) {
+            uint32_t a0, a1, a2, a3;
+            const int r = rb + mt * 16 + (lane & 15);
+            ldsm_x4(wa + sw128(r, 2 * (ks + kk) + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < C_::NT; ++nt)
+              mma16816(acc[mt][nt], a0, a1, a2, a3, b[nt][2 * kk], b[nt][2 * kk + 1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(smem_u32(&sh.empty[s]));
+      mbar_arrive(smem_u32(&sh.xempty[xs]));
+    }
+  }
+  if (!ok) {
+    if (lane == 0) atomicExch(&flags[0], 1);
+    return;
+  }
+  // every stage is consumed: the weight ring holds the warps' partials [WARPS][ROWS_MAX_H][NP]
+  float* red = reinterpret_cast<float*>(sh.ring);
+  asm volatile("bar.sync 4, 256;" ::: "memory");
+  {
+    const int gr = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int mt = 0; mt < MT_MAX; ++mt) {
+      if (mt < mtc) {
+#pragma unroll
+        for (int nt = 0; nt < C_::NT; ++nt) {
+          const int row = mt * 16 + gr, tok = tok0 + nt * 8 + 2 * t;
+          float* d = red + (warp * ROWS_MAX_H + row) * NP + tok;
+          *reinterpret_cast<float2*>(d) = make_float2(acc[mt][nt][0], acc[mt][nt][1]);
+          *reinterpret_cast<float2*>(d + 8 * NP) = make_float2(acc[mt][nt][2], acc[mt][nt][3]);
+        }
+      }
+    }
+  }
+  asm volatile("bar.sync 4, 256;" ::: "memory");
+  // epilogue: thread -> (row pair, token)
+  const int fbase = (mr.mat == 0 ? 0 : (mr.mat == 1 ? p.r1 : p.r2)) + mr.row0;  // feature of row 0
+  for (int idx = threadIdx.x; idx < (mr.h / 2) * p.M; idx += WARPS * 32) {
+    const int m = idx % p.M, pr = idx / p.M;
+    const int r = 2 * pr, f = fbase + r;
+    float x0 = 0.f, x1 = 0.f;
+    // the warps that hold token m: all 8, or the 4 of its half
+    const int w0 = C_::TOKEN_SPLIT ? (m / (NP / 2)) * KC : 0;
+#pragma unroll
+    for (int w = 0; w < (C_::TOKEN_SPLIT ? KC : WARPS); ++w) {
+      x0 += red[((w0 + w) * ROWS_MAX_H + r) * NP + m];
+      x1 += red[((w0 + w) * ROWS_MAX_H + r + 1) * NP + m];
+    }
+    __nv_bfloat16* dst;
+    if constexpr (QKV) {
+      const int b = m / p.T;
+      const int start = p.sp.get(b);
+      if (!p.sp.ok(start)) continue;
+      const int pos = start + (m - b * p.T);
+      if (f < D_MODEL + KV_ROW) {
+        const float2 cs = *reinterpret_cast<const float2*>(
+            p.rope + (static_cast<size_t>(pos) * ROPE_PAIRS + ((f & (HEAD_DIM - 1)) >> 1)) * 2);
+        const float y0 = x0 * cs.x - x1 * cs.y;
+        const float y1 = x0 * cs.y + x1 * cs.x;
+        x0 = y0;
+        x1 = y1;
+      }
+      if (f < D_MODEL) {
+        dst = p.out + static_cast<size_t>(m) * D_MODEL + f;
+      } else {
+        const size_t row = (static_cast<size_t>(b) * p.s_max + pos) * KV_ROW;
+        dst = f < D_MODEL + KV_ROW ? p.cache_k + row + (f - D_MODEL) : p.cache_v + row + (f - D_MODEL - KV_ROW);
+      }
+    } else {
+      dst = p.out + static_cast<size_t>(m) * p.N + f;
+    }
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16(x0, x1);
+  }
+  fence_proxy_async_global();  // later phases of the grid read these rows by TMA
+  __threadfence();
+  asm volatile("bar.sync 4, 256;" ::: "memory");
+  if (threadIdx.x == 0) rows_done();
+}
+
+// After an aborted phase: let loads that were issued but never consumed land
+// (bounded) before the shared memory is reused or the CTA exits. One thread.
+template <class C_>
+__device__ __forceinline__ void rows_drain(const Shared& sh, const RowPlan& plan) {
+  constexpr int XS = C_::XS;
+  const int S = min(MAX_STAGES, (C_::W_RING - OVERREAD) / wstage_bytes(plan));
+  for (int i = max(0, sh.flags[2] - S); i < sh.flags[2]; ++i) mbar_wait(smem_u32(&sh.full[i % S]), (i / S) & 1);
+  for (int i = max(0, sh.flags[3] - XS); i < sh.flags[3]; ++i) mbar_wait(smem_u32(&sh.xfull[i % XS]), (i / XS) & 1);
+}
+
+}  // namespace rowsk
+}  // namespace gqa
