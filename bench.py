@@ -112,9 +112,14 @@ def kernel_traffic(name: str):
     ent = d.get(name)
     if not ent:
         return None
-    src = os.path.join(ROOT, "grouped_query_attention_gemv_gb300", "csrc", ent["source"])
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] if os.path.exists(src) else None
-    return ent["bytes_per_launch"] if h == ent.get("source_sha256_16") else None
+    srcs = ent["source"] if isinstance(ent["source"], list) else [ent["source"]]
+    h = hashlib.sha256()
+    for f in srcs:
+        path = os.path.join(ROOT, "grouped_query_attention_gemv_gb300", "csrc", f)
+        if not os.path.exists(path):
+            return None
+        h.update(open(path, "rb").read())
+    return ent["bytes_per_launch"] if h.hexdigest()[:16] == ent.get("source_sha256_16") else None
 
 
 class ClockSampler:
