@@ -231,9 +231,12 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
         seg_units = 0;
         seg_start = u;
       }
+      // each warp on its own: no barrier per unit (the merge step makes the
+      // outcome uniform)
       const int s = i % STAGES;
       const bool landed = mbar_wait(smem_u32(&sh.full[s]), (i / STAGES) & 1);
-      if (!compute_all(landed && !*reinterpret_cast<volatile int*>(&flags[0]))) {
+      if (!__all_sync(0xffffffffu, landed)) {
+        if (lane == 0) atomicExch(&flags[0], 1);
         ok = false;
         break;
       }

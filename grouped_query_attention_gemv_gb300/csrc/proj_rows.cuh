@@ -204,12 +204,17 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
 #pragma unroll
     for (int nt = 0; nt < C_::NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
 
+  // Each warp runs through the stages on its own (no per-stage barrier, so
+  // that warps drift and cover each other's latencies); a warp whose bounded
+  // wait gives up records it and leaves the loop. Every warp then meets the
+  // others at the barrier after the loop, where the outcome is read.
   bool ok = prologue();
   for (int i = 0; ok && i < NST; ++i) {
     const int s = i % S, xs = i % XS;
     bool landed = mbar_wait(smem_u32(&sh.full[s]), (i / S) & 1);
     landed = landed && mbar_wait(smem_u32(&sh.xfull[xs]), (i / XS) & 1);
-    if (!compute_all(landed && !*reinterpret_cast<volatile int*>(&flags[0]))) {
+    if (!__all_sync(0xffffffffu, landed)) {
+      if (lane == 0) atomicExch(&flags[0], 1);
       ok = false;
       break;
     }
@@ -246,13 +251,15 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
       mbar_arrive(smem_u32(&sh.xempty[xs]));
     }
   }
-  if (!ok) {
+  if (!ok && lane == 0) atomicExch(&flags[0], 1);
+  // every warp is past its stages (a producer may still give up at any time:
+  // the vote gives every compute thread the same answer)
+  if (!compute_all(ok && !*reinterpret_cast<volatile int*>(&flags[0]))) {
     if (lane == 0) atomicExch(&flags[0], 1);
     return;
   }
-  // every stage is consumed: the weight ring holds the warps' partials [WARPS][ROWS_MAX_H][NP]
+  // the weight ring now holds the warps' partials [WARPS][ROWS_MAX_H][NP]
   float* red = reinterpret_cast<float*>(sh.ring);
-  asm volatile("bar.sync 4, 256;" ::: "memory");
   {
     const int gr = lane >> 2, t = lane & 3;
 #pragma unroll
