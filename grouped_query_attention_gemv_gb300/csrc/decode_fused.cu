@@ -83,7 +83,7 @@ struct FusedParams {
 template <int NP>
 using CfgA = rowsk::Cfg<NP>;
 template <int NP>
-using CfgC = rowsk::Cfg<NP, NP == 16 ? 16 : (NP == 32 ? 8 : 3), true>;
+using CfgC = rowsk::Cfg<NP, NP <= 16 ? 16 : (NP == 32 ? 8 : 3), true>;
 
 template <int NP>
 struct Layout {
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
         mbar_init(smem_u32(&set[MS + s]), rowsk::WARPS);
       }
       for (int s = 0; s < XS; ++s) {
-        mbar_init(smem_u32(&set[2 * MS + s]), 1);
+        mbar_init(smem_u32(&set[2 * MS + s]), 32);
         mbar_init(smem_u32(&set[2 * MS + XS + s]), rowsk::WARPS);
       }
     }
@@ -266,6 +266,7 @@ cudaError_t launch_fused_np(const DecodeFusedArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
+  if (a.pq.M <= 8) return launch_fused_np<8>(a, s);  // half the tensor work of 16 padded tokens
   switch (proj_stream_np(a.pq.M)) {
     case 16: return launch_fused_np<16>(a, s);
     case 32: return launch_fused_np<32>(a, s);

@@ -184,13 +184,11 @@ struct RowPlan {
   int h_lo[3];
 };
 constexpr int ROWS_MAX_H = 48;   // rows one CTA can own (3 row tiles of 16)
-// Tensor maps over (64 k, row, k block) views of [rows][4096] matrices:
+// Tensor maps over (64 k, row, k block) views of the weight matrices:
 // w[i][0] / w[i][1] are matrix i with boxes of 64 x h_lo[i] (or h_lo[i] + 2)
-// rows x 4 k blocks; x is the [M][4096] token matrix with boxes of 64 x NP
 // rows x 4 k blocks.
 struct RowMaps {
   CUtensorMap w[3][2];
-  CUtensorMap x;
 };
 // Splits nmat matrices of the given row counts over `ctas` CTAs; false if a
 // CTA would own more than ROWS_MAX_H rows or a matrix gets no CTA.

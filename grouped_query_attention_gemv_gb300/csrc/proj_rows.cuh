@@ -63,7 +63,7 @@ constexpr int XS_MAX = NST;              // token stages at most (all of a phase
 // L2_REST: once the weight ring is full, ask L2 for the rest of the CTA's
 // weights (for a phase whose first loads go out long before its tokens are
 // ready, so that HBM works through the wait).
-template <int NP_, int XS_ = (NP_ == 16 ? 4 : (NP_ == 32 ? 3 : 2)), bool L2_REST_ = false>
+template <int NP_, int XS_ = (NP_ <= 16 ? 4 : (NP_ == 32 ? 3 : 2)), bool L2_REST_ = false>
 struct Cfg {
   static constexpr int NP = NP_;
   static constexpr bool L2_REST = L2_REST_;
@@ -118,7 +118,7 @@ struct Shared {
   uint8_t* ring;    // RING_BYTES, 1024-aligned: weight ring, then token ring
   uint64_t* full;   // [MAX_STAGES], count 1
   uint64_t* empty;  // [MAX_STAGES], count WARPS
-  uint64_t* xfull;  // [XS_MAX], count 1
+  uint64_t* xfull;  // [XS_MAX], count 32 (the token producer's lanes)
   uint64_t* xempty; // [XS_MAX], count WARPS
   int* flags;       // [0] abort, [2] weight stages issued, [3] token stages issued
 };
@@ -170,23 +170,41 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     return;
   }
   if (warp == WARPS + 1) {
-    if (lane != 0) return;
-    // ---------------- token producer: the token rows may come from an earlier phase
-    tma_prefetch_desc(&maps.x);
-    bool ok = gate();
+    // ---------------- token producer (the whole warp): the token rows may come
+    // from an earlier phase. They are small and in L2, and every CTA reads all
+    // of them, so they go through cp.async (16 bytes a lane) rather than the
+    // CTA's TMA queue, which the weight stream keeps busy. Rows past M are
+    // zero-filled. Each lane arrives on the stage's barrier once its copies
+    // land (count 32).
+    int okv = 1;
+    if (lane == 0) okv = gate() ? 1 : 0;
+    okv = __shfl_sync(0xffffffffu, okv, 0);  // lane 0 acquired the gate; the shuffle orders the others after it
+    __syncwarp();
+    bool ok = okv != 0;
     int i = 0;
+    constexpr int CHUNKS = KC * NP * 8;  // 16-byte pieces of one token stage
     for (; ok && i < NST; ++i) {
       const int s = i % XS, ks = (i + rot) % NST;
-      if (i >= XS && !mbar_wait(smem_u32(&sh.xempty[s]), ((i / XS) & 1) ^ 1)) {
-        ok = false;
-        break;
+      if (i >= XS) {
+        const bool freed = mbar_wait(smem_u32(&sh.xempty[s]), ((i / XS) & 1) ^ 1);
+        if (!__all_sync(0xffffffffu, freed)) {
+          ok = false;
+          break;
+        }
       }
-      const uint32_t fb = smem_u32(&sh.xfull[s]);
-      mbar_expect_tx(fb, C_::X_STAGE);
-      tma_load_3d(smem_u32(xring + s * C_::X_STAGE), &maps.x, fb, 0, 0, ks * KC);
+      const uint32_t dst = smem_u32(xring + s * C_::X_STAGE);
+#pragma unroll 4
+      for (int c = lane; c < CHUNKS; c += 32) {
+        const int kb = c / (NP * 8), rem = c - kb * NP * 8;
+        const int tok = rem >> 3, ch = rem & 7;
+        const bool real = tok < p.M;
+        const __nv_bfloat16* src = p.x + static_cast<size_t>(real ? tok : 0) * D_MODEL + (ks * KC + kb) * KBLK + ch * 8;
+        cp_async_16(dst + kb * C_::B_BYTES + sw128(tok, ch), src, real ? 16 : 0);
+      }
+      cp_async_mbar_arrive(smem_u32(&sh.xfull[s]));
     }
-    if (!ok) atomicExch(&flags[0], 1);
-    flags[3] = i;
+    if (!ok && lane == 0) atomicExch(&flags[0], 1);
+    if (lane == 0) flags[3] = i;
     return;
   }
   if (warp > WARPS + 1) return;
