@@ -138,13 +138,28 @@ bool map_cache_by_position(CUtensorMap* m, const void* ptr, int B, int s_max, in
 }
 
 // KV cache [B, s_max, 8, 128] bf16 as a 4-D tensor (d, g, pos, b); boxes of
-// 64 dims x 1 head x box_pos positions. Positions past s_max read as zero.
-bool map_cache(CUtensorMap* m, const void* ptr, int B, int s_max, int box_pos) {
+// 64 dims x 1 head x box_pos positions. Positions at or past `rows` (<= s_max)
+// read as zero.
+bool map_cache(CUtensorMap* m, const void* ptr, int B, int s_max, int rows, int box_pos) {
   EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[4] = {HEAD_DIM, N_KV, static_cast<cuuint64_t>(s_max), static_cast<cuuint64_t>(B)};
+  if (!enc || rows <= 0 || rows > s_max) return false;
+  const cuuint64_t dims[4] = {HEAD_DIM, N_KV, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {HEAD_DIM * 2, KV_ROW * 2, static_cast<cuuint64_t>(s_max) * KV_ROW * 2};
   const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_pos), 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Rotated queries [B*T, 4096] bf16 as a 4-D tensor (d, head, t, b); boxes of
+// 64 dims x 4 heads (one KV group) x 32 tokens. Tokens past T read as zero.
+bool map_q_prefill(CUtensorMap* m, const void* ptr, int B, int T) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {HEAD_DIM, N_HEADS, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {HEAD_DIM * 2, D_MODEL * 2, static_cast<cuuint64_t>(T) * D_MODEL * 2};
+  const cuuint32_t box[4] = {64, N_REP, 32, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -305,17 +320,20 @@ int run_attention(const Call& c) {
     if (attn_decode_slots(a.ctas) > c.L.att_slots) return fail_cuda(cudaErrorInvalidConfiguration);
     e = launch_attn_decode(maps, a, c.stream);
   } else {
-    CUtensorMap mk, mv;
-    if (!map_cache(&mk, c.cache_k, c.B, c.s_max, PREFILL_TILE) || !map_cache(&mv, c.cache_v, c.B, c.s_max, PREFILL_TILE))
+    PrefillMaps maps;
+    const void* q = c.ws + c.L.q;
+    if (!map_q_prefill(&maps.q, q, c.B, c.T) ||
+        !map_cache(&maps.k, c.cache_k, c.B, c.s_max, c.max_keys, PREFILL_TILE) ||
+        !map_cache(&maps.v, c.cache_v, c.B, c.s_max, c.max_keys, PREFILL_TILE))
       return fail_cuda(cudaErrorInvalidValue);
     PrefillAttnParams a{};
-    a.q = reinterpret_cast<const __nv_bfloat16*>(c.ws + c.L.q);
+    a.q = reinterpret_cast<const __nv_bfloat16*>(q);
     a.B = c.B;
     a.T = c.T;
     a.sp = c.sp;
     a.o = reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.o);
     a.status = reinterpret_cast<int*>(c.ws + c.L.status);
-    e = launch_attn_prefill(mk, mv, a, c.stream);
+    e = launch_attn_prefill(maps, a, c.stream);
   }
   if (e != cudaSuccess) return fail_cuda(e);
   ++t_launches;

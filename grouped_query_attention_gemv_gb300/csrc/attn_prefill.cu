@@ -1,14 +1,30 @@
-// Causal prefill attention: T new tokens per sequence after start_pos cached
-// rows. Query t (position start_pos + t) of head h attends to cache rows
-// 0..start_pos+t of KV head h / 4 ("Llama 3.1 8B · Grouped-query attention":
-// the mask of Transformer.forward is -inf above the diagonal, left-padded with
-// start_pos visible columns; softmax in fp32; output heads merged h*128 + d).
+// Causal prefill attention on the 5th-generation tensor cores. Query t
+// (position start_pos + t) of head h attends to cache rows 0..start_pos+t of
+// KV head h / 4 ("Llama 3.1 8B · Grouped-query attention": the mask of
+// Transformer.forward is -inf above the diagonal, left-padded with start_pos
+// visible columns; softmax in fp32; output heads merged h*128 + d).
 //
-// One CTA takes 32 query positions of one sequence and the 4 query heads of
-// one KV group (8 warps, 16 rows each). K/V tiles of 64 keys come in by 4-D
-// TMA (128B swizzle, 2-stage mbarrier ring) once for all 4 heads; QK^T and PV
-// run on mma.sync m16n8k16 with an online softmax in fp32. Tiles above a
-// warp's diagonal are skipped; CTAs with the longest key range launch first.
+// One CTA owns 32 query positions of one sequence and the 4 query heads of
+// one KV group: a 128-row Q tile (row r = position r/4, head r%4), so every
+// K/V tile is staged once for all 4 heads. Key tiles of 64 positions:
+//   warp 4 (one lane)  TMA producer: Q once, then K_j / V_j (128B swizzle,
+//                      two-stage rings on mbarriers)
+//   warp 5 (one lane)  MMA issuer, in the order S_0, S_1, PV_0, S_2, PV_1 ...:
+//                      S_j = Q K_j^T (M=128, N=64) into TMEM slot j%2, then
+//                      O += P_j V_j (M=128, N=128) with P_j read from TMEM and
+//                      V_j as an MN-major shared-memory operand
+//   warps 0-3          one thread per row: loads S_j from TMEM, masks keys past
+//                      the row's position, keeps a running max / sum in fp32,
+//                      writes P_j = 2^(S*scale - max) as bf16 over S_j, and at
+//                      the end reads O, divides by the sum and stores bf16.
+// TMEM (256 columns): S slots at [0,64) and [64,128), O at [128,256), so two
+// CTAs share an SM and one's softmax overlaps the other's matrix products.
+// O is rescaled only when a row's running max grows by more than 2^8 over the
+// max its P values were taken against (the result is the same: every P and
+// the sum use that reference).
+// Every barrier wait is bounded; a wait that gives up records
+// DEV_WAIT_TIMEOUT, lets issued copies and products finish (bounded) and frees
+// TMEM before the CTA exits.
 #include <math.h>
 
 #include "kernels.h"
@@ -17,229 +33,296 @@ namespace gqa {
 
 namespace {
 
-constexpr int TILE = PREFILL_TILE;  // keys per stage (= TMA box height)
-constexpr int QT = 32;                          // query positions per CTA
+constexpr int QP = 32;                    // query positions per CTA
+constexpr int ROWS = QP * N_REP;          // 128 rows = MMA M
+constexpr int KT = PREFILL_TILE;          // keys per tile (= TMA box height)
 constexpr int STAGES = 2;
-constexpr int HALF_BYTES = TILE * 128;
-constexpr int KV_TILE_BYTES = 2 * HALF_BYTES;
-constexpr int STAGE_BYTES = 2 * KV_TILE_BYTES;
-constexpr int THREADS = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 128;
-constexpr float SCALE_LOG2 = 0.08838834764831845f * 1.4426950408889634f;
+constexpr int Q_HALF = ROWS * 128;        // 128 rows x 64 dims
+constexpr int KV_HALF = KT * 128;         // 64 keys x 64 dims
+constexpr int KV_TILE = 2 * KV_HALF;
+constexpr int K_OFF = 2 * Q_HALF;
+constexpr int V_OFF = K_OFF + STAGES * KV_TILE;
+constexpr int BAR_OFF = V_OFF + STAGES * KV_TILE;
+constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+constexpr int THREADS = 192;
+constexpr int PRODUCER_WARP = 4, MMA_WARP = 5;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t O_COL = 128;
+constexpr float SCALE_LOG2 = 0.08838834764831845f * 1.4426950408889634f;  // log2(e) / sqrt(128)
+constexpr float RESCALE_LOG2 = 8.f;
 
-__device__ __forceinline__ void issue_tile(uint8_t* smem, uint64_t* full, const CUtensorMap* mk,
-                                           const CUtensorMap* mv, int i, int g, int b) {
-  const int st = i % STAGES;
-  const uint32_t fb = smem_u32(&full[st]);
-  const uint32_t base = smem_u32(smem + st * STAGE_BYTES);
-  const int pos = i * TILE;
-  mbar_expect_tx(fb, STAGE_BYTES);
-  tma_load_4d(base, mk, fb, 0, g, pos, b);
-  tma_load_4d(base + HALF_BYTES, mk, fb, 64, g, pos, b);
-  tma_load_4d(base + KV_TILE_BYTES, mv, fb, 0, g, pos, b);
-  tma_load_4d(base + KV_TILE_BYTES + HALF_BYTES, mv, fb, 64, g, pos, b);
-}
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_done, mma_done;
+  uint32_t tmem_slot;
+  int abort;
+  int k_issued, v_issued;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
-__global__ void __launch_bounds__(THREADS, 1)
-    attn_prefill_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                        PrefillAttnParams a) {
+__device__ __forceinline__ bool aborted(const Bars& bs) { return *reinterpret_cast<const volatile int*>(&bs.abort) != 0; }
+
+__global__ void __launch_bounds__(THREADS, 2)
+    attn_prefill_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                        const __grid_constant__ CUtensorMap mv, PrefillAttnParams a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  int* sflag = reinterpret_cast<int*>(empty + STAGES);  // [0] abort, [2] issued
+  Bars& bs = *reinterpret_cast<Bars*>(smem + BAR_OFF);
 
-  const int nqt = (a.T + QT - 1) / QT;
-  const int qtile = nqt - 1 - static_cast<int>(blockIdx.x);  // longest key ranges first
-  const int g = blockIdx.y, b = blockIdx.z;
+  // longest key ranges first: the query tile index falls with blockIdx.x
+  const int nqt = (a.T + QP - 1) / QP;
+  const int g = blockIdx.x % N_KV;
+  const int rest = blockIdx.x / N_KV;
+  const int b = rest % a.B;
+  const int qtile = nqt - 1 - rest / a.B;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gr = lane >> 2, t = lane & 3;
-  const int hh = warp >> 1;
-  const int h = g * N_REP + hh;
   const int start = a.sp.get(b);
   if (!a.sp.ok(start)) {
     if (qtile == nqt - 1 && g == 0 && threadIdx.x == 0) report(a.status, DEV_BAD_POSITION);
     return;
   }
-  const int q0 = qtile * QT;
-  const int kv_end = start + min(q0 + QT, a.T);
-  const int ntiles = (kv_end + TILE - 1) / TILE;
-  const int row0 = q0 + (warp & 1) * 16 + gr;  // query index t of rows gr and gr+8
-  const int row1 = row0 + 8;
-  const int qp0 = row0 < a.T ? start + row0 : -1;  // absolute positions (-1: no such row)
-  const int qp1 = row1 < a.T ? start + row1 : -1;
-  const int wmax = start + min(q0 + (warp & 1) * 16 + 15, a.T - 1);  // last position of this warp
+  const int q0 = qtile * QP;
+  const int kv_end = start + min(q0 + QP, a.T);
+  const int n = (kv_end + KT - 1) / KT;
 
   if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bs.q_full), 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), THREADS / 32);
+      mbar_init(smem_u32(&bs.k_full[s]), 1);
+      mbar_init(smem_u32(&bs.k_empty[s]), 1);
+      mbar_init(smem_u32(&bs.v_full[s]), 1);
+      mbar_init(smem_u32(&bs.v_empty[s]), 1);
     }
-    sflag[0] = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bs.s_full[s]), 1);
+      mbar_init(smem_u32(&bs.p_full[s]), 4);
+    }
+    mbar_init(smem_u32(&bs.o_done), 1);
+    mbar_init(smem_u32(&bs.mma_done), 1);
+    bs.abort = 0;
+    bs.k_issued = 0;
+    bs.v_issued = 0;
     fence_barrier_init();
-    const int first = min(STAGES, ntiles);
-    for (int i = 0; i < first; ++i) issue_tile(smem, full, &mk, &mv, i, g, b);
-    sflag[2] = first;
   }
-
-  // Q fragments: rows gr / gr+8 = query rows row0 / row1, cols = dims
-  uint32_t qa[8][4];
-  {
-    const size_t tok0 = static_cast<size_t>(b) * a.T + row0;
-    const uint32_t* q0p = reinterpret_cast<const uint32_t*>(a.q + tok0 * D_MODEL + static_cast<size_t>(h) * HEAD_DIM);
-    const uint32_t* q1p = q0p + 8 * D_MODEL / 2;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qa[ks][0] = row0 < a.T ? q0p[ks * 8 + t] : 0u;
-      qa[ks][1] = row1 < a.T ? q1p[ks * 8 + t] : 0u;
-      qa[ks][2] = row0 < a.T ? q0p[ks * 8 + 4 + t] : 0u;
-      qa[ks][3] = row1 < a.T ? q1p[ks * 8 + 4 + t] : 0u;
-    }
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(&bs.tmem_slot), TMEM_COLS);
+    tmem_relinquish();
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bs.tmem_slot;
+  const uint32_t sbase = smem_u32(smem);
 
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float oacc[16][4];
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.f;
-
-  bool aborted = false;
-  for (int i = 0; i < ntiles; ++i) {
-    const int st = i % STAGES;
-    const uint32_t ph = (i / STAGES) & 1;
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[st]), ph))) {
-      aborted = true;
-      break;
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+      const uint32_t qb = smem_u32(&bs.q_full);
+      mbar_expect_tx(qb, 2 * Q_HALF);
+      tma_load_4d(sbase, &mq, qb, 0, g * N_REP, q0, b);
+      tma_load_4d(sbase + Q_HALF, &mq, qb, 64, g * N_REP, q0, b);
+      int kn = 0, vn = 0;
+      bool ok = true;
+      for (int j = 0; j <= n && ok; ++j) {
+        if (j < n) {
+          const int s = j & 1;
+          if (j >= STAGES) ok = mbar_wait(smem_u32(&bs.k_empty[s]), ((j >> 1) - 1) & 1);
+          if (!ok || aborted(bs)) break;
+          const uint32_t fb = smem_u32(&bs.k_full[s]);
+          const uint32_t dst = sbase + K_OFF + s * KV_TILE;
+          mbar_expect_tx(fb, KV_TILE);
+          tma_load_4d(dst, &mk, fb, 0, g, j * KT, b);
+          tma_load_4d(dst + KV_HALF, &mk, fb, 64, g, j * KT, b);
+          kn = j + 1;
+        }
+        if (j >= 1) {
+          const int i = j - 1, s = i & 1;
+          if (i >= STAGES) ok = mbar_wait(smem_u32(&bs.v_empty[s]), ((i >> 1) - 1) & 1);
+          if (!ok || aborted(bs)) break;
+          const uint32_t fb = smem_u32(&bs.v_full[s]);
+          const uint32_t dst = sbase + V_OFF + s * KV_TILE;
+          mbar_expect_tx(fb, KV_TILE);
+          tma_load_4d(dst, &mv, fb, 0, g, i * KT, b);
+          tma_load_4d(dst + KV_HALF, &mv, fb, 64, g, i * KT, b);
+          vn = i + 1;
+        }
+      }
+      if (!ok) atomicExch(&bs.abort, 1);
+      bs.k_issued = kn;
+      bs.v_issued = vn;
     }
-    const int base_key = i * TILE;
-    if (base_key <= wmax) {
-      const uint32_t kt = smem_u32(smem + st * STAGE_BYTES);
-      const uint32_t vt = kt + KV_TILE_BYTES;
-      float sc[8][4];
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      const uint32_t idesc_s = umma_idesc_bf16(ROWS, KT);
+      const uint32_t idesc_o = umma_idesc_bf16(ROWS, HEAD_DIM) | (1u << 16);  // B (V) MN-major
+      bool ok = mbar_wait(smem_u32(&bs.q_full), 0);
+      for (int j = 0; ok && j <= n; ++j) {
+        if (j < n) {
+          const int s = j & 1;
+          ok = mbar_wait(smem_u32(&bs.k_full[s]), (j >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t kt = sbase + K_OFF + s * KV_TILE;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-        const int r = j * 8 + (lane & 7);
+          for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
+            const uint32_t off = (ks & 3) * 32;
+            umma_bf16(tmem + s * KT, umma_desc_sw128(sbase + (ks >> 2) * Q_HALF + off),
+                      umma_desc_sw128(kt + (ks >> 2) * KV_HALF + off), idesc_s, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&bs.k_empty[s]));
+          umma_commit(smem_u32(&bs.s_full[s]));
+        }
+        if (j >= 1) {
+          const int i = j - 1, s = i & 1;
+          ok = mbar_wait(smem_u32(&bs.p_full[s]), (i >> 1) & 1) && mbar_wait(smem_u32(&bs.v_full[s]), (i >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t vt = sbase + V_OFF + s * KV_TILE;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int ch = 4 * c + (lane >> 3);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kt + (ch >> 3) * HALF_BYTES + sw128(r, ch & 7), b0, b1, b2, b3);
-          mma16816(sc[j], qa[2 * c][0], qa[2 * c][1], qa[2 * c][2], qa[2 * c][3], b0, b1);
-          mma16816(sc[j], qa[2 * c + 1][0], qa[2 * c + 1][1], qa[2 * c + 1][2], qa[2 * c + 1][3], b2, b3);
+          for (int ks = 0; ks < KT / 16; ++ks)
+            umma_bf16_ts(tmem + O_COL, tmem + s * KT + ks * 8, umma_desc_sw128_mn(vt + ks * 16 * 128, KV_HALF), idesc_o,
+                         (i > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&bs.v_empty[s]));
+          umma_commit(smem_u32(&bs.o_done));
         }
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int key = base_key + 8 * j + 2 * t + e;
-          const float v0 = key <= qp0 ? sc[j][e] * SCALE_LOG2 : -INFINITY;
-          const float v1 = key <= qp1 ? sc[j][2 + e] * SCALE_LOG2 : -INFINITY;
-          sc[j][e] = v0;
-          sc[j][2 + e] = v1;
-          mx0 = fmaxf(mx0, v0);
-          mx1 = fmaxf(mx1, v1);
-        }
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
-      const float al0 = exp2f(m0 - u0), al1 = exp2f(m1 - u1);
-      m0 = n0;
-      m1 = n1;
-      float s0 = 0.f, s1 = 0.f;
-      uint32_t pa[4][4];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float p0 = exp2f(sc[j][0] - u0), p1 = exp2f(sc[j][1] - u0);
-        const float p2 = exp2f(sc[j][2] - u1), p3 = exp2f(sc[j][3] - u1);
-        s0 += p0 + p1;
-        s1 += p2 + p3;
-        pa[j >> 1][(j & 1) * 2] = pack_bf16(p0, p1);
-        pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
-      }
-      l0 = l0 * al0 + s0;
-      l1 = l1 * al1 + s1;
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        oacc[nt][0] *= al0;
-        oacc[nt][1] *= al0;
-        oacc[nt][2] *= al1;
-        oacc[nt][3] *= al1;
-      }
-      const bool ragged = base_key + TILE > kv_end;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t mask_a = 0xffffffffu, mask_b = 0xffffffffu;
-        if (ragged) {
-          const int ka = base_key + 16 * kk + 2 * t, kb = ka + 8;
-          mask_a = (ka < kv_end ? 0x0000ffffu : 0u) | (ka + 1 < kv_end ? 0xffff0000u : 0u);
-          mask_b = (kb < kv_end ? 0x0000ffffu : 0u) | (kb + 1 < kv_end ? 0xffff0000u : 0u);
-        }
-        const int vr = 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-        for (int dp = 0; dp < 8; ++dp) {
-          const int ch = 2 * dp + (lane >> 4);
-          uint32_t v0, v1, v2, v3;
-          ldsm_x4_t(vt + (ch >> 3) * HALF_BYTES + sw128(vr, ch & 7), v0, v1, v2, v3);
-          mma16816(oacc[2 * dp], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], v0 & mask_a, v1 & mask_b);
-          mma16816(oacc[2 * dp + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], v2 & mask_a, v3 & mask_b);
-        }
-      }
+      if (!ok) atomicExch(&bs.abort, 1);
+      umma_commit(smem_u32(&bs.mma_done));
+      mbar_wait(smem_u32(&bs.mma_done), 0);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
-    if (threadIdx.x == 0 && i + STAGES < ntiles) {
-      if (mbar_wait(smem_u32(&empty[st]), ph)) {
-        issue_tile(smem, full, &mk, &mv, i + STAGES, g, b);
-        sflag[2] = i + STAGES + 1;
+  } else {
+    // softmax / epilogue: thread r owns row r = TMEM lane r
+    const int r = warp * 32 + lane;
+    const int t = q0 + (r >> 2);
+    const int hh = r & 3;
+    const int lim = min(start + t, kv_end - 1);  // last key this row sees
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float m_ref = -INFINITY;  // max the current P values and O are taken against (raw score units)
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int s = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.s_full[s]), (j >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[KT];
+      tmem_ld32(lane_addr + s * KT, sr);
+      tmem_ld32(lane_addr + s * KT + 32, sr + 32);
+      tmem_ld_wait();
+      float mx = -INFINITY;
+      const int vis = lim - j * KT;  // columns 0..vis are visible to this row
+      if (vis < KT - 1) {
+#pragma unroll
+        for (int c = 0; c < KT; ++c) {
+          const float v = c <= vis ? __uint_as_float(sr[c]) : -INFINITY;
+          sr[c] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
       } else {
-        aborted = true;
+#pragma unroll
+        for (int c = 0; c < KT; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
       }
+      float alpha = 1.f;
+      const bool grow = mx > m_ref && (m_ref == -INFINITY || (mx - m_ref) * SCALE_LOG2 > RESCALE_LOG2);
+      if (grow) {
+        alpha = m_ref == -INFINITY ? 0.f : ex2_approx((m_ref - mx) * SCALE_LOG2);
+        m_ref = mx;
+      }
+      const float neg = m_ref == -INFINITY ? 0.f : -m_ref * SCALE_LOG2;
+      float sum = 0.f;
+      uint32_t pk[KT / 2];
+#pragma unroll
+      for (int c = 0; c < KT; c += 2) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), SCALE_LOG2, neg));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), SCALE_LOG2, neg));
+        sum += p0 + p1;
+        pk[c >> 1] = pack_bf16(p0, p1);
+      }
+      l = l * alpha + sum;
+      if (j > 0) {
+        // O must hold P_{j-1} V_{j-1} before it is rescaled (and this keeps
+        // the o_done phases in step with j)
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.o_done), (j - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+          for (int c = 0; c < HEAD_DIM; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(lane_addr + O_COL + c, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(lane_addr + O_COL + c, o);
+          }
+        }
+      }
+      tmem_st32(lane_addr + s * KT, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bs.p_full[s]));
     }
-    if (__any_sync(0xffffffffu, aborted)) {
-      aborted = true;
-      break;
+    if (ok && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.o_done), (n - 1) & 1))) ok = false;
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = a.o + (static_cast<size_t>(b) * a.T + t) * D_MODEL +
+                           static_cast<size_t>(g * N_REP + hh) * HEAD_DIM;
+#pragma unroll 1
+      for (int c = 0; c < HEAD_DIM; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(lane_addr + O_COL + c, o);
+        tmem_ld_wait();
+        if (t < a.T) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+            d4[e] = w;
+          }
+        }
+      }
+    } else if (lane == 0) {
+      atomicExch(&bs.abort, 1);
     }
-  }
-  if (aborted) atomicExch(&sflag[0], 1);
-  __syncthreads();
-  if (sflag[0]) {
-    if (threadIdx.x == 0) {
-      report(a.status, DEV_WAIT_TIMEOUT);
-      const int issued = sflag[2];
-      for (int i = max(0, issued - STAGES); i < issued; ++i)
-        mbar_wait(smem_u32(&full[i % STAGES]), (i / STAGES) & 1);
-    }
-    return;
   }
 
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
-  const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  __nv_bfloat16* o0 = a.o + (static_cast<size_t>(b) * a.T + row0) * D_MODEL + static_cast<size_t>(h) * HEAD_DIM;
-  __nv_bfloat16* o1 = o0 + 8 * static_cast<size_t>(D_MODEL);
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    if (row0 < a.T)
-      *reinterpret_cast<uint32_t*>(o0 + nt * 8 + 2 * t) = pack_bf16(oacc[nt][0] * inv0, oacc[nt][1] * inv0);
-    if (row1 < a.T)
-      *reinterpret_cast<uint32_t*>(o1 + nt * 8 + 2 * t) = pack_bf16(oacc[nt][2] * inv1, oacc[nt][3] * inv1);
+  tc_fence_before();
+  __syncthreads();
+  if (aborted(bs)) {
+    if (threadIdx.x == 0) report(a.status, DEV_WAIT_TIMEOUT);
+    if (warp == PRODUCER_WARP && lane == 0) {
+      // the last copy into each stage may still be in flight
+      mbar_wait(smem_u32(&bs.q_full), 0);
+      for (int u = max(0, bs.k_issued - STAGES); u < bs.k_issued; ++u)
+        mbar_wait(smem_u32(&bs.k_full[u & 1]), (u >> 1) & 1);
+      for (int u = max(0, bs.v_issued - STAGES); u < bs.v_issued; ++u)
+        mbar_wait(smem_u32(&bs.v_full[u & 1]), (u >> 1) & 1);
+    }
+    __syncthreads();
+  }
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_attn_prefill(const CUtensorMap& mk, const CUtensorMap& mv, const PrefillAttnParams& a,
-                                cudaStream_t s) {
+cudaError_t launch_attn_prefill(const PrefillMaps& maps, const PrefillAttnParams& a, cudaStream_t s) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -250,8 +333,10 @@ cudaError_t launch_attn_prefill(const CUtensorMap& mk, const CUtensorMap& mv, co
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const dim3 grid((a.T + QT - 1) / QT, N_KV, a.B);
-  attn_prefill_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(mk, mv, a);
+  if (a.B <= 0 || a.T <= 0) return cudaErrorInvalidValue;
+  const long long ctas = static_cast<long long>((a.T + QP - 1) / QP) * N_KV * a.B;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  attn_prefill_kernel<<<static_cast<unsigned>(ctas), THREADS, SMEM_BYTES, s>>>(maps.q, maps.k, maps.v, a);
   return cudaGetLastError();
 }
 

@@ -171,8 +171,14 @@ struct PrefillAttnParams {
   __nv_bfloat16* o;        // [B*T][4096]
   int* status;
 };
-cudaError_t launch_attn_prefill(const CUtensorMap& mk, const CUtensorMap& mv, const PrefillAttnParams& a,
-                                cudaStream_t s);
+// Tensor maps of the prefill attention: q over (dim, head, token, sequence)
+// with boxes of 64 dims x 4 heads x 32 tokens; k / v over (dim, KV head,
+// position, sequence) with boxes of 64 dims x 1 head x PREFILL_TILE positions
+// and a position extent of start_pos + T, so later positions read as zero.
+struct PrefillMaps {
+  CUtensorMap q, k, v;
+};
+cudaError_t launch_attn_prefill(const PrefillMaps& maps, const PrefillAttnParams& a, cudaStream_t s);
 
 // Row-owner projection of the fused decode grid: the rows of matrix i are
 // split over ctas[i] CTAs in row pairs; a CTA owns h_lo[i] or h_lo[i] + 2
