@@ -304,7 +304,7 @@ int run_projection(const Call& c, bool qkv, bool pdl) {
       maps.b[1] = maps.b[0];
       maps.b[2] = maps.b[0];
     }
-    e = launch_gemm_tc(maps, p, c.stream);
+    e = launch_gemm_tc(maps, p, launch_sms(), c.stream);
   }
   if (e != cudaSuccess) return fail_cuda(e);
   ++t_launches;

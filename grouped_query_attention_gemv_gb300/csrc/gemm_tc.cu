@@ -2,16 +2,25 @@
 // y[M, N] = x[M, 4096] W^T with W stored [out, in] (the F.linear storage of
 // the "Query projection" page), K fixed at 4096.
 //
-// One CTA computes a 128 x 256 output tile:
+// Persistent: one CTA per SM walks the 128 x 256 output tiles t = CTA,
+// CTA + grid, ... in n-major order (consecutive tiles share a weight tile, so
+// the weights come from HBM once and the re-reads hit L2):
 //   warp 0 (one lane)   TMA producer: 128x64 x tile and 256x64 W tile per
-//                       stage, 128B-swizzled, 4-stage ring on mbarriers
+//                       stage, 128B-swizzled, 4-stage ring on mbarriers, one
+//                       ring across the CTA's tiles
 //   warp 1 (one lane)   MMA issuer: tcgen05.mma kind::f16 (bf16 in, fp32 out)
-//                       into a 256-column TMEM accumulator, tcgen05.commit
-//                       releases each stage
-//   warps 2-5           epilogue: tcgen05.ld of their 32 TMEM lanes, fused
-//                       RoPE + KV-cache append (Q|K|V) or bf16 store (W_O)
+//                       into one of two 256-column TMEM accumulators;
+//                       tcgen05.commit releases each stage, then the tile
+//   warps 2-5           epilogue of the previous tile while the next one is
+//                       multiplied: tcgen05.ld of their 32 TMEM lanes (one
+//                       token each), fused RoPE + KV-cache append (Q|K|V) or a
+//                       bf16 store (W_O), then the accumulator goes back.
+// A 256-column tile holds two heads: the RoPE pairs of column c and c + 128
+// share one (cos, sin), so each thread loads its position's 64 pairs (one
+// 512-byte table row) once per tile and rotates both heads with them.
 // Every barrier wait is bounded; a wait that gives up records
-// DEV_WAIT_TIMEOUT, drains outstanding copies (bounded) and frees TMEM.
+// DEV_WAIT_TIMEOUT, drains outstanding copies and products (bounded) and
+// frees TMEM.
 #include "kernels.h"
 
 namespace gqa {
@@ -25,6 +34,119 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NKB = D_MODEL / BK;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
+constexpr int EPI_WARPS = 4;
+
+struct Bars {
+  uint64_t full[STAGES], empty[STAGES];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_slot;
+  int abort;
+  int issued, consumed;  // k-block loads requested / consumed by the MMA issuer
+};
+
+__device__ __forceinline__ bool aborted(const Bars& bs) { return *reinterpret_cast<const volatile int*>(&bs.abort) != 0; }
+
+// Weight map and row of output feature n0 (tiles never straddle w0/w1/w2).
+__device__ __forceinline__ const CUtensorMap* weight_of(const ProjParams& p, const CUtensorMap* b0, const CUtensorMap* b1,
+                                                        const CUtensorMap* b2, int n0, int& brow) {
+  if (n0 < p.r1) {
+    brow = n0;
+    return b0;
+  }
+  if (n0 < p.r2) {
+    brow = n0 - p.r1;
+    return b1;
+  }
+  brow = n0 - p.r2;
+  return b2;
+}
+
+__device__ __forceinline__ void store32(__nv_bfloat16* dst, const float (&v)[16]) {
+  uint4 lo, hi;
+  lo.x = pack_bf16(v[0], v[1]);
+  lo.y = pack_bf16(v[2], v[3]);
+  lo.z = pack_bf16(v[4], v[5]);
+  lo.w = pack_bf16(v[6], v[7]);
+  hi.x = pack_bf16(v[8], v[9]);
+  hi.y = pack_bf16(v[10], v[11]);
+  hi.z = pack_bf16(v[12], v[13]);
+  hi.w = pack_bf16(v[14], v[15]);
+  reinterpret_cast<uint4*>(dst)[0] = lo;
+  reinterpret_cast<uint4*>(dst)[1] = hi;
+}
+
+// Rotate the 8 pairs of v by (cos, sin) pairs cs[0..3] (two pairs per float4).
+__device__ __forceinline__ void rotate16(float (&v)[16], const float4* cs) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 c = cs[j];
+    float a = v[4 * j], b = v[4 * j + 1];
+    v[4 * j] = a * c.x - b * c.y;
+    v[4 * j + 1] = a * c.y + b * c.x;
+    a = v[4 * j + 2];
+    b = v[4 * j + 3];
+    v[4 * j + 2] = a * c.z - b * c.w;
+    v[4 * j + 3] = a * c.w + b * c.z;
+  }
+}
+
+// Epilogue of one tile for token m (this thread's TMEM lane): columns n0 .. n0+255.
+__device__ __forceinline__ void epilogue_tile(const ProjParams& p, uint32_t acc, int m, int n0) {
+  __nv_bfloat16* dst = nullptr;
+  int pos = 0;
+  bool rope = false;
+  if (m < p.M) {
+    if (!p.qkv) {
+      dst = p.out + static_cast<size_t>(m) * p.N + n0;
+    } else {
+      const int b = m / p.T;
+      const int t = m - b * p.T;
+      const int start = p.sp.get(b);
+      if (p.sp.ok(start)) {
+        pos = start + t;
+        if (n0 < D_MODEL) {
+          dst = p.out + static_cast<size_t>(m) * D_MODEL + n0;
+          rope = true;
+        } else {
+          const size_t row = (static_cast<size_t>(b) * p.s_max + pos) * KV_ROW;
+          rope = n0 < D_MODEL + KV_ROW;
+          dst = rope ? p.cache_k + row + (n0 - D_MODEL) : p.cache_v + row + (n0 - D_MODEL - KV_ROW);
+        }
+      } else if (t == 0 && n0 == 0) {
+        report(p.status, DEV_BAD_POSITION);
+      }
+    }
+  }
+  float4 cs[32];  // (cos, sin) of the 64 pairs at this position
+  if (rope) {
+    const float4* row = reinterpret_cast<const float4*>(p.rope + static_cast<size_t>(pos) * ROPE_PAIRS * 2);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cs[j] = __ldg(row + j);
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t r0[16], r1[16];
+    tmem_ld16(acc + c * 16, r0);
+    tmem_ld16(acc + 128 + c * 16, r1);
+    tmem_ld_wait();
+    float v0[16], v1[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      v0[e] = __uint_as_float(r0[e]);
+      v1[e] = __uint_as_float(r1[e]);
+    }
+    if (rope) {
+      rotate16(v0, cs + 4 * c);
+      rotate16(v1, cs + 4 * c);
+    }
+    if (dst) {
+      store32(dst + c * 16, v0);
+      store32(dst + 128 + c * 16, v1);
+    }
+  }
+}
 
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
@@ -32,135 +154,146 @@ __global__ void __launch_bounds__(THREADS, 1)
                    ProjParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* acc_bar = empty + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
-  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] issued, [2] consumed
+  Bars& bs = *reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN;
-  const int m0 = blockIdx.y * BM;
-  const CUtensorMap* map_b;
-  int brow;
-  if (n0 < p.r1) {
-    map_b = &map_b0;
-    brow = n0;
-  } else if (n0 < p.r2) {
-    map_b = &map_b1;
-    brow = n0 - p.r1;
-  } else {
-    map_b = &map_b2;
-    brow = n0 - p.r2;
-  }
+  const int tiles_m = (p.M + BM - 1) / BM;
+  const int tiles = tiles_m * (p.N / BN);
+  const int G = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&bs.full[s]), 1);
+      mbar_init(smem_u32(&bs.empty[s]), 1);
     }
-    mbar_init(smem_u32(acc_bar), 1);
-    flags[0] = 0;
-    flags[1] = 0;
-    flags[2] = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bs.acc_full[i]), 1);
+      mbar_init(smem_u32(&bs.acc_empty[i]), EPI_WARPS);
+    }
+    mbar_init(smem_u32(&bs.mma_done), 1);
+    bs.abort = 0;
+    bs.issued = 0;
+    bs.consumed = 0;
     fence_barrier_init();
     tma_prefetch_desc(&map_a);
-    tma_prefetch_desc(map_b);
+    tma_prefetch_desc(&map_b0);
+    tma_prefetch_desc(&map_b1);
+    tma_prefetch_desc(&map_b2);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), BN);
+    tmem_alloc(smem_u32(&bs.tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = bs.tmem_slot;
+  const uint32_t sbase = smem_u32(smem);
 
-  if (warp == 0 && lane == 0) {
-    int kb = 0;
-    for (; kb < NKB; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = (kb / STAGES) & 1;
-      if (kb >= STAGES && !mbar_wait(smem_u32(&empty[s]), ph ^ 1)) {
-        atomicExch(&flags[0], 1);
-        break;
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += G) {
+        const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+        int brow;
+        const CUtensorMap* mb = weight_of(p, &map_b0, &map_b1, &map_b2, n0, brow);
+        for (int kb = 0; kb < NKB; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (it >= STAGES && !mbar_wait(smem_u32(&bs.empty[s]), ((it / STAGES) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          if (aborted(bs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&bs.full[s]);
+          const uint32_t sa = sbase + s * STAGE_BYTES;
+          mbar_expect_tx(fb, STAGE_BYTES);
+          tma_load_2d(sa, &map_a, fb, kb * BK, m0);
+          tma_load_2d(sa + A_BYTES, mb, fb, kb * BK, brow);
+        }
       }
-      if (*reinterpret_cast<volatile int*>(&flags[0])) break;
-      const uint32_t fb = smem_u32(&full[s]);
-      const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-      mbar_expect_tx(fb, STAGE_BYTES);
-      tma_load_2d(sa, &map_a, fb, kb * BK, m0);
-      tma_load_2d(sa + A_BYTES, map_b, fb, kb * BK, brow);
+      if (!ok) atomicExch(&bs.abort, 1);
+      bs.issued = it;
     }
-    flags[1] = kb;
-  } else if (warp == 1 && lane == 0) {
-    const uint32_t idesc = umma_idesc_bf16(BM, BN);
-    int kb = 0;
-    for (; kb < NKB; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = (kb / STAGES) & 1;
-      if (!mbar_wait(smem_u32(&full[s]), ph)) {
-        atomicExch(&flags[0], 1);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16(BM, BN);
+      int it = 0, j = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += G, ++j) {
+        const int buf = j & 1;
+        if (j >= 2 && !mbar_wait(smem_u32(&bs.acc_empty[buf]), ((j >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + buf * BN;
+        for (int kb = 0; kb < NKB; ++kb, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(smem_u32(&bs.full[s]), (it / STAGES) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16(d, umma_desc_sw128(sa + k * 32), umma_desc_sw128(sb + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
+          umma_commit(smem_u32(&bs.empty[s]));
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&bs.acc_full[buf]));
+      }
+      if (!ok) atomicExch(&bs.abort, 1);
+      bs.consumed = it;
+      umma_commit(smem_u32(&bs.mma_done));
+      mbar_wait(smem_u32(&bs.mma_done), 0);
+    }
+  } else {
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    int j = 0;
+    for (int t = blockIdx.x; t < tiles; t += G, ++j) {
+      const int buf = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.acc_full[buf]), (j >> 1) & 1)) ||
+          __any_sync(0xffffffffu, aborted(bs))) {
+        if (lane == 0) atomicExch(&bs.abort, 1);
         break;
       }
       tc_fence_after();
-      const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-      const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-      for (int k = 0; k < BK / 16; ++k) {
-        umma_bf16(tmem, umma_desc_sw128(sa + k * 32), umma_desc_sw128(sb + k * 32), idesc,
-                  (kb | k) != 0 ? 1u : 0u);
-      }
-      umma_commit(smem_u32(&empty[s]));
-    }
-    flags[2] = kb;
-    umma_commit(smem_u32(acc_bar));
-  } else if (warp >= 2) {
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    bool ok = mbar_wait(smem_u32(acc_bar), 0);
-    tc_fence_after();
-    ok = __all_sync(0xffffffffu, ok && !*reinterpret_cast<volatile int*>(&flags[0]));
-    if (ok) {
-      const int m = m0 + quarter * 32 + lane;
-      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 16) {
-        uint32_t r[16];
-        tmem_ld16(lane_addr + c, r);
-        tmem_ld_wait();
-        if (m < p.M) {
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-          proj_store16(p, m, n0 + c, v);
-        }
-      }
-    } else if (lane == 0) {
-      atomicExch(&flags[0], 1);
+      const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+      epilogue_tile(p, lane_addr + buf * BN, m0 + quarter * 32 + lane, n0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bs.acc_empty[buf]));
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (flags[0]) {
+  if (aborted(bs)) {
     if (threadIdx.x == 0) {
       report(p.status, DEV_WAIT_TIMEOUT);
-      // let copies that were issued but never consumed land before exit
-      for (int kb = flags[2]; kb < flags[1]; ++kb) mbar_wait(smem_u32(&full[kb % STAGES]), (kb / STAGES) & 1);
-      mbar_wait(smem_u32(acc_bar), 0);
+      // copies that were requested but never consumed land before exit
+      for (int it = bs.consumed; it < bs.issued; ++it)
+        mbar_wait(smem_u32(&bs.full[it % STAGES]), (it / STAGES) & 1);
     }
     __syncthreads();
   }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_tc(const GemmMaps& maps, const ProjParams& p, cudaStream_t s) {
+cudaError_t launch_gemm_tc(const GemmMaps& maps, const ProjParams& p, int ctas, cudaStream_t s) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -171,8 +304,10 @@ cudaError_t launch_gemm_tc(const GemmMaps& maps, const ProjParams& p, cudaStream
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  if (p.N % BN != 0 || p.r1 % BN != 0 || p.r2 % BN != 0) return cudaErrorInvalidValue;
-  const dim3 grid(p.N / BN, (p.M + BM - 1) / BM);
+  if (p.M <= 0 || p.N % BN != 0 || p.r1 % BN != 0 || p.r2 % BN != 0 || ctas <= 0) return cudaErrorInvalidValue;
+  const long long tiles = static_cast<long long>((p.M + BM - 1) / BM) * (p.N / BN);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const int grid = tiles < ctas ? static_cast<int>(tiles) : ctas;
   gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(maps.a, maps.b[0], maps.b[1], maps.b[2], p);
   return cudaGetLastError();
 }

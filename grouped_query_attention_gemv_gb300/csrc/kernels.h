@@ -102,12 +102,13 @@ __device__ __forceinline__ void proj_store2(const ProjParams& p, int m, int f, f
 }
 
 // ----------------------------------------------------------------- launches
-// tcgen05 GEMM for M > 64 tokens. Maps are created by the caller.
+// tcgen05 GEMM for M > 64 tokens, persistent over at most `ctas` CTAs (one
+// per SM). Maps are created by the caller.
 struct GemmMaps {
   CUtensorMap a;      // activations [M][4096]
   CUtensorMap b[3];   // w0, w1, w2
 };
-cudaError_t launch_gemm_tc(const GemmMaps& maps, const ProjParams& p, cudaStream_t s);
+cudaError_t launch_gemm_tc(const GemmMaps& maps, const ProjParams& p, int ctas, cudaStream_t s);
 constexpr int GEMM_BN = 256;
 constexpr int GEMM_BM = 128;
 

@@ -60,13 +60,9 @@ constexpr int XS_MAX = NST;              // token stages at most (all of a phase
 // from HBM wants most of shared memory for them (few token stages); one whose
 // weights are already in L2 but whose tokens only become ready when it starts
 // wants the tokens in flight instead.
-// L2_REST: once the weight ring is full, ask L2 for the rest of the CTA's
-// weights (for a phase whose first loads go out long before its tokens are
-// ready, so that HBM works through the wait).
-template <int NP_, int XS_ = (NP_ <= 16 ? 4 : (NP_ == 32 ? 3 : 2)), bool L2_REST_ = false>
+template <int NP_, int XS_ = (NP_ <= 16 ? 4 : (NP_ == 32 ? 3 : 2))>
 struct Cfg {
   static constexpr int NP = NP_;
-  static constexpr bool L2_REST = L2_REST_;
   static constexpr int B_BYTES = NP * KBLK * 2;      // one k block of the token tile
   static constexpr int X_STAGE = KC * B_BYTES;       // the token rows of one weight stage
   static constexpr int XS = XS_;                     // token stages
@@ -154,9 +150,6 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     int i = 0;
     for (; i < NST; ++i) {
       const int s = i % S, ks = (i + rot) % NST;
-      if (C_::L2_REST && i == S) {
-        for (int r = S; r < NST; ++r) tma_prefetch_3d(wmap, 0, mr.row0, ((r + rot) % NST) * KC);
-      }
       if (i >= S && !mbar_wait(smem_u32(&sh.empty[s]), ((i / S) & 1) ^ 1)) {
         atomicExch(&flags[0], 1);
         break;
