@@ -102,14 +102,14 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def kernel_traffic(name: str):
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+def kernel_traffic(name: str, workload: str):
+    """dram bytes per launch of kernel `name` at `workload` from the committed
+    ncu summary, if it was taken on the current kernel sources (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    ent = d.get(name)
+    ent = d.get(f"{name}@{workload}")
     if not ent:
         return None
     srcs = ent["source"] if isinstance(ent["source"], list) else [ent["source"]]
@@ -436,7 +436,7 @@ def main():
         e2e_value = world * w.B * a.steps / (ems / 1e3)
         achieved = work[dom] / (per_kernel[dom] / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": kernel_traffic(dom), "algorithmic_bytes_per_launch": work[dom],
+                "frac": achieved / hbm, "traffic": kernel_traffic(dom, w.name), "algorithmic_bytes_per_launch": work[dom],
                 "launch_ms": per_kernel[dom], "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}
         step_rate = {"step_hbm_gbs": work["step"] / (ms_step / 1e3) / 1e9}
         step_rate["step_hbm_frac"] = step_rate["step_hbm_gbs"] / hbm
@@ -447,7 +447,7 @@ def main():
         e2e_value = world * work["step"] * a.steps / (ems / 1e3) / 1e12
         achieved = work[dom] / (per_kernel[dom] / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
-                "frac": achieved / tflops, "traffic": kernel_traffic(dom), "algorithmic_flops_per_launch": work[dom],
+                "frac": achieved / tflops, "traffic": kernel_traffic(dom, w.name), "algorithmic_flops_per_launch": work[dom],
                 "launch_ms": per_kernel[dom], "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({peak_kind})"}
         step_rate = {"step_tflops": work["step"] / (ms_step / 1e3) / 1e12}
         step_rate["step_tensor_frac"] = step_rate["step_tflops"] / tflops

@@ -3,8 +3,10 @@
 // the "Query projection" page), K fixed at 4096.
 //
 // Persistent: one CTA per SM walks the 128 x 256 output tiles t = CTA,
-// CTA + grid, ... in n-major order (consecutive tiles share a weight tile, so
-// the weights come from HBM once and the re-reads hit L2):
+// CTA + grid, ... with the output features fastest: the CTAs in flight cover
+// a few token tiles against the whole weight matrix (50 MB for Q|K|V, which
+// L2 holds), so both x and W come from HBM once. (Token tiles fastest made
+// every wave sweep all of x: at 8192 tokens its 67 MB were read ~10 times.)
 //   warp 0 (one lane)   TMA producer: 128x64 x tile and 256x64 W tile per
 //                       stage, 128B-swizzled, 4-stage ring on mbarriers, one
 //                       ring across the CTA's tiles
@@ -158,8 +160,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int tiles_m = (p.M + BM - 1) / BM;
-  const int tiles = tiles_m * (p.N / BN);
+  const int tiles_n = p.N / BN;
+  const int tiles = ((p.M + BM - 1) / BM) * tiles_n;
   const int G = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < tiles; t += G) {
-        const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+        const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
         int brow;
         const CUtensorMap* mb = weight_of(p, &map_b0, &map_b1, &map_b2, n0, brow);
         for (int kb = 0; kb < NKB; ++kb, ++it) {
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+      const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
       epilogue_tile(p, lane_addr + buf * BN, m0 + quarter * 32 + lane, n0);
       tc_fence_before();
       __syncwarp();
