@@ -111,6 +111,9 @@ WORKLOADS = {
                  description="causal prefill, B=4, T=2048"),
         Workload("long_decode_b8_p131071", B=8, T=1, start_pos=131071, s_max=131072,
                  description="long-context decode, B=8, P=131071 (131,072 keys)"),
+        Workload("prefill_chunk_b1_t1024_p7168", B=1, T=1024, start_pos=7168, s_max=8192,
+                 description="chunked prefill: the last 1,024 tokens of an 8,192-token prompt "
+                             "after 7,168 cached positions"),
     ]
 }
 

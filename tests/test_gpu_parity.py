@@ -224,6 +224,40 @@ def test_prefill_then_decode_equals_longer_prefill(weights):
         assert np.abs(d1).max() <= 1
 
 
+def test_chunked_prefill_large_matches_oracle(weights):
+    """A 640-token chunk after 1800 cached positions: ragged against both the
+    32-position query tiles and the 64-key tiles (the diagonal tile straddles
+    the cached prefix); sampled query rows plus the first and the last."""
+    c = H.make_case(2, 640, [1800, 1800], 2440, weights=weights)
+    out, _ = run_prefill(c)
+    g = np.random.default_rng(1)
+    for b in range(c.B):
+        q = sorted(set(g.choice(c.T, 48, replace=False).tolist()) | {0, 31, 32, c.T - 1})
+        H.compare_sequence(c, out, b, query_rows=q)
+    H.check_canaries(c)
+
+
+@pytest.mark.parametrize("kind", ["decode", "prefill"])
+def test_llama3_unscaled_rope_block_matches_oracle(weights, kind):
+    """Llama 3 8B ("use_scaled_rope": false): same block, only the RoPE table
+    differs. Positions past the 8192-token original context, where the scaled
+    and unscaled tables disagree most; the scaled table's answer must then be
+    far from the GPU's (the table really is the unscaled one)."""
+    if kind == "decode":
+        c = H.make_case(3, 1, [9000, 12345, 8191], 12346, rope=I.LLAMA3_ROPE, weights=weights)
+        out, _ = run_decode(c)
+    else:
+        c = H.make_case(1, 96, [9000], 9096, rope=I.LLAMA3_ROPE, weights=weights)
+        out, _ = run_prefill(c)
+    for b in range(c.B):
+        H.compare_sequence(c, out, b)
+    H.check_canaries(c)
+    import dataclasses
+    scaled = dataclasses.replace(c, rope=I.LLAMA31_ROPE)
+    other, _, _ = H.oracle_sequence(scaled, 0)
+    assert H.rel_l2(H.f64(out[0]), other) > 0.1
+
+
 @pytest.mark.parametrize("name,rows", [("prefill_b1_t2048", None), ("prefill_b4_t2048", 192)])
 def test_prefill_workloads_full(weights, name, rows):
     w = I.workload(name)
