@@ -222,40 +222,47 @@ __global__ void __launch_bounds__(THREADS, 1)
       bs.issued = it;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16(BM, BN);
-      int it = 0, j = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < tiles; t += G, ++j) {
-        const int buf = j & 1;
-        if (j >= 2 && !mbar_wait(smem_u32(&bs.acc_empty[buf]), ((j >> 1) - 1) & 1)) {
+    // the whole warp runs the loop (descriptors stay warp-uniform); one
+    // elected lane issues the products and commits
+    const uint32_t idesc = umma_idesc_bf16(BM, BN);
+    int it = 0, j = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < tiles; t += G, ++j) {
+      const int buf = j & 1;
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.acc_empty[buf]), ((j >> 1) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + buf * BN;
+      for (int kb = 0; kb < NKB; ++kb, ++it) {
+        const int s = it % STAGES;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.full[s]), (it / STAGES) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + buf * BN;
-        for (int kb = 0; kb < NKB; ++kb, ++it) {
-          const int s = it % STAGES;
-          if (!mbar_wait(smem_u32(&bs.full[s]), (it / STAGES) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = sbase + s * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+        const uint32_t sa = sbase + s * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+        if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             umma_bf16(d, umma_desc_sw128(sa + k * 32), umma_desc_sw128(sb + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
           umma_commit(smem_u32(&bs.empty[s]));
         }
-        if (!ok) break;
-        umma_commit(smem_u32(&bs.acc_full[buf]));
+        __syncwarp();
       }
+      if (!ok) break;
+      if (elect_one()) umma_commit(smem_u32(&bs.acc_full[buf]));
+      __syncwarp();
+    }
+    if (lane == 0) {
       if (!ok) atomicExch(&bs.abort, 1);
       bs.consumed = it;
-      umma_commit(smem_u32(&bs.mma_done));
-      mbar_wait(smem_u32(&bs.mma_done), 0);
     }
+    if (elect_one()) umma_commit(smem_u32(&bs.mma_done));
+    __syncwarp();
+    mbar_wait(smem_u32(&bs.mma_done), 0);
   } else {
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
