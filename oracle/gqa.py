@@ -26,6 +26,11 @@ Readings of points the pages leave open are stated where they are used:
   * the cache holds K after RoPE and V as projected, both in bf16, laid out
     [B, S_max, n_kv_heads, d_h]; only the stored cache rows are rounded.
 
+The block's attention half with its residual (``rms_norm``,
+``layer_sequence_forward``, ``layer_forward``) follows the handoff excerpt
+h = x + attention(attention_norm(x)); RMSNorm's body is read as the usual
+root-mean-square normalisation (the pages do not print it).
+
 Parity status: every function here is pinned by the CPU tests (page
 figures, invariants, closed forms, brute force) except the exact values of
 the scaled-RoPE frequencies inside the interpolation band, which the pages
@@ -220,3 +225,37 @@ def block_forward(x: np.ndarray, weights: dict, start_pos, cache_k: np.ndarray,
         ck[b, sp[b]:sp[b] + T] = nk
         cv[b, sp[b]:sp[b] + T] = nv
     return delta, ck, cv
+
+
+def rms_norm(x: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
+    """attention_norm of the block: "Llama 3.1 8B · Grouped-query attention",
+    handoff excerpt (``RMSNorm(args.dim, eps=args.norm_eps)``, norm_eps 1e-05 in
+    the catalogue entry). The pages name the module without printing its body;
+    read as y_i = g_i x_i / sqrt(mean_j x_j^2 + eps) over the model dimension
+    (the last axis), float64, no intermediate rounding."""
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * weight
+
+
+def layer_sequence_forward(x: np.ndarray, norm_weight: np.ndarray, eps: float, wq: np.ndarray,
+                           wk: np.ndarray, wv: np.ndarray, wo: np.ndarray, start_pos: int,
+                           cached_k: np.ndarray, cached_v: np.ndarray, freqs: np.ndarray,
+                           n_heads: int, n_kv_heads: int, query_rows: Optional[Sequence[int]] = None):
+    """The block's attention half with its residual for one sequence:
+    h = x + attention(attention_norm(x)) (the handoff excerpt of "Llama 3.1 8B ·
+    Grouped-query attention"; "Llama 3 8B · Attention update", block-residuals).
+
+    Returns (h [len(query_rows), d], new_k, new_v) as ``sequence_forward``."""
+    rows = np.arange(x.shape[0]) if query_rows is None else np.asarray(query_rows, dtype=np.int64)
+    delta, new_k, new_v = sequence_forward(rms_norm(x, norm_weight, eps), wq, wk, wv, wo, start_pos,
+                                           cached_k, cached_v, freqs, n_heads, n_kv_heads, query_rows)
+    return x[rows] + delta, new_k, new_v
+
+
+def layer_forward(x: np.ndarray, norm_weight: np.ndarray, eps: float, weights: dict, start_pos,
+                  cache_k: np.ndarray, cache_v: np.ndarray, freqs: np.ndarray, n_heads: int,
+                  n_kv_heads: int):
+    """Whole batch of ``layer_sequence_forward``: returns (h [B, T, d], cache_k', cache_v')."""
+    delta, ck, cv = block_forward(rms_norm(x, norm_weight, eps), weights, start_pos, cache_k, cache_v,
+                                  freqs, n_heads, n_kv_heads)
+    return x + delta, ck, cv

@@ -30,6 +30,11 @@ MUTANTS = {
                        "v = rope_rotate((x @ wv.T).reshape(T, n_kv_heads, head_dim), cos[:, None, :], sin[:, None, :])"),
     "softmax_wrong_axis": ("return e / np.sum(e, axis=axis, keepdims=True)",
                                             "return e / np.sum(e, axis=0, keepdims=True)"),
+    "rms_mean_over_rows": ("ms = np.mean(x * x, axis=-1, keepdims=True)", "ms = np.mean(x * x, axis=0, keepdims=True)"),
+    "rms_no_sqrt": ("return x / np.sqrt(ms + eps) * weight", "return x / (ms + eps) * weight"),
+    "rms_eps_outside_sqrt": ("return x / np.sqrt(ms + eps) * weight", "return x / (np.sqrt(ms) + eps) * weight"),
+    "rms_weight_dropped": ("return x / np.sqrt(ms + eps) * weight", "return x / np.sqrt(ms + eps)"),
+    "residual_on_normalised_input": ("    return x + delta, ck, cv", "    return rms_norm(x, norm_weight, eps) + delta, ck, cv"),
 }
 
 
@@ -87,7 +92,26 @@ def pin_gqa_vs_mha(M):
     np.testing.assert_allclose(d1, d2, rtol=1e-12, atol=1e-14)
 
 
-PINS = (pin_brute, pin_scaled_frequencies, pin_gqa_vs_mha)
+def pin_rms_norm(M):
+    x = np.array([[2.5] * 8, [-0.125] * 8])
+    np.testing.assert_allclose(M.rms_norm(x, np.ones(8), 0.0), [[1.0] * 8, [-1.0] * 8], rtol=1e-15)
+    np.testing.assert_allclose(M.rms_norm(np.array([3.0, 4.0]), np.array([2.0, -0.5]), 3.5), [1.5, -0.5], rtol=1e-15)
+    rng = np.random.default_rng(5)
+    y = M.rms_norm(rng.standard_normal((3, 64)) * np.array([[0.01], [1.0], [300.0]]), np.ones(64), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-13)
+
+
+def pin_layer_residual(M):
+    rng = np.random.default_rng(6)
+    d, H, Hkv, hd = 16, 4, 2, 4
+    w, x, ck, cv = case(M, rng, d, H, Hkv, hd, 1, 3, 8, (0,))
+    w["wo"] = np.zeros_like(w["wo"])
+    g = M.bf16_round(1.0 + 0.1 * rng.standard_normal(d))
+    h, _, _ = M.layer_forward(x, g, 1e-5, w, 0, ck, cv, M.rope_frequencies(hd, 500000.0, True), H, Hkv)
+    np.testing.assert_array_equal(h, x)
+
+
+PINS = (pin_brute, pin_scaled_frequencies, pin_gqa_vs_mha, pin_rms_norm, pin_layer_residual)
 
 
 def test_unmutated_oracle_passes_every_pin():

@@ -312,3 +312,44 @@ def test_weight_orientation_is_out_by_in():
     assert w["wk"].shape == (8, 16)
     _, k, _ = run(w, x, [0], ck, cv, 4, 2)
     np.testing.assert_array_equal(k[0, 0].reshape(-1), O.bf16_round(w["wk"] @ x[0, 0]))
+
+
+# ------------------------------------------------------------------ attention_norm and the residual
+
+def test_rms_norm_closed_forms():
+    """A constant row normalises to +-1; a [3, 4] row with eps = 3.5 has
+    mean square 12.5 + 3.5 = 16, so it maps to [0.75, 1.0]; the weight
+    multiplies the normalised row feature by feature."""
+    x = np.array([[2.5] * 8, [-0.125] * 8])
+    np.testing.assert_allclose(O.rms_norm(x, np.ones(8), 0.0), [[1.0] * 8, [-1.0] * 8], rtol=1e-15)
+    np.testing.assert_allclose(O.rms_norm(np.array([3.0, 4.0]), np.ones(2), 3.5), [0.75, 1.0], rtol=1e-15)
+    g = np.array([2.0, -0.5])
+    np.testing.assert_allclose(O.rms_norm(np.array([3.0, 4.0]), g, 3.5), [1.5, -0.5], rtol=1e-15)
+
+
+def test_rms_norm_rows_have_unit_rms_and_ignore_scale():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 64)) * np.array([[0.01], [1.0], [300.0]])
+    y = O.rms_norm(x, np.ones(64), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(O.rms_norm(7.0 * x, np.ones(64), 0.0), y, rtol=1e-13)
+
+
+def test_layer_residual_is_the_input_when_the_output_projection_is_zero():
+    rng = np.random.default_rng(6)
+    d, H, Hkv, hd, T = 16, 4, 2, 4, 3
+    w = {k: O.bf16_round(rng.standard_normal(s) * d ** -0.5) for k, s in
+         (("wq", (H * hd, d)), ("wk", (Hkv * hd, d)), ("wv", (Hkv * hd, d)), ("wo", (d, H * hd)))}
+    x = O.bf16_round(rng.standard_normal((1, T, d)))
+    ck, cv = np.zeros((1, 8, Hkv, hd)), np.zeros((1, 8, Hkv, hd))
+    g = O.bf16_round(1.0 + 0.1 * rng.standard_normal(d))
+    fr = O.rope_frequencies(hd, 500000.0, True)
+    w0 = dict(w, wo=np.zeros_like(w["wo"]))
+    h, _, _ = O.layer_forward(x, g, 1e-5, w0, 0, ck, cv, fr, H, Hkv)
+    np.testing.assert_array_equal(h, x)
+    # with the projection back, h - x is the block on the normalised input
+    h, k2, _ = O.layer_forward(x, g, 1e-5, w, 0, ck, cv, fr, H, Hkv)
+    d2, k3, _ = O.block_forward(O.rms_norm(x, g, 1e-5), w, 0, ck, cv, fr, H, Hkv)
+    np.testing.assert_allclose(h - x, d2, rtol=1e-12, atol=1e-15)
+    np.testing.assert_array_equal(k2, k3)
+
