@@ -29,7 +29,8 @@ Readings of points the pages leave open are stated where they are used:
 The block's attention half with its residual (``rms_norm``,
 ``layer_sequence_forward``, ``layer_forward``) follows the handoff excerpt
 h = x + attention(attention_norm(x)); RMSNorm's body is read as the usual
-root-mean-square normalisation (the pages do not print it).
+root-mean-square normalisation (the pages do not print it), and its output,
+the attention's input tensor, is stored in bf16 like the block input.
 
 Parity status: every function here is pinned by the CPU tests (page
 figures, invariants, closed forms, brute force) except the exact values of
@@ -245,10 +246,16 @@ def layer_sequence_forward(x: np.ndarray, norm_weight: np.ndarray, eps: float, w
     h = x + attention(attention_norm(x)) (the handoff excerpt of "Llama 3.1 8B ·
     Grouped-query attention"; "Llama 3 8B · Attention update", block-residuals).
 
+    The normalised rows are the attention's input tensor and are stored in
+    bf16, as the block input x is: every module excerpt on the pages hands
+    its result back in its input's dtype (apply_rotary_emb, the softmax), so
+    they are rounded once here.
+
     Returns (h [len(query_rows), d], new_k, new_v) as ``sequence_forward``."""
     rows = np.arange(x.shape[0]) if query_rows is None else np.asarray(query_rows, dtype=np.int64)
-    delta, new_k, new_v = sequence_forward(rms_norm(x, norm_weight, eps), wq, wk, wv, wo, start_pos,
-                                           cached_k, cached_v, freqs, n_heads, n_kv_heads, query_rows)
+    xn = bf16_round(rms_norm(x, norm_weight, eps))
+    delta, new_k, new_v = sequence_forward(xn, wq, wk, wv, wo, start_pos, cached_k, cached_v, freqs, n_heads,
+                                           n_kv_heads, query_rows)
     return x[rows] + delta, new_k, new_v
 
 
@@ -256,6 +263,6 @@ def layer_forward(x: np.ndarray, norm_weight: np.ndarray, eps: float, weights: d
                   cache_k: np.ndarray, cache_v: np.ndarray, freqs: np.ndarray, n_heads: int,
                   n_kv_heads: int):
     """Whole batch of ``layer_sequence_forward``: returns (h [B, T, d], cache_k', cache_v')."""
-    delta, ck, cv = block_forward(rms_norm(x, norm_weight, eps), weights, start_pos, cache_k, cache_v,
+    delta, ck, cv = block_forward(bf16_round(rms_norm(x, norm_weight, eps)), weights, start_pos, cache_k, cache_v,
                                   freqs, n_heads, n_kv_heads)
     return x + delta, ck, cv

@@ -347,9 +347,9 @@ def test_layer_residual_is_the_input_when_the_output_projection_is_zero():
     w0 = dict(w, wo=np.zeros_like(w["wo"]))
     h, _, _ = O.layer_forward(x, g, 1e-5, w0, 0, ck, cv, fr, H, Hkv)
     np.testing.assert_array_equal(h, x)
-    # with the projection back, h - x is the block on the normalised input
+    # with the projection back, h - x is the block on the normalised input (stored in bf16)
     h, k2, _ = O.layer_forward(x, g, 1e-5, w, 0, ck, cv, fr, H, Hkv)
-    d2, k3, _ = O.block_forward(O.rms_norm(x, g, 1e-5), w, 0, ck, cv, fr, H, Hkv)
+    d2, k3, _ = O.block_forward(O.bf16_round(O.rms_norm(x, g, 1e-5)), w, 0, ck, cv, fr, H, Hkv)
     np.testing.assert_allclose(h - x, d2, rtol=1e-12, atol=1e-15)
     np.testing.assert_array_equal(k2, k3)
 
