@@ -31,7 +31,8 @@ import torch
 
 __all__ = [
     "Dims", "RopeConfig", "Workload", "WORKLOADS", "LLAMA31_8B", "LLAMA31_ROPE",
-    "LLAMA3_ROPE", "draw_weights", "draw_x", "draw_cache", "draw_start_positions",
+    "LLAMA3_ROPE", "draw_weights", "draw_x", "draw_cache", "draw_start_positions", "draw_norm_weight",
+    "NORM_EPS",
     "workload", "DEVICE_DRAW_THRESHOLD",
 ]
 
@@ -180,3 +181,17 @@ def draw_cache(B: int, s_max: int, filled_rows: Sequence[int], dims: Dims = LLAM
                 c[b, :p] = vals.to(torch.bfloat16)
         out.append(c)
     return out[0], out[1]
+
+
+# norm_eps of the catalogue entries
+NORM_EPS = 1e-5
+
+
+def draw_norm_weight(seed: int = 0, dims: Dims = LLAMA31_8B) -> torch.Tensor:
+    """attention_norm weight g [d_model] bf16: 1 + 0.1 N(0,1) from a CPU
+    generator seeded ``seed + 2`` (trained weights are not available; a
+    weight near 1 with spread keeps the normalised rows at the block's scale
+    and makes a dropped or misplaced g visible)."""
+    gen = torch.Generator("cpu").manual_seed(seed + 2)
+    return (1.0 + 0.1 * torch.randn(dims.d_model, generator=gen, dtype=torch.float32)).to(torch.bfloat16)
+

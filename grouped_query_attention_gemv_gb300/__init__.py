@@ -23,7 +23,7 @@ __all__ = [
     "GQAError", "D_MODEL", "N_HEADS", "N_KV_HEADS", "HEAD_DIM", "library_path", "lib",
     "exported_symbols", "workspace_bytes", "make_workspace", "rope_table", "block_forward",
     "decode", "prefill", "device_status", "last_launch_count", "set_profile_events",
-    "set_decode_fusion", "decode_static", "static_device_status", "STATIC_SCRATCH_BYTES",
+    "set_decode_fusion", "decode_static", "rms_norm", "layer_forward", "layer_decode", "static_device_status", "STATIC_SCRATCH_BYTES",
 ]
 
 D_MODEL, N_HEADS, N_KV_HEADS, HEAD_DIM = 4096, 32, 8, 128
@@ -41,6 +41,11 @@ _SIGNATURES = {
     "gqa_block_forward": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "gqa_prefill": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "gqa_decode": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
+    "gqa_rms_norm": (_i, [_vp, _i, _vp, ctypes.c_float, _vp, _vp]),
+    "gqa_layer_forward": (_i, [_vp, _i, _i, _i, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp,
+                               _vp, _sz, _vp]),
+    "gqa_layer_decode": (_i, [_vp, _i, _vp, _i, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp,
+                              _vp, _sz, _vp]),
     "gqa_strerror": (ctypes.c_char_p, [_i]),
     "gqa_last_launch_count": (_i, []),
     "gqa_set_decode_fusion": (_i, [_i]),
@@ -198,6 +203,49 @@ def decode(x, start_pos: torch.Tensor, max_start_pos: int, wq, wk, wv, wo, rope,
                          _p(workspace), workspace.numel(), _s(stream))
     if r:
         raise GQAError(r, "gqa_decode")
+    return out
+
+
+def rms_norm(x, norm_w, eps: float, out=None, stream=None) -> torch.Tensor:
+    """attention_norm of rows of 4096 features (bf16 in and out)."""
+    _check(x, "x", torch.bfloat16)
+    _check(norm_w, "norm_w", torch.bfloat16, (4096,))
+    if x.shape[-1] != 4096:
+        raise ValueError("x: last dimension must be 4096")
+    out = torch.empty_like(x) if out is None else out
+    _check(out, "out", torch.bfloat16, tuple(x.shape))
+    r = lib().gqa_rms_norm(_p(x), x.numel() // 4096, _p(norm_w), float(eps), _p(out), _s(stream))
+    if r:
+        raise GQAError(r, "gqa_rms_norm")
+    return out
+
+
+def layer_forward(x, start_pos: int, norm_w, eps: float, wq, wk, wv, wo, rope, cache_k, cache_v, out=None,
+                  workspace=None, stream=None) -> torch.Tensor:
+    """h = x + attention(RMSNorm(x)) for B sequences of T tokens after ``start_pos`` cached rows."""
+    B, out = _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, x.shape[1])
+    _check(norm_w, "norm_w", torch.bfloat16, (4096,))
+    workspace = _ws(workspace, B, x.shape[1], int(start_pos) + x.shape[1], x.device)
+    r = lib().gqa_layer_forward(_p(x), B, x.shape[1], int(start_pos), _p(norm_w), float(eps), _p(wq), _p(wk),
+                                _p(wv), _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1],
+                                _p(out), _p(workspace), workspace.numel(), _s(stream))
+    if r:
+        raise GQAError(r, "gqa_layer_forward")
+    return out
+
+
+def layer_decode(x, start_pos: torch.Tensor, max_start_pos: int, norm_w, eps: float, wq, wk, wv, wo, rope,
+                 cache_k, cache_v, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """One decode step of h = x + attention(RMSNorm(x)); ``start_pos`` as in ``decode``."""
+    B, out = _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, 1)
+    _check(start_pos, "start_pos", torch.int32, (B,))
+    _check(norm_w, "norm_w", torch.bfloat16, (4096,))
+    workspace = _ws(workspace, B, 1, max_start_pos + 1, x.device)
+    r = lib().gqa_layer_decode(_p(x), B, _p(start_pos), int(max_start_pos), _p(norm_w), float(eps), _p(wq),
+                               _p(wk), _p(wv), _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v),
+                               cache_k.shape[1], _p(out), _p(workspace), workspace.numel(), _s(stream))
+    if r:
+        raise GQAError(r, "gqa_layer_decode")
     return out
 
 

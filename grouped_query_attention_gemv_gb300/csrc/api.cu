@@ -180,6 +180,8 @@ int sm_count() {
 
 struct Call {
   const gqa_bf16* x;
+  const gqa_bf16* norm_w;  // layer entries: attention_norm weight (x is normalised first, then added back)
+  float eps;
   int B, T;
   StartPos sp;
   int max_keys;
@@ -212,7 +214,10 @@ ProjParams proj_params(const Call& c, bool qkv) {
   p.M = c.B * c.T;
   p.T = c.T;
   if (qkv) {
-    p.x = reinterpret_cast<const __nv_bfloat16*>(c.x);
+    // the layer entries project the normalised rows, which the norm kernel
+    // left in the attention-output buffer (the attention overwrites them
+    // only after this projection)
+    p.x = reinterpret_cast<const __nv_bfloat16*>(c.norm_w ? reinterpret_cast<const gqa_bf16*>(c.ws + c.L.o) : c.x);
     p.w0 = reinterpret_cast<const __nv_bfloat16*>(c.wq);
     p.w1 = reinterpret_cast<const __nv_bfloat16*>(c.wk);
     p.w2 = reinterpret_cast<const __nv_bfloat16*>(c.wv);
@@ -227,6 +232,7 @@ ProjParams proj_params(const Call& c, bool qkv) {
     p.r1 = p.r2 = p.N = D_MODEL;
     p.qkv = 0;
     p.out = reinterpret_cast<__nv_bfloat16*>(c.out);
+    p.resid = c.norm_w ? reinterpret_cast<const __nv_bfloat16*>(c.x) : nullptr;  // h = x + delta
   }
   p.cache_k = reinterpret_cast<__nv_bfloat16*>(c.cache_k);
   p.cache_v = reinterpret_cast<__nv_bfloat16*>(c.cache_v);
@@ -378,8 +384,23 @@ int run_decode_fused(const Call& c) {
   return GQA_OK;
 }
 
+// attention_norm of the layer entries: the normalised rows go to the
+// attention-output buffer of the workspace.
+int run_norm(const Call& c) {
+  const cudaError_t e = launch_rmsnorm(reinterpret_cast<const __nv_bfloat16*>(c.x),
+                                       reinterpret_cast<const __nv_bfloat16*>(c.norm_w), c.eps, c.B * c.T,
+                                       reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.o), c.stream);
+  if (e != cudaSuccess) return fail_cuda(e);
+  ++t_launches;
+  return GQA_OK;
+}
+
 int run_block(Call& c) {
   t_launches = 0;
+  if (c.norm_w) {
+    const int r = run_norm(c);
+    if (r != GQA_OK) return r;
+  }
   if (c.T == 1 && c.L.np && c.B <= FUSED_MAX_B && t_fused) {
     const int r = run_decode_fused(c);
     if (r != GQA_EINVAL) return r;
@@ -435,7 +456,8 @@ int gqa_rope_table(float* rope, int rows, double theta, int scaled, double facto
   return GQA_OK;
 }
 
-int gqa_block_forward(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* wq, const gqa_bf16* wk,
+static int block_call(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* norm_w, float eps,
+                      const gqa_bf16* wq, const gqa_bf16* wk,
                       const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
                       gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
                       void* stream) {
@@ -445,6 +467,8 @@ int gqa_block_forward(const gqa_bf16* x, int B, int T, int start_pos, const gqa_
   int r = check_common(x, B, T, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, out, workspace, max_keys,
                        workspace_bytes, &c.L);
   if (r != GQA_OK) return r;
+  c.norm_w = norm_w;
+  c.eps = eps;
   c.x = x;
   c.B = B;
   c.T = T;
@@ -464,6 +488,44 @@ int gqa_block_forward(const gqa_bf16* x, int B, int T, int start_pos, const gqa_
   return run_block(c);
 }
 
+// Arguments of the layer entries beyond the block's.
+static int check_layer(const gqa_bf16* x, const gqa_bf16* norm_w, float eps, const gqa_bf16* h) {
+  if (!norm_w || !(eps > 0.f) || !(eps < 1e30f)) return GQA_EINVAL;
+  if (!aligned16(norm_w)) return GQA_EALIGN;
+  if (h == x) return GQA_EINVAL;
+  return GQA_OK;
+}
+
+int gqa_rms_norm(const gqa_bf16* x, int M, const gqa_bf16* norm_w, float eps, gqa_bf16* y, void* stream) {
+  if (!x || !norm_w || !y || M <= 0 || !(eps > 0.f) || !(eps < 1e30f)) return GQA_EINVAL;
+  if (!aligned16(x) || !aligned16(norm_w) || !aligned16(y)) return GQA_EALIGN;
+  t_launches = 0;
+  const cudaError_t e = launch_rmsnorm(reinterpret_cast<const __nv_bfloat16*>(x),
+                                       reinterpret_cast<const __nv_bfloat16*>(norm_w), eps, M,
+                                       reinterpret_cast<__nv_bfloat16*>(y), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  t_launches = 1;
+  return GQA_OK;
+}
+
+int gqa_block_forward(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* wq, const gqa_bf16* wk,
+                      const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
+                      gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  return block_call(x, B, T, start_pos, nullptr, 0.f, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, out,
+                    workspace, workspace_bytes, stream);
+}
+
+int gqa_layer_forward(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* norm_w, float eps,
+                      const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo,
+                      const float* rope, int rope_rows, gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max,
+                      gqa_bf16* h, void* workspace, size_t workspace_bytes, void* stream) {
+  const int r = check_layer(x, norm_w, eps, h);
+  if (r != GQA_OK) return r;
+  return block_call(x, B, T, start_pos, norm_w, eps, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, h,
+                    workspace, workspace_bytes, stream);
+}
+
 int gqa_prefill(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* wq, const gqa_bf16* wk,
                 const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
                 gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes, void* stream) {
@@ -471,10 +533,11 @@ int gqa_prefill(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* 
                            workspace, workspace_bytes, stream);
 }
 
-int gqa_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos, const gqa_bf16* wq,
-               const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows,
-               gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace,
-               size_t workspace_bytes, void* stream) {
+static int decode_call(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos,
+                       const gqa_bf16* norm_w, float eps, const gqa_bf16* wq, const gqa_bf16* wk,
+                       const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
+                       gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
+                       void* stream) {
   if (!start_pos || max_start_pos < 0 || max_start_pos > (1 << 30)) return GQA_EINVAL;
   Call c{};
   const int max_keys = max_start_pos + 1;
@@ -482,6 +545,8 @@ int gqa_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start
                        workspace_bytes, &c.L);
   if (r != GQA_OK) return r;
   if ((reinterpret_cast<uintptr_t>(start_pos) & 3u) != 0) return GQA_EALIGN;
+  c.norm_w = norm_w;
+  c.eps = eps;
   c.x = x;
   c.B = B;
   c.T = 1;
@@ -499,6 +564,24 @@ int gqa_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start
   c.ws = static_cast<uint8_t*>(workspace);
   c.stream = static_cast<cudaStream_t>(stream);
   return run_block(c);
+}
+
+int gqa_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos, const gqa_bf16* wq,
+               const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows,
+               gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  return decode_call(x, B, start_pos, max_start_pos, nullptr, 0.f, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v,
+                     s_max, out, workspace, workspace_bytes, stream);
+}
+
+int gqa_layer_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos, const gqa_bf16* norm_w,
+                     float eps, const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo,
+                     const float* rope, int rope_rows, gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max,
+                     gqa_bf16* h, void* workspace, size_t workspace_bytes, void* stream) {
+  const int r = check_layer(x, norm_w, eps, h);
+  if (r != GQA_OK) return r;
+  return decode_call(x, B, start_pos, max_start_pos, norm_w, eps, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v,
+                     s_max, h, workspace, workspace_bytes, stream);
 }
 
 const char* gqa_strerror(int status) {

@@ -79,6 +79,21 @@ __device__ __forceinline__ void store32(__nv_bfloat16* dst, const float (&v)[16]
   reinterpret_cast<uint4*>(dst)[1] = hi;
 }
 
+// v[e] += src[e] for 16 bf16 values (16-byte aligned).
+__device__ __forceinline__ void add_bf16_16(float (&v)[16], const __nv_bfloat16* src) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint4 u = __ldg(s4 + h);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[8 * h + 2 * e] += bf16_lo(w[e]);
+      v[8 * h + 2 * e + 1] += bf16_hi(w[e]);
+    }
+  }
+}
+
 // Rotate the 8 pairs of v by (cos, sin) pairs cs[0..3] (two pairs per float4).
 __device__ __forceinline__ void rotate16(float (&v)[16], const float4* cs) {
 #pragma unroll
@@ -142,6 +157,10 @@ __device__ __forceinline__ void epilogue_tile(const ProjParams& p, uint32_t acc,
     if (rope) {
       rotate16(v0, cs + 4 * c);
       rotate16(v1, cs + 4 * c);
+    }
+    if (dst && p.resid) {  // the block's residual (plain store only)
+      add_bf16_16(v0, p.resid + static_cast<size_t>(m) * p.N + n0 + c * 16);
+      add_bf16_16(v1, p.resid + static_cast<size_t>(m) * p.N + n0 + 128 + c * 16);
     }
     if (dst) {
       store32(dst + c * 16, v0);

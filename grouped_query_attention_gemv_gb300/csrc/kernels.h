@@ -26,6 +26,7 @@ struct ProjParams {
   const float* rope;  // [rope_rows][64][2] (cos, sin)
   StartPos sp;
   int* status;
+  const __nv_bfloat16* resid;  // plain store only: [M][N] added to the output (the block's residual), or null
 };
 
 // Rotate pair (a, b) of feature f (even) by the table row `pos`.
@@ -214,6 +215,10 @@ struct DecodeFusedArgs {
   int ctas;                // one CTA per SM
 };
 cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s);
+
+// attention_norm: y[m] = g * x[m] / sqrt(mean(x[m]^2) + eps) for M rows of 4096.
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, float eps, int M, __nv_bfloat16* y,
+                           cudaStream_t s);
 
 cudaError_t launch_rope_table(float* rope, int rows, double theta, int scaled, double factor, double lo,
                               double hi, double ctx, cudaStream_t s);

@@ -108,6 +108,9 @@ __device__ __forceinline__ void store_tile(const ProjParams& p, int rt, int r, f
         }
       }
     }
+    if constexpr (!QKV) {
+      if (p.resid && m < p.M) v += __bfloat162float(p.resid[static_cast<size_t>(m) * p.N + f]);  // the block's residual
+    }
     stage[m * TILE_ROWS + r] = __float2bfloat16_rn(v);
   }
   asm volatile("bar.sync 1, 128;" ::: "memory");

@@ -322,6 +322,11 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
       }
     } else {
       dst = p.out + static_cast<size_t>(m) * p.N + f;
+      if (p.resid) {  // the block's residual
+        const uint32_t rv = *reinterpret_cast<const uint32_t*>(p.resid + static_cast<size_t>(m) * p.N + f);
+        x0 += bf16_lo(rv);
+        x1 += bf16_hi(rv);
+      }
     }
     *reinterpret_cast<uint32_t*>(dst) = pack_bf16(x0, x1);
   }

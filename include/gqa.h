@@ -141,6 +141,41 @@ int gqa_prefill(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* 
                 int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
                 void* stream);
 
+/* The attention half of a transformer block with its norm and residual: the
+ * TransformerBlock.forward excerpt of "Llama 3.1 8B · Grouped-query
+ * attention" (handoff) and "Llama 3 8B · Attention update"
+ * (block-residuals):
+ *     h = x + attention(attention_norm(x))
+ * attention_norm is RMSNorm over the 4096 features,
+ *     g_i x_i / sqrt(mean_j x_j^2 + eps)
+ * (norm_eps 1e-05 in the catalogue entries; the pages name the module but
+ * do not print its body), and attention() is gqa_block_forward's operation
+ * on the normalised rows.
+ *   x       [B, T, 4096] bf16, the block input (the residual stream)
+ *   norm_w  [4096] bf16, the RMSNorm weight g (16-byte aligned)
+ *   eps     finite, > 0
+ *   h       [B, T, 4096] bf16, x + delta_attn; must not be x itself
+ * Every other argument, the cache update and the error behaviour as in
+ * gqa_block_forward. One more kernel than gqa_block_forward (the norm). */
+int gqa_layer_forward(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* norm_w, float eps,
+                      const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo,
+                      const float* rope, int rope_rows, gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max,
+                      gqa_bf16* h, void* workspace, size_t workspace_bytes, void* stream);
+
+/* attention_norm alone: y[m] = g * x[m] / sqrt(mean(x[m]^2) + eps) for M rows
+ * of 4096 features (x, y [M, 4096] bf16, norm_w [4096] bf16, all 16-byte
+ * aligned; y may be x). The same kernel gqa_layer_forward runs first;
+ * computed in fp32, rounded once to bf16. */
+int gqa_rms_norm(const gqa_bf16* x, int M, const gqa_bf16* norm_w, float eps, gqa_bf16* y, void* stream);
+
+/* gqa_layer_forward for one decode step with a start position per sequence
+ * (start_pos, max_start_pos as in gqa_decode). */
+int gqa_layer_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos,
+                     const gqa_bf16* norm_w, float eps, const gqa_bf16* wq, const gqa_bf16* wk,
+                     const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows,
+                     gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max, gqa_bf16* h, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
 /* Static description of a return code (GQA_ECUDA appends the last CUDA
  * error name seen by this library on the calling thread). */
 const char* gqa_strerror(int status);

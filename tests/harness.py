@@ -79,6 +79,49 @@ def oracle_sequence(c: Case, b: int, query_rows=None):
                               freqs, 32, 8, query_rows)
 
 
+def oracle_layer_sequence(c: Case, b: int, g: torch.Tensor, eps: float, query_rows=None):
+    """Oracle h = x + attention(norm(x)) / new cache rows of sequence b."""
+    r = c.rope
+    freqs = O.rope_frequencies(128, r.theta, r.scaled, r.factor, r.low_freq_factor,
+                               r.high_freq_factor, r.original_context)
+    w = weights64(c)
+    sp = c.start[b]
+    ck = f64(c.dev["cache_k0"][b, :sp])
+    cv = f64(c.dev["cache_v0"][b, :sp])
+    return O.layer_sequence_forward(f64(c.host["x"][b]), f64(g), eps, w["wq"], w["wk"], w["wv"], w["wo"], sp,
+                                    ck, cv, freqs, 32, 8, query_rows)
+
+
+def compare_layer_sequence(c: Case, h: torch.Tensor, b: int, g: torch.Tensor, eps: float, xn: torch.Tensor,
+                           query_rows=None):
+    """Oracle vs GPU for the layer of sequence b: h against the oracle layer
+    (the delta bar); the written cache rows against the oracle block applied
+    to the GPU's own normalised rows ``xn`` (the 1-ulp bar). The normalised
+    rows are a bf16 rounding of a computed value, taken in fp32 on the GPU and
+    fp64 in the oracle: where the two land on neighbouring bf16 values, one
+    element's ulp times a weight moves a whole K row by up to ~6e-4, more than
+    an ulp of its small values, so the rows are checked from the same input."""
+    hl, _, _ = oracle_layer_sequence(c, b, g, eps, query_rows)
+    r = c.rope
+    freqs = O.rope_frequencies(128, r.theta, r.scaled, r.factor, r.low_freq_factor,
+                               r.high_freq_factor, r.original_context)
+    w = weights64(c)
+    sp = c.start[b]
+    _, nk, nv = O.sequence_forward(f64(xn[b]), w["wq"], w["wk"], w["wv"], w["wo"], sp,
+                                   f64(c.dev["cache_k0"][b, :sp]), f64(c.dev["cache_v0"][b, :sp]), freqs, 32, 8, [0])
+    rows = slice(None) if query_rows is None else list(query_rows)
+    got = f64(h[b])[rows]
+    r2 = rel_l2(got, hl)
+    ma = float(np.abs(got - hl).max())
+    assert np.isfinite(got).all(), f"non-finite output in sequence {b}"
+    assert r2 <= REL_L2_TOL, f"sequence {b}: rel L2 {r2:.3e} > {REL_L2_TOL}"
+    assert ma <= MAX_ABS_TOL, f"sequence {b}: max abs {ma:.3e} > {MAX_ABS_TOL}"
+    sp, T = c.start[b], c.T
+    check_rows_within_one_ulp(c.dev["cache_k"][b, sp:sp + T], nk, f"cache_k rows of sequence {b}")
+    check_rows_within_one_ulp(c.dev["cache_v"][b, sp:sp + T], nv, f"cache_v rows of sequence {b}")
+    return r2, ma
+
+
 def rel_l2(got: np.ndarray, ref: np.ndarray) -> float:
     return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
 

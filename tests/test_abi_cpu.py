@@ -107,3 +107,28 @@ def test_decode_static_rejects_requests_beyond_its_scratch(lib):
     assert r == -6
     assert b"static" in lib.gqa_strerror(-6)
     assert lib.gqa_decode_static(FAKE, 0, FAKE, 10, FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, FAKE, 64, FAKE, None) == -1
+
+
+def test_layer_entries_reject_bad_arguments(lib):
+    """Validation of the norm weight, eps and the output buffer happens on the
+    host before anything else (no device needed)."""
+    f = lib.gqa_layer_forward
+    ok = [FAKE, 1, 4, 0, FAKE, 1e-5, FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, FAKE, 64, FAKE + 4096, FAKE, 0, None]
+    for i, v, code in ((4, None, -1),          # no norm weight
+                       (5, 0.0, -1),           # eps must be > 0
+                       (5, -1e-5, -1),
+                       (5, float("nan"), -1),
+                       (4, FAKE + 8, -2),      # norm weight misaligned
+                       (15, FAKE, -1)):        # h is x itself
+        bad = list(ok)
+        bad[i] = v
+        assert f(*bad) == code, (i, v)
+    d = lib.gqa_layer_decode
+    okd = [FAKE, 4, FAKE, 10, FAKE, 1e-5, FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, FAKE, 64, FAKE + 4096, FAKE, 0,
+           None]
+    bad = list(okd)
+    bad[4] = None
+    assert d(*bad) == -1
+    bad = list(okd)
+    bad[15] = FAKE
+    assert d(*bad) == -1

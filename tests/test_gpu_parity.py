@@ -288,3 +288,67 @@ def test_large_decode_workloads_sampled(weights, name, sample):
             lo = max(0, sp - 64)
             assert torch.equal(now[lo:sp], before[lo:sp])
             assert torch.equal(now[sp + 1:sp + 65], before[sp + 1:sp + 65])
+
+
+# ------------------------------------------------------------------ the layer: h = x + attention(norm(x))
+
+@pytest.mark.parametrize("B,starts,s_max,fused", [
+    (16, [3, 40, 17, 100] * 4, 128, True),    # the fused decode grid
+    (16, [3, 40, 17, 100] * 4, 128, False),   # three kernels
+    (80, list(range(5, 85)), 100, True),      # above the fused grid's batch: tensor-core projections
+])
+def test_layer_decode_matches_oracle(weights, B, starts, s_max, fused):
+    c = H.make_case(B, 1, starts, s_max, weights=weights)
+    g = I.draw_norm_weight(seed=0).cuda()
+    d = c.dev
+    sp = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    ws = G.make_workspace(B, 1, max(starts) + 1)
+    prev = G.set_decode_fusion(fused)
+    try:
+        h = G.layer_decode(d["x"], sp, max(starts), g, I.NORM_EPS, d["wq"], d["wk"], d["wv"], d["wo"],
+                           H.rope_for(c), d["cache_k"], d["cache_v"], workspace=ws)
+        torch.cuda.synchronize()
+    finally:
+        G.set_decode_fusion(prev)
+    assert G.device_status(ws) == 0
+    xn = G.rms_norm(d["x"], g, I.NORM_EPS)
+    for b in range(0, B, max(1, B // 8)):
+        H.compare_layer_sequence(c, h, b, g, I.NORM_EPS, xn)
+    H.check_canaries(c)
+
+
+@pytest.mark.parametrize("B,T,start,s_max", [
+    (1, 5, 0, 8),         # few tokens: stream-K projections
+    (2, 37, 0, 40),       # tensor-core projections with a ragged tile
+    (1, 96, 300, 400),    # chunked
+])
+def test_layer_prefill_matches_oracle(weights, B, T, start, s_max):
+    c = H.make_case(B, T, [start] * B, s_max, weights=weights)
+    g = I.draw_norm_weight(seed=0).cuda()
+    d = c.dev
+    ws = G.make_workspace(B, T, start + T)
+    h = G.layer_forward(d["x"], start, g, I.NORM_EPS, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c),
+                        d["cache_k"], d["cache_v"], workspace=ws)
+    torch.cuda.synchronize()
+    assert G.device_status(ws) == 0
+    xn = G.rms_norm(d["x"], g, I.NORM_EPS)
+    for b in range(B):
+        H.compare_layer_sequence(c, h, b, g, I.NORM_EPS, xn)
+    H.check_canaries(c)
+    # the residual is really there: h - x is the normalised block's delta, not h
+    assert float((h.float() - d["x"].float()).abs().max()) < float(h.float().abs().max())
+
+
+def test_rms_norm_matches_oracle():
+    """The norm alone: every value within one bf16 ulp of the oracle's (fp32
+    arithmetic on the GPU, one rounding), nearly all identical; the x rows
+    span four orders of magnitude."""
+    gen = torch.Generator().manual_seed(11)
+    x = (torch.randn(64, 4096, generator=gen) * torch.logspace(-2, 2, 64).unsqueeze(1)).to(torch.bfloat16)
+    g = I.draw_norm_weight(seed=3)
+    y = G.rms_norm(x.cuda(), g.cuda(), I.NORM_EPS).cpu()
+    ref = O.bf16_round(O.rms_norm(H.f64(x), H.f64(g), I.NORM_EPS))
+    got = H.f64(y)
+    assert np.all(np.abs(got - ref) <= H.bf16_ulp(ref))
+    assert (got != ref).mean() < 1e-3
+
