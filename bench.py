@@ -57,6 +57,8 @@ def args_():
     ap.add_argument("--replicas", type=int, default=4)
     ap.add_argument("--graph-steps", type=int, default=8, help="steps captured per CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--entry", choices=["block", "layer"], default="block",
+                    help="block: delta = attention(x); layer: h = x + attention(RMSNorm(x)) (one more kernel)")
     ap.add_argument("--decode-kernels", choices=["fused", "three"], default="fused",
                     help="decode step as one persistent grid (default) or as three kernels")
     return ap.parse_args()
@@ -78,6 +80,7 @@ def step_bytes(B: int, starts) -> dict:
         "o_projection": 33554432 + B * 8192 + B * 8192,              # Wo, o, delta
         "step": WEIGHT_BYTES + kv_read + B * 4096 + 2 * B * 8192,    # the roofline's byte count
         "decode_step": WEIGHT_BYTES + kv_read + B * 4096 + 2 * B * 8192,  # the fused kernel: the whole step
+        "attention_norm": 2 * B * 8192 + 8192,                       # x in, normalised rows out, weight
     }
 
 
@@ -90,6 +93,7 @@ def step_flops(B: int, T: int, start: int) -> dict:
         "prefill_attention": 16384.0 * pairs,
         "o_projection": 2.0 * B * T * 4096 * 4096,
         "step": 2.0 * 41943040 * B * T + 16384.0 * pairs,
+        "attention_norm": 3.0 * B * T * 4096,
     }
 
 
@@ -257,6 +261,8 @@ def config_dict(w: I.Workload, a, starts):
          "parallelism": "replicas"}
     if w.T == 1:
         c["decode_kernels"] = a.decode_kernels
+    if getattr(a, "entry", "block") != "block":
+        c["entry"] = a.entry
     if w.start_pos is not None:
         c["start_pos"] = w.start_pos
     else:
@@ -317,12 +323,21 @@ def main():
     sp = torch.tensor(starts, dtype=torch.int32, device=dev)
     rope = G.rope_table(s_max, device=dev)
 
+    layer = a.entry == "layer"
+    norm_w = I.draw_norm_weight(seed=w.seed).to(dev)
+
     def step(i):
         # stream=None: the current stream (the capture stream while a graph is recorded)
         r = reps[i % R]
-        if decode:
+        if decode and layer:
+            G.layer_decode(r["x"], sp, max_start, norm_w, I.NORM_EPS, r["wq"], r["wk"], r["wv"], r["wo"], rope,
+                           r["ck"], r["cv"], out=r["out"], workspace=r["ws"])
+        elif decode:
             G.decode(r["x"], sp, max_start, r["wq"], r["wk"], r["wv"], r["wo"], rope, r["ck"], r["cv"],
                      out=r["out"], workspace=r["ws"])
+        elif layer:
+            G.layer_forward(r["x"], starts[0], norm_w, I.NORM_EPS, r["wq"], r["wk"], r["wv"], r["wo"], rope,
+                            r["ck"], r["cv"], out=r["out"], workspace=r["ws"])
         else:
             G.prefill(r["x"], starts[0], r["wq"], r["wk"], r["wv"], r["wo"], rope, r["ck"], r["cv"],
                       out=r["out"], workspace=r["ws"])
@@ -331,10 +346,13 @@ def main():
         step(i)
     torch.cuda.synchronize()
     per_step_launches = G.last_launch_count()
+    block_launches = per_step_launches - (1 if layer else 0)
     if decode:
-        kernels = ("decode_step",) if per_step_launches == 1 else KERNELS
+        kernels = ("decode_step",) if block_launches == 1 else KERNELS
     else:
         kernels = ("qkv_projection", "prefill_attention", "o_projection")
+    if layer:
+        kernels = ("attention_norm",) + kernels
     for r in reps:
         assert G.device_status(r["ws"]) == 0, "device status set during warm-up"
 
@@ -431,6 +449,8 @@ def main():
     dom = max(per_kernel, key=per_kernel.get)
     if decode:
         work = step_bytes(w.B, starts)
+        if a.entry == "layer":  # the norm's x in and rows out, the residual's x in
+            work["step"] += 3 * w.B * 8192 + 8192
         value = world * w.B * a.steps / (ms / 1e3)
         unit = "seq-steps/s"
         e2e_value = world * w.B * a.steps / (ems / 1e3)

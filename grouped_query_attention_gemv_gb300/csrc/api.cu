@@ -18,7 +18,9 @@ thread_local void* const* t_prof_events = nullptr;
 thread_local int t_prof_count = 0;
 thread_local int t_fused = 1;
 
+thread_local int t_prof_base = 0;  // 1 while a layer call's norm kernel occupies events[0..1]
 void prof_mark(int i, cudaStream_t s) {
+  i += t_prof_base;
   if (t_prof_events && i < t_prof_count && t_prof_events[i])
     cudaEventRecord(static_cast<cudaEvent_t>(t_prof_events[i]), s);
 }
@@ -397,9 +399,13 @@ int run_norm(const Call& c) {
 
 int run_block(Call& c) {
   t_launches = 0;
+  t_prof_base = 0;
   if (c.norm_w) {
+    prof_mark(0, c.stream);
     const int r = run_norm(c);
+    prof_mark(1, c.stream);
     if (r != GQA_OK) return r;
+    t_prof_base = 1;  // the block's kernels follow in the event list
   }
   if (c.T == 1 && c.L.np && c.B <= FUSED_MAX_B && t_fused) {
     const int r = run_decode_fused(c);
