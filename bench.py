@@ -346,12 +346,14 @@ def main():
         step(i)
     torch.cuda.synchronize()
     per_step_launches = G.last_launch_count()
-    block_launches = per_step_launches - (1 if layer else 0)
+    # a layer call adds the norm kernel, except where the fused decode grid folds it in
+    norm_kernel = layer and per_step_launches not in (1, 3)
+    block_launches = per_step_launches - (1 if norm_kernel else 0)
     if decode:
         kernels = ("decode_step",) if block_launches == 1 else KERNELS
     else:
         kernels = ("qkv_projection", "prefill_attention", "o_projection")
-    if layer:
+    if norm_kernel:
         kernels = ("attention_norm",) + kernels
     for r in reps:
         assert G.device_status(r["ws"]) == 0, "device status set during warm-up"

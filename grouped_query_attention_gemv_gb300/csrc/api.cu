@@ -211,7 +211,9 @@ int check_common(const gqa_bf16* x, int B, int T, const gqa_bf16* wq, const gqa_
   return GQA_OK;
 }
 
-ProjParams proj_params(const Call& c, bool qkv) {
+// fold_norm: the kernel applies attention_norm to x itself (the fused decode
+// grid); otherwise a layer call's projection reads the norm kernel's rows.
+ProjParams proj_params(const Call& c, bool qkv, bool fold_norm = false) {
   ProjParams p{};
   p.M = c.B * c.T;
   p.T = c.T;
@@ -219,7 +221,10 @@ ProjParams proj_params(const Call& c, bool qkv) {
     // the layer entries project the normalised rows, which the norm kernel
     // left in the attention-output buffer (the attention overwrites them
     // only after this projection)
-    p.x = reinterpret_cast<const __nv_bfloat16*>(c.norm_w ? reinterpret_cast<const gqa_bf16*>(c.ws + c.L.o) : c.x);
+    p.x = reinterpret_cast<const __nv_bfloat16*>(c.norm_w && !fold_norm ? reinterpret_cast<const gqa_bf16*>(c.ws + c.L.o)
+                                                                         : c.x);
+    p.norm_w = fold_norm ? reinterpret_cast<const __nv_bfloat16*>(c.norm_w) : nullptr;
+    p.eps = c.eps;
     p.w0 = reinterpret_cast<const __nv_bfloat16*>(c.wq);
     p.w1 = reinterpret_cast<const __nv_bfloat16*>(c.wk);
     p.w2 = reinterpret_cast<const __nv_bfloat16*>(c.wv);
@@ -368,7 +373,7 @@ int run_decode_fused(const Call& c) {
   const int o_rows[1] = {D_MODEL};
   if (!make_row_plan(3, qkv_rows, a.ctas, &a.qkv_plan) || !make_row_plan(1, o_rows, a.ctas, &a.o_plan))
     return GQA_EINVAL;
-  a.pq = proj_params(c, true);
+  a.pq = proj_params(c, true, /*fold_norm=*/true);
   a.po = proj_params(c, false);
   const gqa_bf16* wqkv[3] = {c.wq, c.wk, c.wv};
   const gqa_bf16* wo[1] = {c.wo};
@@ -400,16 +405,17 @@ int run_norm(const Call& c) {
 int run_block(Call& c) {
   t_launches = 0;
   t_prof_base = 0;
+  // the fused decode grid applies a layer call's norm itself
+  if (c.T == 1 && c.L.np && c.B <= FUSED_MAX_B && t_fused) {
+    const int r = run_decode_fused(c);
+    if (r != GQA_EINVAL) return r;
+  }
   if (c.norm_w) {
     prof_mark(0, c.stream);
     const int r = run_norm(c);
     prof_mark(1, c.stream);
     if (r != GQA_OK) return r;
     t_prof_base = 1;  // the block's kernels follow in the event list
-  }
-  if (c.T == 1 && c.L.np && c.B <= FUSED_MAX_B && t_fused) {
-    const int r = run_decode_fused(c);
-    if (r != GQA_EINVAL) return r;
   }
   prof_mark(0, c.stream);
   int r = run_projection(c, true, false);

@@ -91,7 +91,7 @@ struct Layout {
   static constexpr int RING = rowsk::RING_BYTES > attnk::RING ? rowsk::RING_BYTES : attnk::RING;
   static constexpr int PSET = 2 * rowsk::MAX_STAGES + 2 * rowsk::XS_MAX;   // barriers of one projection
   static constexpr int BARS = 2 * PSET + 2 * attnk::STAGES;                // two projections + attention
-  static constexpr int FIXED = RING + BARS * 8 + 16 * 4 + 1024;
+  static constexpr int FIXED = RING + BARS * 8 + 16 * 4 + FUSED_MAX_B * 4 + 1024;  // ..., flags, norm scales
   // the attention's output staging lies past its ring, inside the projections' ring
   static_assert(attnk::RING + attnk::STAGE_OUT_BYTES <= RING, "attention staging fits");
 };
@@ -110,7 +110,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   int* flags_a = ints + 4;
   int* flags_b = ints + 8;
   int* flags_c = ints + 12;
-  int* pre = ints + 16;
+  float* rs = reinterpret_cast<float*>(ints + 16);  // [FUSED_MAX_B] attention_norm scales (layer calls)
+  int* pre = ints + 16 + FUSED_MAX_B;
 
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   int* const cnt = fp.counters;
 
   // ---------------- phase A: Q|K|V projection, RoPE, cache append
-  const rowsk::Shared sha{smem, a_bars, a_bars + MS, a_bars + 2 * MS, a_bars + 2 * MS + XS, flags_a};
+  const rowsk::Shared sha{smem, a_bars, a_bars + MS, a_bars + 2 * MS, a_bars + 2 * MS + XS, flags_a, rs};
   // once its weight stream is requested, the CTA asks L2 for its first KV
   // stages after the ones phase B loads before its gate: HBM would otherwise
   // idle through this phase's epilogue and the grid wait
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   // ---------------- phase C: W_O projection. Its weight loads start at once;
   // meanwhile the compute warps meet the grid and merge the attention
   // outputs of split sequences; its token loads wait for every CTA's outputs.
-  const rowsk::Shared shc{smem, c_bars, c_bars + MS, c_bars + 2 * MS, c_bars + 2 * MS + XS, flags_c};
+  const rowsk::Shared shc{smem, c_bars, c_bars + MS, c_bars + 2 * MS, c_bars + 2 * MS + XS, flags_c, nullptr};
   if (!aborted && flags_b[0]) {
     // this CTA's units gave up: it still meets the grid (no other CTA waits in vain)
     if (warp < attnk::COMPUTE_WARPS) {

@@ -27,6 +27,8 @@ struct ProjParams {
   StartPos sp;
   int* status;
   const __nv_bfloat16* resid;  // plain store only: [M][N] added to the output (the block's residual), or null
+  const __nv_bfloat16* norm_w; // fused decode Q|K|V phase only: attention_norm weight applied to x, or null
+  float eps;
 };
 
 // Rotate pair (a, b) of feature f (even) by the table row `pos`.

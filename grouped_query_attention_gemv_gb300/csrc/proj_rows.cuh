@@ -40,6 +40,7 @@
 #pragma once
 
 #include "kernels.h"
+#include "norm_core.cuh"
 
 namespace gqa {
 namespace rowsk {
@@ -117,6 +118,7 @@ struct Shared {
   uint64_t* xfull;  // [XS_MAX], count 32 (the token producer's lanes)
   uint64_t* xempty; // [XS_MAX], count WARPS
   int* flags;       // [0] abort, [2] weight stages issued, [3] token stages issued
+  float* rs;        // [NP] attention_norm scale of each token (Q|K|V phase of a layer call), or null
 };
 
 // One projection phase. Roles: warps 0-7 compute, warp 8 lane 0 loads the
@@ -220,7 +222,41 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
   // wait gives up records it and leaves the loop. Every warp then meets the
   // others at the barrier after the loop, where the outcome is read.
   bool ok = prologue();
+  // attention_norm folded in (a layer call): each token's 1/rms from its raw
+  // row, while the first weight stages are in flight; the token fragments are
+  // then normalised feature by feature (x * r * g, one bf16 rounding, as the
+  // standalone norm kernel) just before the products
+  const bool norm = QKV && p.norm_w != nullptr;
+  float rn[C_::NT];
+  if (norm) {
+    for (int tok = warp; tok < NP; tok += WARPS) {
+      float r = 0.f;
+      if (tok < p.M) {
+        uint4 v[NORM_VEC];
+        norm_load_row(p.x + static_cast<size_t>(tok) * D_MODEL, lane, v);
+        r = norm_inv_rms(v, p.eps);
+      }
+      if (lane == 0) sh.rs[tok] = r;
+    }
+    asm volatile("bar.sync 4, 256;" ::: "memory");
+#pragma unroll
+    for (int nt = 0; nt < C_::NT; ++nt) rn[nt] = sh.rs[tok0 + nt * 8 + (lane >> 2)];
+  }
+  // norm weights of this warp's features, one stage ahead of their use
+  constexpr int NG = KS * 2;  // (KS / 2) k16 pairs x 4 chunks
+  uint32_t gnext[NG];
+  auto load_g = [&](int stage, uint32_t(&g)[NG]) {
+    const int kbase = (((stage + rot) % NST) * KC + kb) * KBLK + 2 * (lane & 3);
+#pragma unroll
+    for (int j = 0; j < NG; ++j)
+      g[j] = __ldg(reinterpret_cast<const uint32_t*>(p.norm_w + kbase + (2 * (ks0 + 2 * (j >> 2)) + (j & 3)) * 8));
+  };
+  if (norm) load_g(0, gnext);
   for (int i = 0; ok && i < NST; ++i) {
+    uint32_t gcur[NG];
+#pragma unroll
+    for (int j = 0; j < NG; ++j) gcur[j] = gnext[j];
+    if (norm && i + 1 < NST) load_g(i + 1, gnext);
     const int s = i % S, xs = i % XS;
     bool landed = mbar_wait(smem_u32(&sh.full[s]), (i / S) & 1);
     landed = landed && mbar_wait(smem_u32(&sh.xfull[xs]), (i / XS) & 1);
@@ -240,6 +276,15 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
       for (int nt = 0; nt < C_::NT; ++nt) {
         const int tr = tok0 + nt * 8 + (lane & 7);
         ldsm_x4(xb + sw128(tr, 2 * ks + (lane >> 3)), b[nt][0], b[nt][1], b[nt][2], b[nt][3]);
+      }
+      if (norm) {
+        // fragment q holds token tok0 + nt*8 + lane/4, features k, k+1 of chunk 2ks + q
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t g2 = gcur[((ks - ks0) >> 1) * 4 + q];
+#pragma unroll
+          for (int nt = 0; nt < C_::NT; ++nt) b[nt][q] = norm_pair(b[nt][q], rn[nt], g2);
+        }
       }
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
