@@ -200,19 +200,38 @@ def cpu_baseline(w: I.Workload, budget_s: float = 12.0):
     for b in range(w.B):
         per.append((x[b].to(torch.float64).numpy(), ck[b, :starts[b]].to(torch.float64).numpy(),
                     cv[b, :starts[b]].to(torch.float64).numpy(), starts[b]))
+    unit_step = _oracle_unit(w, O, W, freqs, per)
     n = 0
     t0 = time.perf_counter()
     while True:
-        xb, kb, vb, sp = per[n % w.B]
-        O.sequence_forward(xb, W["wq"], W["wk"], W["wv"], W["wo"], sp, kb, vb, freqs, 32, 8)
+        unit_step(n)
         n += 1
         el = time.perf_counter() - t0
         if el > budget_s or n >= 64 * w.B:
             break
     threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
-    return {"value": n / el, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n} single-sequence decode steps of {w.name} (whole sequences: projections, "
-                      f"attention over P+1 keys, output projection), {el:.1f} s, numpy float64"}
+    what = "layer steps (one sequence through one layer" if w.layers > 1 else "decode steps (whole sequences"
+    return {"value": n / el / w.layers, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} single-sequence {what}: projections, attention over P+1 keys, output projection) of "
+                      f"{w.name}, {el:.1f} s, numpy float64"
+                      + (f"; value = that rate / {w.layers} layers" if w.layers > 1 else "")}
+
+
+def _oracle_unit(w: I.Workload, O, W, freqs, per):
+    """One oracle unit of work: a sequence through the block (or, for a
+    multi-layer workload, through one layer with its norm and residual)."""
+    if w.layers > 1:
+        g = I.draw_norm_weight(seed=w.seed).to(torch.float64).numpy()
+
+        def unit(i):
+            xb, kb, vb, sp = per[i % w.B]
+            O.layer_sequence_forward(xb, g, I.NORM_EPS, W["wq"], W["wk"], W["wv"], W["wo"], sp, kb, vb, freqs, 32, 8)
+        return unit
+
+    def unit(i):
+        xb, kb, vb, sp = per[i % w.B]
+        O.sequence_forward(xb, W["wq"], W["wk"], W["wv"], W["wo"], sp, kb, vb, freqs, 32, 8)
+    return unit
 
 
 def run_reference(a, w: I.Workload, rank: int, world: int):
@@ -230,9 +249,11 @@ def run_reference(a, w: I.Workload, rank: int, world: int):
     per = [(x[b].to(torch.float64).numpy(), ck[b, :starts[b]].to(torch.float64).numpy(),
             cv[b, :starts[b]].to(torch.float64).numpy(), starts[b]) for b in range(w.B)]
 
-    def step(i):
-        xb, kb, vb, sp = per[i % w.B]
-        O.sequence_forward(xb, W["wq"], W["wk"], W["wv"], W["wo"], sp, kb, vb, freqs, 32, 8)
+    unit = _oracle_unit(w, O, W, freqs, per)
+
+    def step(i):   # one sequence through every layer
+        for _ in range(w.layers):
+            unit(i)
 
     for i in range(a.warmup):
         step(i)
@@ -250,7 +271,7 @@ def run_reference(a, w: I.Workload, rank: int, world: int):
                                              "d2h_bytes_per_step": 0},
         "cpu_baseline": {"value": val, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
                          "sample": f"each step: one sequence of {w.name} through the CPU oracle "
-                                   "(numpy float64, whole sequence)"},
+                                   f"(numpy float64, whole sequence, {w.layers} layer(s))"},
     }))
 
 
@@ -259,6 +280,11 @@ def config_dict(w: I.Workload, a, starts):
          "n_kv_heads": 8, "head_dim": 128,
          "l2": f"inputs larger than L2: {a.replicas} rotating replicas of weights+cache+x, one per step",
          "parallelism": "replicas"}
+    if w.layers > 1:
+        c["layers"] = w.layers
+        c["entry"] = "layer"
+        c["l2"] = (f"inputs larger than L2: {w.layers} layers, each with its own weights and cache, "
+                   "streamed back to back within a step")
     if w.T == 1:
         c["decode_kernels"] = a.decode_kernels
     if getattr(a, "entry", "block") != "block":
@@ -313,7 +339,10 @@ def main():
     gen, wt = I.draw_weights(seed=w.seed)
     x0 = I.draw_x(gen, w.B, w.T)
     ck0, cv0 = I.draw_cache(w.B, s_max, starts, seed=w.seed)
-    R = max(1, a.replicas)
+    L = w.layers
+    # a multi-layer step: one replica per layer (its own weights, cache and
+    # workspace), chained; the working set (L x 150 MB) is far above L2
+    R = L if L > 1 else max(1, a.replicas)
     max_start = max(starts)
     reps = []
     for _ in range(R):
@@ -323,11 +352,25 @@ def main():
     sp = torch.tensor(starts, dtype=torch.int32, device=dev)
     rope = G.rope_table(s_max, device=dev)
 
-    layer = a.entry == "layer"
+    layer = a.entry == "layer" or L > 1
     norm_w = I.draw_norm_weight(seed=w.seed).to(dev)
+    norms = [norm_w.clone() for _ in range(R)] if L > 1 else None
+
+    def in_buf(i):
+        return reps[0]["x"] if L > 1 else reps[i % R]["x"]
+
+    def out_buf(i):
+        return reps[-1]["out"] if L > 1 else reps[i % R]["out"]
 
     def step(i):
         # stream=None: the current stream (the capture stream while a graph is recorded)
+        if L > 1:
+            xin = reps[0]["x"]
+            for li, r in enumerate(reps):
+                G.layer_decode(xin, sp, max_start, norms[li], I.NORM_EPS, r["wq"], r["wk"], r["wv"], r["wo"], rope,
+                               r["ck"], r["cv"], out=r["out"], workspace=r["ws"])
+                xin = r["out"]
+            return
         r = reps[i % R]
         if decode and layer:
             G.layer_decode(r["x"], sp, max_start, norm_w, I.NORM_EPS, r["wq"], r["wk"], r["wv"], r["wo"], rope,
@@ -345,10 +388,11 @@ def main():
     for i in range(max(a.warmup, R)):
         step(i)
     torch.cuda.synchronize()
-    per_step_launches = G.last_launch_count()
+    per_step_launches = G.last_launch_count() * L
     # a layer call adds the norm kernel, except where the fused decode grid folds it in
-    norm_kernel = layer and per_step_launches not in (1, 3)
-    block_launches = per_step_launches - (1 if norm_kernel else 0)
+    launches_per_call = per_step_launches // L
+    norm_kernel = layer and launches_per_call not in (1, 3)
+    block_launches = launches_per_call - (1 if norm_kernel else 0)
     if decode:
         kernels = ("decode_step",) if block_launches == 1 else KERNELS
     else:
@@ -423,18 +467,17 @@ def main():
     xh = x0.pin_memory()
     oh = torch.empty_like(x0).pin_memory()
     for i in range(min(a.warmup, 5)):
-        reps[i % R]["x"].copy_(xh, non_blocking=True)
+        in_buf(i).copy_(xh, non_blocking=True)
         step(i)
-        oh.copy_(reps[i % R]["out"], non_blocking=True)
+        oh.copy_(out_buf(i), non_blocking=True)
     _barrier(world)
     torch.cuda.synchronize()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     for i in range(a.steps):
-        r = reps[i % R]
-        r["x"].copy_(xh, non_blocking=True)
+        in_buf(i).copy_(xh, non_blocking=True)
         step(i)
-        oh.copy_(r["out"], non_blocking=True)
+        oh.copy_(out_buf(i), non_blocking=True)
     f1.record(stream)
     torch.cuda.synchronize()
     _barrier(world)
@@ -451,8 +494,9 @@ def main():
     dom = max(per_kernel, key=per_kernel.get)
     if decode:
         work = step_bytes(w.B, starts)
-        if a.entry == "layer":  # the norm's x in and rows out, the residual's x in
+        if layer:  # the norm's x in and rows out, the residual's x in
             work["step"] += 3 * w.B * 8192 + 8192
+        work["step"] *= L   # per-kernel figures stay per launch (one layer)
         value = world * w.B * a.steps / (ms / 1e3)
         unit = "seq-steps/s"
         e2e_value = world * w.B * a.steps / (ems / 1e3)
@@ -487,6 +531,8 @@ def main():
                   f"replicas in turn); e2e calls the Python API per step",
         "clocks": clocks.summary(),
     }
+    if L > 1:
+        line["timing"] += f"; a step chains {L} layer calls (one replica per layer), kernels_ms is one layer's launch"
     if not a.no_cpu_baseline and world == 1 and decode:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line))

@@ -85,6 +85,7 @@ class Workload:
     s_max: Optional[int] = None       # cache rows per sequence
     seed: int = 0
     description: str = ""
+    layers: int = 1                   # consecutive blocks per step (each with its own weights and cache)
 
     def start_positions(self) -> torch.Tensor:
         if self.start_pos is not None:
@@ -112,6 +113,11 @@ WORKLOADS = {
                  description="causal prefill, B=4, T=2048"),
         Workload("long_decode_b8_p131071", B=8, T=1, start_pos=131071, s_max=131072,
                  description="long-context decode, B=8, P=131071 (131,072 keys)"),
+        Workload("decode32_b16_p1000", B=16, T=1, start_pos=1000, s_max=1001, layers=32,
+                 description="32 consecutive layers of one decode step at P=1000, B=16: the attention half "
+                             "of each block with its norm and residual (h = x + attention(RMSNorm(x))), each "
+                             "layer with its own weights and KV cache in device memory (copies of one seeded "
+                             "draw), the output of one the input of the next"),
         Workload("prefill_chunk_b1_t1024_p7168", B=1, T=1024, start_pos=7168, s_max=8192,
                  description="chunked prefill: the last 1,024 tokens of an 8,192-token prompt "
                              "after 7,168 cached positions"),

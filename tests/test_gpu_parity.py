@@ -352,3 +352,56 @@ def test_rms_norm_matches_oracle():
     assert np.all(np.abs(got - ref) <= H.bf16_ulp(ref))
     assert (got != ref).mean() < 1e-3
 
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_layer_decode_chained_layers_match_oracle(fused):
+    """Three consecutive layers of one decode step, each with its own weights
+    and KV cache, one shared workspace, the output of one the input of the
+    next: every layer against the oracle layer on that layer's GPU input, and
+    the whole chain against the oracle chained in fp64 (h rounded to bf16
+    between layers, as the block stores it; the max-abs bar widened by one
+    bf16 ulp of h per layer for those roundings)."""
+    B, starts, s_max, L = 4, [0, 17, 128, 300], 320, 3
+    cases = [H.make_case(B, 1, starts, s_max, seed=10 + l) for l in range(L)]
+    gs = [I.draw_norm_weight(seed=10 + l).cuda() for l in range(L)]
+    sp = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    ws = G.make_workspace(B, 1, max(starts) + 1)
+    prev = G.set_decode_fusion(fused)
+    try:
+        xs = [cases[0].dev["x"]]
+        for l, c in enumerate(cases):
+            d = c.dev
+            xs.append(G.layer_decode(xs[-1], sp, max(starts), gs[l], I.NORM_EPS, d["wq"], d["wk"], d["wv"], d["wo"],
+                                     H.rope_for(c), d["cache_k"], d["cache_v"], workspace=ws))
+        torch.cuda.synchronize()
+    finally:
+        G.set_decode_fusion(prev)
+    assert G.device_status(ws) == 0
+    for l, c in enumerate(cases):
+        c.host["x"] = xs[l].cpu()          # this layer's input, as the GPU saw it
+        xn = G.rms_norm(xs[l], gs[l], I.NORM_EPS)
+        for b in range(B):
+            H.compare_layer_sequence(c, xs[l + 1], b, gs[l], I.NORM_EPS, xn)
+        H.check_canaries(c)
+    r = I.LLAMA31_ROPE
+    freqs = O.rope_frequencies(128, r.theta, r.scaled, r.factor, r.low_freq_factor, r.high_freq_factor,
+                               r.original_context)
+    for b in range(B):
+        h = H.f64(cases[0].dev["x"][b])
+        for l, c in enumerate(cases):
+            w = H.weights64(c)
+            sp_b = starts[b]
+            h, _, _ = O.layer_sequence_forward(h, H.f64(gs[l]), I.NORM_EPS, w["wq"], w["wk"], w["wv"], w["wo"], sp_b,
+                                               H.f64(c.dev["cache_k0"][b, :sp_b]), H.f64(c.dev["cache_v0"][b, :sp_b]),
+                                               freqs, 32, 8)
+            h = O.bf16_round(h)
+        got = H.f64(xs[-1][b])
+        assert H.rel_l2(got, h) <= H.REL_L2_TOL
+        # both sides round h to bf16 after every layer: where they land on
+        # neighbouring values an element differs by one ulp of h (0.0625 for
+        # |h| in [8, 16)), and the residual carries that difference into the
+        # next layer's h unchanged, so L layers allow L ulps on top of the
+        # delta bar
+        err = np.abs(got - h) - L * H.bf16_ulp(np.abs(h))
+        assert float(err.max()) <= H.MAX_ABS_TOL
