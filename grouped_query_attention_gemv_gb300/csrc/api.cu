@@ -353,14 +353,15 @@ int run_attention(const Call& c) {
   return GQA_OK;
 }
 
-// Tensor maps of a row-owner projection: per matrix, boxes of its two row counts.
-bool row_maps(const gqa_bf16* const* w, const RowPlan& plan, RowMaps* m) {
+// Tensor maps of a row-owner projection: per matrix, boxes of its two row
+// counts; the token rows x (M of them), boxes of np rows.
+bool row_maps(const gqa_bf16* const* w, const RowPlan& plan, const void* x, int M, int np, RowMaps* m) {
   for (int i = 0; i < 3; ++i) {
     const int mi = i < plan.nmat ? i : 0;
     for (int hi = 0; hi < 2; ++hi)
       if (!map_rows_kblocks(&m->w[i][hi], w[mi], plan.rows[mi], plan.h_lo[mi] + 2 * hi, 4)) return false;
   }
-  return true;
+  return np > 0 && map_rows_kblocks(&m->x, x, M, np, 4);
 }
 
 // The whole decode step as one persistent grid (B <= FUSED_MAX_B). Returns
@@ -377,7 +378,9 @@ int run_decode_fused(const Call& c) {
   a.po = proj_params(c, false);
   const gqa_bf16* wqkv[3] = {c.wq, c.wk, c.wv};
   const gqa_bf16* wo[1] = {c.wo};
-  if (!row_maps(wqkv, a.qkv_plan, &a.qkv_maps) || !row_maps(wo, a.o_plan, &a.o_maps) ||
+  const int np = decode_fused_np(a.pq.M);
+  if (!row_maps(wqkv, a.qkv_plan, a.pq.x, a.pq.M, np, &a.qkv_maps) ||
+      !row_maps(wo, a.o_plan, a.po.x, a.po.M, np, &a.o_maps) ||
       !decode_cache_maps(c, &a.cache))
     return fail_cuda(cudaErrorInvalidValue);
   a.at = decode_attn_params(c);

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
         mbar_init(smem_u32(&set[MS + s]), rowsk::WARPS);
       }
       for (int s = 0; s < XS; ++s) {
-        mbar_init(smem_u32(&set[2 * MS + s]), 32);
+        mbar_init(smem_u32(&set[2 * MS + s]), 1);
         mbar_init(smem_u32(&set[2 * MS + XS + s]), rowsk::WARPS);
       }
     }
@@ -267,9 +267,13 @@ cudaError_t launch_fused_np(const DecodeFusedArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+int decode_fused_np(int M) {
+  return M <= 8 ? 8 : proj_stream_np(M);  // 8: half the tensor work of 16 padded tokens
+}
+
 cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
-  if (a.pq.M <= 8) return launch_fused_np<8>(a, s);  // half the tensor work of 16 padded tokens
-  switch (proj_stream_np(a.pq.M)) {
+  switch (decode_fused_np(a.pq.M)) {
+    case 8: return launch_fused_np<8>(a, s);
     case 16: return launch_fused_np<16>(a, s);
     case 32: return launch_fused_np<32>(a, s);
     case 64: return launch_fused_np<64>(a, s);

@@ -196,9 +196,11 @@ struct RowPlan {
 constexpr int ROWS_MAX_H = 48;   // rows one CTA can own (3 row tiles of 16)
 // Tensor maps over (64 k, row, k block) views of the weight matrices:
 // w[i][0] / w[i][1] are matrix i with boxes of 64 x h_lo[i] (or h_lo[i] + 2)
-// rows x 4 k blocks.
+// rows x 4 k blocks; x is the same view of the M token rows with boxes of 64 x
+// NP tokens x 4 k blocks (NP = decode_fused_np(M)).
 struct RowMaps {
   CUtensorMap w[3][2];
+  CUtensorMap x;
 };
 // Splits nmat matrices of the given row counts over `ctas` CTAs; false if a
 // CTA would own more than ROWS_MAX_H rows or a matrix gets no CTA.
@@ -217,6 +219,7 @@ struct DecodeFusedArgs {
   int ctas;                // one CTA per SM
 };
 cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s);
+int decode_fused_np(int M);   // padded tokens of the fused grid's projections (0 if M > 64)
 
 // attention_norm: y[m] = g * x[m] / sqrt(mean(x[m]^2) + eps) for M rows of 4096.
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* g, float eps, int M, __nv_bfloat16* y,

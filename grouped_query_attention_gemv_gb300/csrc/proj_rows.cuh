@@ -20,7 +20,11 @@
 //     row R = block * h + r at R * 128 bytes with the 128-byte swizzle of R,
 //     which ldmatrix addresses directly (the MMAs here need no tensor-core
 //     descriptor layout). The token rows of the same 4 k blocks (one box of 64
-//     k x NP tokens x 4 blocks) go to a separate ring: they come from L2;
+//     k x NP tokens x 4 blocks over the same view of x) go to a separate
+//     ring: they come from L2, and every CTA reads all of them. One TMA
+//     request a stage: 512 16-byte cp.async a stage through one warp issued
+//     at ~0.27 us a stage and bounded the W_O phase, whose tokens only
+//     become ready at its gate;
 //   * CTAs walk the 16 stages from different starting points: were they in
 //     step, every request in flight would fall in the same 512-byte window of
 //     the 8 KB weight rows;
@@ -115,7 +119,7 @@ struct Shared {
   uint8_t* ring;    // RING_BYTES, 1024-aligned: weight ring, then token ring
   uint64_t* full;   // [MAX_STAGES], count 1
   uint64_t* empty;  // [MAX_STAGES], count WARPS
-  uint64_t* xfull;  // [XS_MAX], count 32 (the token producer's lanes)
+  uint64_t* xfull;  // [XS_MAX], count 1 (expect-tx)
   uint64_t* xempty; // [XS_MAX], count WARPS
   int* flags;       // [0] abort, [2] weight stages issued, [3] token stages issued
   float* rs;        // [NP] attention_norm scale of each token (Q|K|V phase of a layer call), or null
@@ -123,7 +127,9 @@ struct Shared {
 
 // One projection phase. Roles: warps 0-7 compute, warp 8 lane 0 loads the
 // weights, warp 9 lane 0 the token rows; other lanes return at once. gate()
-// runs on the token producer before its first load (false = give up);
+// runs on the token producer before its first load (false = give up; it
+// orders the earlier phases' plain stores of the token rows before the
+// token producer's TMA reads);
 // prologue() runs on the 256 compute threads before they consume anything
 // (other work of the grid that may overlap the first weight loads; false =
 // give up); w_issued() runs on the weight producer once all its loads are
@@ -165,41 +171,25 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     return;
   }
   if (warp == WARPS + 1) {
-    // ---------------- token producer (the whole warp): the token rows may come
-    // from an earlier phase. They are small and in L2, and every CTA reads all
-    // of them, so they go through cp.async (16 bytes a lane) rather than the
-    // CTA's TMA queue, which the weight stream keeps busy. Rows past M are
-    // zero-filled. Each lane arrives on the stage's barrier once its copies
-    // land (count 32).
-    int okv = 1;
-    if (lane == 0) okv = gate() ? 1 : 0;
-    okv = __shfl_sync(0xffffffffu, okv, 0);  // lane 0 acquired the gate; the shuffle orders the others after it
-    __syncwarp();
-    bool ok = okv != 0;
+    if (lane != 0) return;
+    // ---------------- token producer: the token rows may come from an earlier
+    // phase (gate() waits for them). Rows past M read as zero (the map's rows
+    // end at M).
+    tma_prefetch_desc(&maps.x);
+    bool ok = gate();
     int i = 0;
-    constexpr int CHUNKS = KC * NP * 8;  // 16-byte pieces of one token stage
     for (; ok && i < NST; ++i) {
       const int s = i % XS, ks = (i + rot) % NST;
-      if (i >= XS) {
-        const bool freed = mbar_wait(smem_u32(&sh.xempty[s]), ((i / XS) & 1) ^ 1);
-        if (!__all_sync(0xffffffffu, freed)) {
-          ok = false;
-          break;
-        }
+      if (i >= XS && !mbar_wait(smem_u32(&sh.xempty[s]), ((i / XS) & 1) ^ 1)) {
+        ok = false;
+        break;
       }
-      const uint32_t dst = smem_u32(xring + s * C_::X_STAGE);
-#pragma unroll 4
-      for (int c = lane; c < CHUNKS; c += 32) {
-        const int kb = c / (NP * 8), rem = c - kb * NP * 8;
-        const int tok = rem >> 3, ch = rem & 7;
-        const bool real = tok < p.M;
-        const __nv_bfloat16* src = p.x + static_cast<size_t>(real ? tok : 0) * D_MODEL + (ks * KC + kb) * KBLK + ch * 8;
-        cp_async_16(dst + kb * C_::B_BYTES + sw128(tok, ch), src, real ? 16 : 0);
-      }
-      cp_async_mbar_arrive(smem_u32(&sh.xfull[s]));
+      const uint32_t fb = smem_u32(&sh.xfull[s]);
+      mbar_expect_tx(fb, C_::X_STAGE);
+      tma_load_3d(smem_u32(xring + s * C_::X_STAGE), &maps.x, fb, 0, 0, ks * KC);
     }
-    if (!ok && lane == 0) atomicExch(&flags[0], 1);
-    if (lane == 0) flags[3] = i;
+    if (!ok) atomicExch(&flags[0], 1);
+    flags[3] = i;
     return;
   }
   if (warp > WARPS + 1) return;
