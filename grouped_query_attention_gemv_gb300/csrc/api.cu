@@ -560,6 +560,10 @@ static int decode_call(const gqa_bf16* x, int B, const int32_t* start_pos, int m
                        workspace_bytes, &c.L);
   if (r != GQA_OK) return r;
   if ((reinterpret_cast<uintptr_t>(start_pos) & 3u) != 0) return GQA_EALIGN;
+  // the attention splits its units over the grid in 32-bit arithmetic
+  const unsigned long long units = static_cast<unsigned long long>(B) * ((max_keys + DECODE_UNIT - 1) / DECODE_UNIT);
+  if ((units + 1) * (static_cast<unsigned long long>(attn_decode_ctas(launch_sms())) + 1) >= (1ull << 32))
+    return GQA_EINVAL;
   c.norm_w = norm_w;
   c.eps = eps;
   c.x = x;

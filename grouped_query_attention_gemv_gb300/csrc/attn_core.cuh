@@ -78,10 +78,17 @@ __device__ __forceinline__ Cursor locate(long long u, const int* pre, int B) {
   return Cursor{lo, static_cast<int>(u - pre[lo])};
 }
 
+// Units split over the grid: CTA c takes units [U c / C, U (c + 1) / C).
+// Calls are refused unless (units + 1) x (CTAs + 1) < 2^32, so 32-bit
+// unsigned arithmetic is exact here (a 64-bit division is a long software
+// sequence, and a merge takes one per partial it reads).
 __device__ __forceinline__ int cta_of(long long u, long long U, long long C) {
-  return static_cast<int>(((u + 1) * C + U - 1) / U) - 1;
+  const uint32_t uu = static_cast<uint32_t>(u), UU = static_cast<uint32_t>(U), CC = static_cast<uint32_t>(C);
+  return static_cast<int>(((uu + 1) * CC + UU - 1) / UU) - 1;
 }
-__device__ __forceinline__ long long range_start(long long c, long long U, long long C) { return U * c / C; }
+__device__ __forceinline__ long long range_start(long long c, long long U, long long C) {
+  return static_cast<uint32_t>(U) * static_cast<uint32_t>(c) / static_cast<uint32_t>(C);
+}
 
 // Units per sequence prefix-summed into pre[0..B]; returns (on every lane) the
 // number of sequences with a valid start position. Run by one whole warp.

@@ -114,16 +114,31 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   int* pre = ints + 16 + FUSED_MAX_B;
 
   const int warp = threadIdx.x >> 5;
+  const rowsk::Shared sha{smem, a_bars, a_bars + MS, a_bars + 2 * MS, a_bars + 2 * MS + XS, flags_a, rs};
+  // phase A needs nothing from the grid: its two producers set up their own
+  // barriers and request their first stages at once, before the CTA's setup
+  // (the prefix of attention units reads the start positions) is done
+  int a_started = 0;
+  if (threadIdx.x == rowsk::WARPS * 32 || threadIdx.x == (rowsk::WARPS + 1) * 32) {
+    const bool wprod = threadIdx.x == rowsk::WARPS * 32;
+    const int n = wprod ? MS : XS;
+    uint64_t* fullb = wprod ? sha.full : sha.xfull;
+    uint64_t* emptyb = wprod ? sha.empty : sha.xempty;
+    for (int s = 0; s < n; ++s) {
+      mbar_init(smem_u32(&fullb[s]), 1);
+      mbar_init(smem_u32(&emptyb[s]), rowsk::WARPS);
+    }
+    fence_barrier_init();
+    a_started = rowsk::rows_start<CfgA<NP>>(m.qkv, fp.qkv_plan, sha);
+  }
   if (threadIdx.x == 0) {
-    for (uint64_t* set : {a_bars, c_bars}) {
-      for (int s = 0; s < MS; ++s) {
-        mbar_init(smem_u32(&set[s]), 1);
-        mbar_init(smem_u32(&set[MS + s]), rowsk::WARPS);
-      }
-      for (int s = 0; s < XS; ++s) {
-        mbar_init(smem_u32(&set[2 * MS + s]), 1);
-        mbar_init(smem_u32(&set[2 * MS + XS + s]), rowsk::WARPS);
-      }
+    for (int s = 0; s < MS; ++s) {
+      mbar_init(smem_u32(&c_bars[s]), 1);
+      mbar_init(smem_u32(&c_bars[MS + s]), rowsk::WARPS);
+    }
+    for (int s = 0; s < XS; ++s) {
+      mbar_init(smem_u32(&c_bars[2 * MS + s]), 1);
+      mbar_init(smem_u32(&c_bars[2 * MS + XS + s]), rowsk::WARPS);
     }
     for (int s = 0; s < attnk::STAGES; ++s) {
       mbar_init(smem_u32(&b_bars[s]), 1);
@@ -132,13 +147,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
     for (int i = 0; i < 4; ++i) flags_a[i] = flags_b[i] = flags_c[i] = 0;
     fence_barrier_init();
   }
-  if (warp == attnk::COMPUTE_WARPS) attnk::build_prefix(fp.at, pre);
+  if (warp == rowsk::WARPS - 1) attnk::build_prefix(fp.at, pre);
   __syncthreads();
   const int grid = static_cast<int>(gridDim.x);
   int* const cnt = fp.counters;
 
   // ---------------- phase A: Q|K|V projection, RoPE, cache append
-  const rowsk::Shared sha{smem, a_bars, a_bars + MS, a_bars + 2 * MS, a_bars + 2 * MS + XS, flags_a, rs};
   // once its weight stream is requested, the CTA asks L2 for its first KV
   // stages after the ones phase B loads before its gate: HBM would otherwise
   // idle through this phase's epilogue and the grid wait
@@ -147,7 +161,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
       [&fp, &m, pre]() {
         attnk::prefetch_units(&m.cache.k, &m.cache.v, fp.at, pre, attnk::STAGES, KV_PREFETCH_UNITS);
       },
-      [cnt]() { signal_counter(&cnt[0], 1); });
+      [cnt]() { signal_counter(&cnt[0], 1); }, a_started);
   fence_proxy_async_smem();  // the ring's generic reads and writes precede phase B's TMA writes into it
   __syncthreads();
   bool aborted = flags_a[0] != 0;
@@ -200,7 +214,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
                                          if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
                                          return ok;
                                        },
-                                       []() {}, []() {});
+                                       []() {}, []() {}, 0);
   }
   aborted = aborted || flags_b[0] != 0;
   __syncthreads();

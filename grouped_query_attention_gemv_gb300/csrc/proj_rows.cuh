@@ -125,6 +125,44 @@ struct Shared {
   float* rs;        // [NP] attention_norm scale of each token (Q|K|V phase of a layer call), or null
 };
 
+// One weight stage (i-th of this CTA's walk) into ring slot i % S.
+__device__ __forceinline__ void issue_w_stage(const CUtensorMap* wmap, const Shared& sh, int i, int S, int wstage,
+                                              const MyRows& mr, int rot) {
+  const int s = i % S, ks = (i + rot) % NST;
+  const uint32_t fb = smem_u32(&sh.full[s]);
+  mbar_expect_tx(fb, KC * mr.h * 128);
+  tma_load_3d(smem_u32(sh.ring + s * wstage), wmap, fb, 0, mr.row0, ks * KC);
+}
+// The token rows of stage i into token slot i % XS.
+template <class C_>
+__device__ __forceinline__ void issue_x_stage(const CUtensorMap* xmap, const Shared& sh, int i, int rot) {
+  const int s = i % C_::XS, ks = (i + rot) % NST;
+  const uint32_t fb = smem_u32(&sh.xfull[s]);
+  mbar_expect_tx(fb, C_::X_STAGE);
+  tma_load_3d(smem_u32(sh.ring + C_::W_RING + s * C_::X_STAGE), xmap, fb, 0, 0, ks * KC);
+}
+__device__ __forceinline__ int ring_stages(int w_ring, const RowPlan& plan) {
+  return min(MAX_STAGES, (w_ring - OVERREAD) / wstage_bytes(plan));
+}
+
+// Starts a phase's streams before the rest of the CTA is ready, for a phase
+// that needs nothing from earlier phases: run by the weight producer (warp
+// 8 lane 0) or the token producer (warp 9 lane 0) right after it has
+// initialised its own barriers; it fills its ring and returns the stages
+// requested, which rows_phase then skips.
+template <class C_>
+__device__ __forceinline__ int rows_start(const RowMaps& maps, const RowPlan& plan, const Shared& sh) {
+  const MyRows mr = my_rows(plan, blockIdx.x);
+  const int rot = (blockIdx.x * 7) % NST;
+  if ((threadIdx.x >> 5) == WARPS) {
+    const int S = ring_stages(C_::W_RING, plan);
+    for (int i = 0; i < S; ++i) issue_w_stage(&maps.w[mr.mat][mr.hi], sh, i, S, wstage_bytes(plan), mr, rot);
+    return S;
+  }
+  for (int i = 0; i < C_::XS; ++i) issue_x_stage<C_>(&maps.x, sh, i, rot);
+  return C_::XS;
+}
+
 // One projection phase. Roles: warps 0-7 compute, warp 8 lane 0 loads the
 // weights, warp 9 lane 0 the token rows; other lanes return at once. gate()
 // runs on the token producer before its first load (false = give up; it
@@ -134,18 +172,19 @@ struct Shared {
 // (other work of the grid that may overlap the first weight loads; false =
 // give up); w_issued() runs on the weight producer once all its loads are
 // requested; rows_done() runs on thread 0 once this CTA's rows are written
-// and fenced.
+// and fenced. `started`: the stages the calling producer thread already
+// requested in rows_start (0 if none).
 template <class C_, bool QKV, class Gate, class Prologue, class WIssued, class RowsDone>
 __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams& p, const RowPlan& plan,
                                            const Shared& sh, Gate gate, Prologue prologue, WIssued w_issued,
-                                           RowsDone rows_done) {
+                                           RowsDone rows_done, int started) {
   constexpr int NP = C_::NP;
   constexpr int XS = C_::XS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const MyRows mr = my_rows(plan, blockIdx.x);
   const int rot = (blockIdx.x * 7) % NST;  // this CTA's first k stage
   const int wstage = wstage_bytes(plan);
-  const int S = min(MAX_STAGES, (C_::W_RING - OVERREAD) / wstage);
+  const int S = ring_stages(C_::W_RING, plan);
   uint8_t* const xring = sh.ring + C_::W_RING;
   int* flags = sh.flags;
 
@@ -153,18 +192,14 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     if (lane != 0) return;
     // ---------------- weight producer: needs nothing from earlier phases
     const CUtensorMap* wmap = &maps.w[mr.mat][mr.hi];
-    tma_prefetch_desc(wmap);
-    const uint32_t bytes = KC * mr.h * 128;
-    int i = 0;
+    if (started == 0) tma_prefetch_desc(wmap);
+    int i = started;
     for (; i < NST; ++i) {
-      const int s = i % S, ks = (i + rot) % NST;
-      if (i >= S && !mbar_wait(smem_u32(&sh.empty[s]), ((i / S) & 1) ^ 1)) {
+      if (i >= S && !mbar_wait(smem_u32(&sh.empty[i % S]), ((i / S) & 1) ^ 1)) {
         atomicExch(&flags[0], 1);
         break;
       }
-      const uint32_t fb = smem_u32(&sh.full[s]);
-      mbar_expect_tx(fb, bytes);
-      tma_load_3d(smem_u32(sh.ring + s * wstage), wmap, fb, 0, mr.row0, ks * KC);
+      issue_w_stage(wmap, sh, i, S, wstage, mr, rot);
     }
     flags[2] = i;
     if (i == NST) w_issued();
@@ -175,18 +210,15 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     // ---------------- token producer: the token rows may come from an earlier
     // phase (gate() waits for them). Rows past M read as zero (the map's rows
     // end at M).
-    tma_prefetch_desc(&maps.x);
+    if (started == 0) tma_prefetch_desc(&maps.x);
     bool ok = gate();
-    int i = 0;
+    int i = started;
     for (; ok && i < NST; ++i) {
-      const int s = i % XS, ks = (i + rot) % NST;
-      if (i >= XS && !mbar_wait(smem_u32(&sh.xempty[s]), ((i / XS) & 1) ^ 1)) {
+      if (i >= XS && !mbar_wait(smem_u32(&sh.xempty[i % XS]), ((i / XS) & 1) ^ 1)) {
         ok = false;
         break;
       }
-      const uint32_t fb = smem_u32(&sh.xfull[s]);
-      mbar_expect_tx(fb, C_::X_STAGE);
-      tma_load_3d(smem_u32(xring + s * C_::X_STAGE), &maps.x, fb, 0, 0, ks * KC);
+      issue_x_stage<C_>(&maps.x, sh, i, rot);
     }
     if (!ok) atomicExch(&flags[0], 1);
     flags[3] = i;
@@ -242,6 +274,31 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
       g[j] = __ldg(reinterpret_cast<const uint32_t*>(p.norm_w + kbase + (2 * (ks0 + 2 * (j >> 2)) + (j & 3)) * 8));
   };
   if (norm) load_g(0, gnext);
+  // the epilogue's first EPF items of this thread (item = (row pair, token)):
+  // their start positions and RoPE factors are loaded now, so that the
+  // loads' latency is spent under the stream rather than after it
+  const int fbase = (mr.mat == 0 ? 0 : (mr.mat == 1 ? p.r1 : p.r2)) + mr.row0;  // feature of row 0
+  const int items = (mr.h / 2) * p.M;
+  constexpr int EPF = 2;
+  int pos_pf[EPF];
+  float2 cs_pf[EPF];
+#pragma unroll
+  for (int k = 0; k < EPF; ++k) {
+    pos_pf[k] = -1;
+    cs_pf[k] = make_float2(1.f, 0.f);
+    const int idx = threadIdx.x + k * WARPS * 32;
+    if (QKV && idx < items) {
+      const int m = idx % p.M, f = fbase + 2 * (idx / p.M);
+      const int b = m / p.T;
+      const int start = p.sp.get(b);
+      if (p.sp.ok(start)) {
+        pos_pf[k] = start + (m - b * p.T);
+        if (f < D_MODEL + KV_ROW)
+          cs_pf[k] = *reinterpret_cast<const float2*>(
+              p.rope + (static_cast<size_t>(pos_pf[k]) * ROPE_PAIRS + ((f & (HEAD_DIM - 1)) >> 1)) * 2);
+      }
+    }
+  }
   for (int i = 0; ok && i < NST; ++i) {
     uint32_t gcur[NG];
 #pragma unroll
@@ -323,8 +380,7 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
   }
   asm volatile("bar.sync 4, 256;" ::: "memory");
   // epilogue: thread -> (row pair, token)
-  const int fbase = (mr.mat == 0 ? 0 : (mr.mat == 1 ? p.r1 : p.r2)) + mr.row0;  // feature of row 0
-  for (int idx = threadIdx.x; idx < (mr.h / 2) * p.M; idx += WARPS * 32) {
+  auto item = [&](int idx, int pos, float2 cs) {
     const int m = idx % p.M, pr = idx / p.M;
     const int r = 2 * pr, f = fbase + r;
     float x0 = 0.f, x1 = 0.f;
@@ -337,13 +393,9 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     }
     __nv_bfloat16* dst;
     if constexpr (QKV) {
+      if (pos < 0) return;  // a start position out of range (reported by the attention)
       const int b = m / p.T;
-      const int start = p.sp.get(b);
-      if (!p.sp.ok(start)) continue;
-      const int pos = start + (m - b * p.T);
       if (f < D_MODEL + KV_ROW) {
-        const float2 cs = *reinterpret_cast<const float2*>(
-            p.rope + (static_cast<size_t>(pos) * ROPE_PAIRS + ((f & (HEAD_DIM - 1)) >> 1)) * 2);
         const float y0 = x0 * cs.x - x1 * cs.y;
         const float y1 = x0 * cs.y + x1 * cs.x;
         x0 = y0;
@@ -364,6 +416,27 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
       }
     }
     *reinterpret_cast<uint32_t*>(dst) = pack_bf16(x0, x1);
+  };
+#pragma unroll
+  for (int k = 0; k < EPF; ++k) {
+    const int idx = threadIdx.x + k * WARPS * 32;
+    if (idx < items) item(idx, pos_pf[k], cs_pf[k]);
+  }
+  for (int idx = threadIdx.x + EPF * WARPS * 32; idx < items; idx += WARPS * 32) {
+    float2 cs = make_float2(1.f, 0.f);
+    int pos = -1;
+    if constexpr (QKV) {
+      const int m = idx % p.M, f = fbase + 2 * (idx / p.M);
+      const int b = m / p.T;
+      const int start = p.sp.get(b);
+      if (p.sp.ok(start)) {
+        pos = start + (m - b * p.T);
+        if (f < D_MODEL + KV_ROW)
+          cs = *reinterpret_cast<const float2*>(
+              p.rope + (static_cast<size_t>(pos) * ROPE_PAIRS + ((f & (HEAD_DIM - 1)) >> 1)) * 2);
+      }
+    }
+    item(idx, pos, cs);
   }
   fence_proxy_async_global();  // later phases of the grid read these rows by TMA
   __threadfence();
@@ -376,7 +449,7 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
 template <class C_>
 __device__ __forceinline__ void rows_drain(const Shared& sh, const RowPlan& plan) {
   constexpr int XS = C_::XS;
-  const int S = min(MAX_STAGES, (C_::W_RING - OVERREAD) / wstage_bytes(plan));
+  const int S = ring_stages(C_::W_RING, plan);
   for (int i = max(0, sh.flags[2] - S); i < sh.flags[2]; ++i) mbar_wait(smem_u32(&sh.full[i % S]), (i / S) & 1);
   for (int i = max(0, sh.flags[3] - XS); i < sh.flags[3]; ++i) mbar_wait(smem_u32(&sh.xfull[i % XS]), (i / XS) & 1);
 }
