@@ -43,7 +43,11 @@ import torch  # noqa: E402
 import gqa_inputs as I  # noqa: E402
 
 METRIC = "GQA block decode seq-steps/s & HBM GB/s vs peak; prefill TFLOP/s vs peak"
-WEIGHT_BYTES = 2 * (4096 * 4096 * 2 + 1024 * 4096 * 2)   # 83,886,080
+
+
+def weight_bytes(kv_row: int = 1024) -> int:
+    """Wq, Wk, Wv, Wo in bf16; kv_row = KV heads x 128 (1024, or 4096 for 32 KV heads)."""
+    return (2 * 4096 + 2 * kv_row) * 4096 * 2
 KERNELS = ("qkv_projection", "decode_attention", "o_projection")
 
 
@@ -71,28 +75,34 @@ def dist_env():
     return rank, world, local
 
 
-def step_bytes(B: int, starts) -> dict:
-    """Algorithmic HBM bytes of one decode step, per kernel (see the design notes)."""
-    kv_read = sum((int(p) + 1) * 4096 for p in starts)
+def step_bytes(B: int, starts, kv_row: int = 1024) -> dict:
+    """Algorithmic HBM bytes of one decode step, per kernel (see the design notes).
+    A cache position is 2 * kv_row * 2 bytes of K and V (4,096 for 8 KV heads)."""
+    pos_bytes = 4 * kv_row
+    kv_read = sum((int(p) + 1) * pos_bytes for p in starts)
+    wqkv = (4096 + 2 * kv_row) * 4096 * 2
+    step = weight_bytes(kv_row) + kv_read + B * pos_bytes + 2 * B * 8192
     return {
-        "qkv_projection": 50331648 + B * 8192 + B * 8192 + B * 4096,   # Wq|Wk|Wv, x, rotated q, new K/V rows
+        "qkv_projection": wqkv + B * 8192 + B * 8192 + B * pos_bytes,  # Wq|Wk|Wv, x, rotated q, new K/V rows
         "decode_attention": kv_read + B * 8192 + B * 8192,           # cache rows 0..P, q, o
         "o_projection": 33554432 + B * 8192 + B * 8192,              # Wo, o, delta
-        "step": WEIGHT_BYTES + kv_read + B * 4096 + 2 * B * 8192,    # the roofline's byte count
-        "decode_step": WEIGHT_BYTES + kv_read + B * 4096 + 2 * B * 8192,  # the fused kernel: the whole step
+        "step": step,                                                # the roofline's byte count
+        "decode_step": step,                                         # the fused kernel: the whole step
         "attention_norm": 2 * B * 8192 + 8192,                       # x in, normalised rows out, weight
     }
 
 
-def step_flops(B: int, T: int, start: int) -> dict:
+def step_flops(B: int, T: int, start: int, kv_row: int = 1024) -> dict:
     """Algorithmic FLOPs of one prefill call: projections 2*41,943,040 per
-    token, attention 16,384 per visible (query, key) pair (causal half only)."""
+    token (8 KV heads), attention 16,384 per visible (query, key) pair (causal
+    half only)."""
     pairs = B * sum(start + t + 1 for t in range(T))
+    qkv = 2.0 * B * T * 4096 * (4096 + 2 * kv_row)
     return {
-        "qkv_projection": 2.0 * B * T * 4096 * 6144,
+        "qkv_projection": qkv,
         "prefill_attention": 16384.0 * pairs,
         "o_projection": 2.0 * B * T * 4096 * 4096,
-        "step": 2.0 * 41943040 * B * T + 16384.0 * pairs,
+        "step": qkv + 2.0 * B * T * 4096 * 4096 + 16384.0 * pairs,
         "attention_norm": 3.0 * B * T * 4096,
     }
 
@@ -188,10 +198,10 @@ def cpu_baseline(w: I.Workload, budget_s: float = 12.0):
     """The oracle, as it stands, on a bounded sample: whole sequences of the
     workload (projections, attention, output) until the budget is spent."""
     from oracle import gqa as O
-    gen, wt = I.draw_weights(seed=w.seed)
+    gen, wt = I.draw_weights(w.dims, seed=w.seed)
     x = I.draw_x(gen, w.B, w.T)
     starts = w.start_positions().tolist()
-    ck, cv = I.draw_cache(w.B, w.cache_rows(), starts, seed=w.seed, device="cpu")
+    ck, cv = I.draw_cache(w.B, w.cache_rows(), starts, w.dims, seed=w.seed, device="cpu")
     W = {k: v.to(torch.float64).numpy() for k, v in wt.items()}
     r = I.LLAMA31_ROPE
     freqs = O.rope_frequencies(128, r.theta, r.scaled, r.factor, r.low_freq_factor, r.high_freq_factor,
@@ -230,7 +240,7 @@ def _oracle_unit(w: I.Workload, O, W, freqs, per):
 
     def unit(i):
         xb, kb, vb, sp = per[i % w.B]
-        O.sequence_forward(xb, W["wq"], W["wk"], W["wv"], W["wo"], sp, kb, vb, freqs, 32, 8)
+        O.sequence_forward(xb, W["wq"], W["wk"], W["wv"], W["wo"], sp, kb, vb, freqs, 32, w.n_kv_heads)
     return unit
 
 
@@ -238,10 +248,10 @@ def run_reference(a, w: I.Workload, rank: int, world: int):
     if rank != 0:
         return
     from oracle import gqa as O
-    gen, wt = I.draw_weights(seed=w.seed)
+    gen, wt = I.draw_weights(w.dims, seed=w.seed)
     x = I.draw_x(gen, w.B, w.T)
     starts = w.start_positions().tolist()
-    ck, cv = I.draw_cache(w.B, w.cache_rows(), starts, seed=w.seed, device="cpu")
+    ck, cv = I.draw_cache(w.B, w.cache_rows(), starts, w.dims, seed=w.seed, device="cpu")
     W = {k: v.to(torch.float64).numpy() for k, v in wt.items()}
     r = I.LLAMA31_ROPE
     freqs = O.rope_frequencies(128, r.theta, r.scaled, r.factor, r.low_freq_factor, r.high_freq_factor,
@@ -277,7 +287,7 @@ def run_reference(a, w: I.Workload, rank: int, world: int):
 
 def config_dict(w: I.Workload, a, starts):
     c = {"workload": w.name, "B": w.B, "T": w.T, "s_max": w.cache_rows(), "d_model": 4096, "n_heads": 32,
-         "n_kv_heads": 8, "head_dim": 128,
+         "n_kv_heads": w.n_kv_heads, "head_dim": 128,
          "l2": f"inputs larger than L2: {a.replicas} rotating replicas of weights+cache+x, one per step",
          "parallelism": "replicas"}
     if w.layers > 1:
@@ -336,9 +346,11 @@ def main():
 
     starts = w.start_positions().tolist()
     s_max = w.cache_rows()
-    gen, wt = I.draw_weights(seed=w.seed)
+    gen, wt = I.draw_weights(w.dims, seed=w.seed)
     x0 = I.draw_x(gen, w.B, w.T)
-    ck0, cv0 = I.draw_cache(w.B, s_max, starts, seed=w.seed)
+    ck0, cv0 = I.draw_cache(w.B, s_max, starts, w.dims, seed=w.seed)
+    nkv = w.n_kv_heads
+    kv_row = nkv * 128
     L = w.layers
     # a multi-layer step: one replica per layer (its own weights, cache and
     # workspace), chained; the working set (L x 150 MB) is far above L2
@@ -353,6 +365,8 @@ def main():
     rope = G.rope_table(s_max, device=dev)
 
     layer = a.entry == "layer" or L > 1
+    if layer and nkv != 8:
+        raise SystemExit("the layer entries take the 8-KV-head block only")
     norm_w = I.draw_norm_weight(seed=w.seed).to(dev)
     norms = [norm_w.clone() for _ in range(R)] if L > 1 else None
 
@@ -377,10 +391,13 @@ def main():
                            r["ck"], r["cv"], out=r["out"], workspace=r["ws"])
         elif decode:
             G.decode(r["x"], sp, max_start, r["wq"], r["wk"], r["wv"], r["wo"], rope, r["ck"], r["cv"],
-                     out=r["out"], workspace=r["ws"])
+                     out=r["out"], workspace=r["ws"], n_kv_heads=nkv)
         elif layer:
             G.layer_forward(r["x"], starts[0], norm_w, I.NORM_EPS, r["wq"], r["wk"], r["wv"], r["wo"], rope,
                             r["ck"], r["cv"], out=r["out"], workspace=r["ws"])
+        elif nkv != 8:
+            G.block_forward(r["x"], starts[0], r["wq"], r["wk"], r["wv"], r["wo"], rope, r["ck"], r["cv"],
+                            out=r["out"], workspace=r["ws"], n_kv_heads=nkv)
         else:
             G.prefill(r["x"], starts[0], r["wq"], r["wk"], r["wv"], r["wo"], rope, r["ck"], r["cv"],
                       out=r["out"], workspace=r["ws"])
@@ -493,7 +510,7 @@ def main():
     hbm, tflops, peak_kind = load_peaks()
     dom = max(per_kernel, key=per_kernel.get)
     if decode:
-        work = step_bytes(w.B, starts)
+        work = step_bytes(w.B, starts, kv_row)
         if layer:  # the norm's x in and rows out, the residual's x in
             work["step"] += 3 * w.B * 8192 + 8192
         work["step"] *= L   # per-kernel figures stay per launch (one layer)
@@ -507,7 +524,7 @@ def main():
         step_rate = {"step_hbm_gbs": work["step"] / (ms_step / 1e3) / 1e9}
         step_rate["step_hbm_frac"] = step_rate["step_hbm_gbs"] / hbm
     else:
-        work = step_flops(w.B, w.T, starts[0])
+        work = step_flops(w.B, w.T, starts[0], kv_row)
         value = world * work["step"] * a.steps / (ms / 1e3) / 1e12
         unit = "TFLOP/s"
         e2e_value = world * work["step"] * a.steps / (ems / 1e3) / 1e12

@@ -30,7 +30,7 @@ from typing import Optional, Sequence
 import torch
 
 __all__ = [
-    "Dims", "RopeConfig", "Workload", "WORKLOADS", "LLAMA31_8B", "LLAMA31_ROPE",
+    "Dims", "RopeConfig", "Workload", "WORKLOADS", "LLAMA31_8B", "LLAMA31_8B_MHA", "LLAMA31_ROPE",
     "LLAMA3_ROPE", "draw_weights", "draw_x", "draw_cache", "draw_start_positions", "draw_norm_weight",
     "NORM_EPS",
     "workload", "DEVICE_DRAW_THRESHOLD",
@@ -68,6 +68,9 @@ class RopeConfig:
 
 
 LLAMA31_8B = Dims()
+# The multi-head variant the "Grouped-query attention" page sets against the
+# model: 32 K/V heads, one per query head (repeat_kv is the identity).
+LLAMA31_8B_MHA = Dims(n_kv_heads=32)
 LLAMA31_ROPE = RopeConfig()
 # "Llama 3 8B · Attention update" page: same dims, use_scaled_rope False.
 LLAMA3_ROPE = RopeConfig(scaled=False)
@@ -86,6 +89,11 @@ class Workload:
     seed: int = 0
     description: str = ""
     layers: int = 1                   # consecutive blocks per step (each with its own weights and cache)
+    n_kv_heads: int = 8               # 32: the multi-head variant
+
+    @property
+    def dims(self) -> "Dims":
+        return LLAMA31_8B if self.n_kv_heads == LLAMA31_8B.n_kv_heads else Dims(n_kv_heads=self.n_kv_heads)
 
     def start_positions(self) -> torch.Tensor:
         if self.start_pos is not None:
@@ -113,6 +121,11 @@ WORKLOADS = {
                  description="causal prefill, B=4, T=2048"),
         Workload("long_decode_b8_p131071", B=8, T=1, start_pos=131071, s_max=131072,
                  description="long-context decode, B=8, P=131071 (131,072 keys)"),
+        Workload("mha_decode_b16_p1000", B=16, T=1, start_pos=1000, s_max=1001, n_kv_heads=32,
+                 description="the multi-head variant (32 K/V heads) at the decode point P=1000, B=16: "
+                             "4x the KV rows of the grouped model (16 KB per position)"),
+        Workload("mha_prefill_b1_t2048", B=1, T=2048, start_pos=0, s_max=2048, n_kv_heads=32,
+                 description="the multi-head variant's causal prefill, B=1, T=2048"),
         Workload("decode32_b16_p1000", B=16, T=1, start_pos=1000, s_max=1001, layers=32,
                  description="32 consecutive layers of one decode step at P=1000, B=16: the attention half "
                              "of each block with its norm and residual (h = x + attention(RMSNorm(x))), each "

@@ -41,6 +41,9 @@ _SIGNATURES = {
     "gqa_block_forward": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "gqa_prefill": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "gqa_decode": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
+    "gqa_block_forward_nkv": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz,
+                                   _vp]),
+    "gqa_decode_nkv": (_i, [_vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "gqa_rms_norm": (_i, [_vp, _i, _vp, ctypes.c_float, _vp, _vp]),
     "gqa_layer_forward": (_i, [_vp, _i, _i, _i, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp,
                                _vp, _sz, _vp]),
@@ -138,20 +141,22 @@ def rope_table(rows: int, theta: float = 500000.0, scaled: bool = True, factor: 
     return out
 
 
-def _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, T):
+def _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, T, n_kv=N_KV_HEADS):
     B = x.shape[0]
+    if n_kv not in (N_KV_HEADS, N_HEADS):
+        raise ValueError(f"n_kv_heads must be {N_KV_HEADS} or {N_HEADS}, got {n_kv}")
     _check(x, "x", torch.bfloat16, (B, T, D_MODEL))
     _check(wq, "wq", torch.bfloat16, (N_HEADS * HEAD_DIM, D_MODEL))
-    _check(wk, "wk", torch.bfloat16, (N_KV_HEADS * HEAD_DIM, D_MODEL))
-    _check(wv, "wv", torch.bfloat16, (N_KV_HEADS * HEAD_DIM, D_MODEL))
+    _check(wk, "wk", torch.bfloat16, (n_kv * HEAD_DIM, D_MODEL))
+    _check(wv, "wv", torch.bfloat16, (n_kv * HEAD_DIM, D_MODEL))
     _check(wo, "wo", torch.bfloat16, (D_MODEL, N_HEADS * HEAD_DIM))
     _check(rope, "rope", torch.float32)
     if rope.dim() != 3 or rope.shape[1:] != (64, 2):
         raise ValueError("rope must be [rows, 64, 2]")
     _check(cache_k, "cache_k", torch.bfloat16)
     _check(cache_v, "cache_v", torch.bfloat16, cache_k.shape)
-    if cache_k.dim() != 4 or cache_k.shape[0] != B or cache_k.shape[2:] != (N_KV_HEADS, HEAD_DIM):
-        raise ValueError(f"cache must be [B, S_max, 8, 128], got {tuple(cache_k.shape)}")
+    if cache_k.dim() != 4 or cache_k.shape[0] != B or cache_k.shape[2:] != (n_kv, HEAD_DIM):
+        raise ValueError(f"cache must be [B, S_max, {n_kv}, 128], got {tuple(cache_k.shape)}")
     if out is None:
         out = torch.empty_like(x)
     _check(out, "out", torch.bfloat16, (B, T, D_MODEL))
@@ -166,16 +171,24 @@ def _ws(workspace, B, T, max_keys, device):
 
 
 def block_forward(x, start_pos: int, wq, wk, wv, wo, rope, cache_k, cache_v, out=None,
-                  workspace=None, stream=None) -> torch.Tensor:
-    """delta_attn for x [B, T, 4096] after ``start_pos`` cached rows; updates the cache."""
+                  workspace=None, stream=None, n_kv_heads: int = N_KV_HEADS) -> torch.Tensor:
+    """delta_attn for x [B, T, 4096] after ``start_pos`` cached rows; updates the cache.
+    ``n_kv_heads`` 32 is the multi-head variant (wk, wv [4096, 4096], cache [B, S, 32, 128])."""
     T = x.shape[1]
-    B, out = _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, T)
+    B, out = _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, T, n_kv_heads)
     workspace = _ws(workspace, B, T, start_pos + T, x.device)
-    r = lib().gqa_block_forward(_p(x), B, T, int(start_pos), _p(wq), _p(wk), _p(wv), _p(wo), _p(rope),
-                                rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
-                                _p(workspace), workspace.numel(), _s(stream))
+    if n_kv_heads == N_KV_HEADS:
+        r = lib().gqa_block_forward(_p(x), B, T, int(start_pos), _p(wq), _p(wk), _p(wv), _p(wo), _p(rope),
+                                    rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
+                                    _p(workspace), workspace.numel(), _s(stream))
+        where = "gqa_block_forward"
+    else:
+        r = lib().gqa_block_forward_nkv(_p(x), B, T, int(start_pos), int(n_kv_heads), _p(wq), _p(wk), _p(wv),
+                                        _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1],
+                                        _p(out), _p(workspace), workspace.numel(), _s(stream))
+        where = "gqa_block_forward_nkv"
     if r:
-        raise GQAError(r, "gqa_block_forward")
+        raise GQAError(r, where)
     return out
 
 
@@ -193,16 +206,24 @@ def prefill(x, start_pos: int, wq, wk, wv, wo, rope, cache_k, cache_v, out=None,
 
 
 def decode(x, start_pos: torch.Tensor, max_start_pos: int, wq, wk, wv, wo, rope, cache_k, cache_v,
-           out=None, workspace=None, stream=None) -> torch.Tensor:
-    """One decode step; ``start_pos`` is a device int32 [B] of cached rows per sequence."""
-    B, out = _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, 1)
+           out=None, workspace=None, stream=None, n_kv_heads: int = N_KV_HEADS) -> torch.Tensor:
+    """One decode step; ``start_pos`` is a device int32 [B] of cached rows per sequence.
+    ``n_kv_heads`` as in ``block_forward``."""
+    B, out = _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, 1, n_kv_heads)
     _check(start_pos, "start_pos", torch.int32, (B,))
     workspace = _ws(workspace, B, 1, max_start_pos + 1, x.device)
-    r = lib().gqa_decode(_p(x), B, _p(start_pos), int(max_start_pos), _p(wq), _p(wk), _p(wv), _p(wo),
-                         _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
-                         _p(workspace), workspace.numel(), _s(stream))
+    if n_kv_heads == N_KV_HEADS:
+        r = lib().gqa_decode(_p(x), B, _p(start_pos), int(max_start_pos), _p(wq), _p(wk), _p(wv), _p(wo),
+                             _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
+                             _p(workspace), workspace.numel(), _s(stream))
+        where = "gqa_decode"
+    else:
+        r = lib().gqa_decode_nkv(_p(x), B, _p(start_pos), int(max_start_pos), int(n_kv_heads), _p(wq), _p(wk),
+                                 _p(wv), _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1],
+                                 _p(out), _p(workspace), workspace.numel(), _s(stream))
+        where = "gqa_decode_nkv"
     if r:
-        raise GQAError(r, "gqa_decode")
+        raise GQAError(r, where)
     return out
 
 

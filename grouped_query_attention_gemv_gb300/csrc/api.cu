@@ -55,11 +55,11 @@ bool make_layout(int B, int T, int max_keys, Layout* L) {
   L->o = take(static_cast<size_t>(M) * D_MODEL * 2);
   L->np = proj_stream_np(static_cast<int>(M));
   if (L->np) {
-    const int segmax = proj_stream_segmax(QKV_ROWS, REF_SMS) > proj_stream_segmax(D_MODEL, REF_SMS)
-                           ? proj_stream_segmax(QKV_ROWS, REF_SMS) : proj_stream_segmax(D_MODEL, REF_SMS);
+    const int segmax = proj_stream_segmax(QKV_ROWS_MAX, REF_SMS) > proj_stream_segmax(D_MODEL, REF_SMS)
+                           ? proj_stream_segmax(QKV_ROWS_MAX, REF_SMS) : proj_stream_segmax(D_MODEL, REF_SMS);
     L->proj_slots = REF_SMS * segmax;
     L->proj_part = take(static_cast<size_t>(L->proj_slots) * 128 * L->np * 4);
-    L->proj_tickets = take(static_cast<size_t>(QKV_ROWS / 128) * 4);
+    L->proj_tickets = take(static_cast<size_t>(QKV_ROWS_MAX / 128) * 4);
   }
   if (T == 1) {
     if (B > DECODE_MAX_B) return false;
@@ -124,14 +124,17 @@ bool map_rows_kblocks(CUtensorMap* m, const void* ptr, long long rows, int box_r
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Decode view of the KV cache [B, s_max, 8, 128] bf16: dims (d, pos, g, b) so
-// that one box of 64 dims x box_pos positions x all 8 heads covers whole
-// position rows. Positions past s_max read as zero.
-bool map_cache_by_position(CUtensorMap* m, const void* ptr, int B, int s_max, int box_pos) {
+// Decode view of the KV cache [B, s_max, n_kv, 128] bf16: dims (d, pos, g, b)
+// so that one box of 64 dims x box_pos positions x 8 heads covers whole
+// position rows of 8 KV heads (all of them, or one group of the multi-head
+// variant). Positions past s_max read as zero.
+bool map_cache_by_position(CUtensorMap* m, const void* ptr, int B, int s_max, int n_kv, int box_pos) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const cuuint64_t dims[4] = {HEAD_DIM, static_cast<cuuint64_t>(s_max), N_KV, static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {KV_ROW * 2, HEAD_DIM * 2, static_cast<cuuint64_t>(s_max) * KV_ROW * 2};
+  const cuuint64_t row = static_cast<cuuint64_t>(n_kv) * HEAD_DIM * 2;  // bytes of one cache position
+  const cuuint64_t dims[4] = {HEAD_DIM, static_cast<cuuint64_t>(s_max), static_cast<cuuint64_t>(n_kv),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {row, HEAD_DIM * 2, static_cast<cuuint64_t>(s_max) * row};
   const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_pos), N_KV, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
@@ -139,14 +142,16 @@ bool map_cache_by_position(CUtensorMap* m, const void* ptr, int B, int s_max, in
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// KV cache [B, s_max, 8, 128] bf16 as a 4-D tensor (d, g, pos, b); boxes of
-// 64 dims x 1 head x box_pos positions. Positions at or past `rows` (<= s_max)
-// read as zero.
-bool map_cache(CUtensorMap* m, const void* ptr, int B, int s_max, int rows, int box_pos) {
+// KV cache [B, s_max, n_kv, 128] bf16 as a 4-D tensor (d, g, pos, b); boxes
+// of 64 dims x 1 head x box_pos positions. Positions at or past `rows`
+// (<= s_max) read as zero.
+bool map_cache(CUtensorMap* m, const void* ptr, int B, int s_max, int n_kv, int rows, int box_pos) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || rows <= 0 || rows > s_max) return false;
-  const cuuint64_t dims[4] = {HEAD_DIM, N_KV, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {HEAD_DIM * 2, KV_ROW * 2, static_cast<cuuint64_t>(s_max) * KV_ROW * 2};
+  const cuuint64_t row = static_cast<cuuint64_t>(n_kv) * HEAD_DIM * 2;
+  const cuuint64_t dims[4] = {HEAD_DIM, static_cast<cuuint64_t>(n_kv), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {HEAD_DIM * 2, row, static_cast<cuuint64_t>(s_max) * row};
   const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_pos), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
@@ -155,13 +160,14 @@ bool map_cache(CUtensorMap* m, const void* ptr, int B, int s_max, int rows, int 
 }
 
 // Rotated queries [B*T, 4096] bf16 as a 4-D tensor (d, head, t, b); boxes of
-// 64 dims x 4 heads (one KV group) x 32 tokens. Tokens past T read as zero.
-bool map_q_prefill(CUtensorMap* m, const void* ptr, int B, int T) {
+// 64 dims x n_rep heads (one KV group) x 128 / n_rep tokens (128 rows). Tokens
+// past T read as zero.
+bool map_q_prefill(CUtensorMap* m, const void* ptr, int B, int T, int n_rep) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {HEAD_DIM, N_HEADS, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {HEAD_DIM * 2, D_MODEL * 2, static_cast<cuuint64_t>(T) * D_MODEL * 2};
-  const cuuint32_t box[4] = {64, N_REP, 32, 1};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(n_rep), static_cast<cuuint32_t>(128 / n_rep), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -191,10 +197,12 @@ struct Call {
   const float* rope;
   gqa_bf16 *cache_k, *cache_v;
   int s_max;
+  int n_kv;  // KV heads: 8 (Llama 3.1 8B), or 32 (the multi-head variant)
   gqa_bf16* out;
   uint8_t* ws;
   cudaStream_t stream;
   Layout L;
+  int kv_row() const { return n_kv * HEAD_DIM; }
 };
 
 int check_common(const gqa_bf16* x, int B, int T, const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv,
@@ -229,8 +237,8 @@ ProjParams proj_params(const Call& c, bool qkv, bool fold_norm = false) {
     p.w1 = reinterpret_cast<const __nv_bfloat16*>(c.wk);
     p.w2 = reinterpret_cast<const __nv_bfloat16*>(c.wv);
     p.r1 = D_MODEL;
-    p.r2 = D_MODEL + KV_ROW;
-    p.N = QKV_ROWS;
+    p.r2 = D_MODEL + c.kv_row();
+    p.N = D_MODEL + 2 * c.kv_row();
     p.qkv = 1;
     p.out = reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.q);
   } else {
@@ -259,7 +267,7 @@ int launch_sms() {
 // weights (128 rows) and of the tokens (np rows).
 bool stream_maps(const Call& c, bool qkv, const ProjParams& p, ProjStreamMaps* m) {
   const gqa_bf16* w[3] = {qkv ? c.wq : c.wo, qkv ? c.wk : c.wo, qkv ? c.wv : c.wo};
-  const long long rows[3] = {D_MODEL, qkv ? KV_ROW : D_MODEL, qkv ? KV_ROW : D_MODEL};
+  const long long rows[3] = {D_MODEL, qkv ? c.kv_row() : D_MODEL, qkv ? c.kv_row() : D_MODEL};
   for (int kc = 1; kc <= 4; ++kc) {
     for (int i = 0; i < 3; ++i)
       if (!map_rows_kblocks(&m->w[kc - 1][i], w[i], rows[i], 128, kc)) return false;
@@ -272,6 +280,7 @@ DecodeAttnParams decode_attn_params(const Call& c) {
   DecodeAttnParams a{};
   a.q = reinterpret_cast<const __nv_bfloat16*>(c.ws + c.L.q);
   a.B = c.B;
+  a.n_kv = c.n_kv;
   a.sp = c.sp;
   a.ctas = attn_decode_ctas(launch_sms());
   a.part_o = reinterpret_cast<float*>(c.ws + c.L.part_o);
@@ -286,8 +295,8 @@ DecodeAttnParams decode_attn_params(const Call& c) {
 }
 
 bool decode_cache_maps(const Call& c, DecodeCacheMaps* m) {
-  return map_cache_by_position(&m->k, c.cache_k, c.B, c.s_max, DECODE_UNIT) &&
-         map_cache_by_position(&m->v, c.cache_v, c.B, c.s_max, DECODE_UNIT);
+  return map_cache_by_position(&m->k, c.cache_k, c.B, c.s_max, c.n_kv, DECODE_UNIT) &&
+         map_cache_by_position(&m->v, c.cache_v, c.B, c.s_max, c.n_kv, DECODE_UNIT);
 }
 
 // PDL (programmatic dependent launch) is only requested for kernels that
@@ -309,8 +318,8 @@ int run_projection(const Call& c, bool qkv, bool pdl) {
   } else {
     if (!map_rows(&maps.a, p.x, p.M, GEMM_BM)) return fail_cuda(cudaErrorInvalidValue);
     if (qkv) {
-      if (!map_rows(&maps.b[0], c.wq, D_MODEL, GEMM_BN) || !map_rows(&maps.b[1], c.wk, KV_ROW, GEMM_BN) ||
-          !map_rows(&maps.b[2], c.wv, KV_ROW, GEMM_BN))
+      if (!map_rows(&maps.b[0], c.wq, D_MODEL, GEMM_BN) || !map_rows(&maps.b[1], c.wk, c.kv_row(), GEMM_BN) ||
+          !map_rows(&maps.b[2], c.wv, c.kv_row(), GEMM_BN))
         return fail_cuda(cudaErrorInvalidValue);
     } else {
       if (!map_rows(&maps.b[0], c.wo, D_MODEL, GEMM_BN)) return fail_cuda(cudaErrorInvalidValue);
@@ -335,14 +344,15 @@ int run_attention(const Call& c) {
   } else {
     PrefillMaps maps;
     const void* q = c.ws + c.L.q;
-    if (!map_q_prefill(&maps.q, q, c.B, c.T) ||
-        !map_cache(&maps.k, c.cache_k, c.B, c.s_max, c.max_keys, PREFILL_TILE) ||
-        !map_cache(&maps.v, c.cache_v, c.B, c.s_max, c.max_keys, PREFILL_TILE))
+    if (!map_q_prefill(&maps.q, q, c.B, c.T, N_HEADS / c.n_kv) ||
+        !map_cache(&maps.k, c.cache_k, c.B, c.s_max, c.n_kv, c.max_keys, PREFILL_TILE) ||
+        !map_cache(&maps.v, c.cache_v, c.B, c.s_max, c.n_kv, c.max_keys, PREFILL_TILE))
       return fail_cuda(cudaErrorInvalidValue);
     PrefillAttnParams a{};
     a.q = reinterpret_cast<const __nv_bfloat16*>(q);
     a.B = c.B;
     a.T = c.T;
+    a.n_kv = c.n_kv;
     a.sp = c.sp;
     a.o = reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.o);
     a.status = reinterpret_cast<int*>(c.ws + c.L.status);
@@ -368,6 +378,7 @@ bool row_maps(const gqa_bf16* const* w, const RowPlan& plan, const void* x, int 
 // GQA_EINVAL without launching anything when this GPU cannot run it (too few
 // SMs for the row split); the caller then takes the three-kernel path.
 int run_decode_fused(const Call& c) {
+  if (c.n_kv != N_KV) return GQA_EINVAL;  // phase A's row split is sized for 8 KV heads
   DecodeFusedArgs a;
   a.ctas = launch_sms();
   const int qkv_rows[3] = {D_MODEL, KV_ROW, KV_ROW};
@@ -471,12 +482,14 @@ int gqa_rope_table(float* rope, int rows, double theta, int scaled, double facto
   return GQA_OK;
 }
 
-static int block_call(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* norm_w, float eps,
+static bool valid_n_kv(int n_kv) { return n_kv == N_KV || n_kv == N_HEADS; }
+
+static int block_call(const gqa_bf16* x, int B, int T, int start_pos, int n_kv, const gqa_bf16* norm_w, float eps,
                       const gqa_bf16* wq, const gqa_bf16* wk,
                       const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
                       gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
                       void* stream) {
-  if (start_pos < 0 || T <= 0 || start_pos > (1 << 30)) return GQA_EINVAL;
+  if (start_pos < 0 || T <= 0 || start_pos > (1 << 30) || !valid_n_kv(n_kv)) return GQA_EINVAL;
   Call c{};
   const int max_keys = start_pos + T;
   int r = check_common(x, B, T, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, out, workspace, max_keys,
@@ -488,6 +501,7 @@ static int block_call(const gqa_bf16* x, int B, int T, int start_pos, const gqa_
   c.B = B;
   c.T = T;
   c.sp = StartPos{nullptr, start_pos, start_pos};
+  c.n_kv = n_kv;
   c.max_keys = max_keys;
   c.wq = wq;
   c.wk = wk;
@@ -527,8 +541,16 @@ int gqa_block_forward(const gqa_bf16* x, int B, int T, int start_pos, const gqa_
                       const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
                       gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
                       void* stream) {
-  return block_call(x, B, T, start_pos, nullptr, 0.f, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, out,
-                    workspace, workspace_bytes, stream);
+  return block_call(x, B, T, start_pos, N_KV, nullptr, 0.f, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max,
+                    out, workspace, workspace_bytes, stream);
+}
+
+int gqa_block_forward_nkv(const gqa_bf16* x, int B, int T, int start_pos, int n_kv_heads, const gqa_bf16* wq,
+                          const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows,
+                          gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  return block_call(x, B, T, start_pos, n_kv_heads, nullptr, 0.f, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v,
+                    s_max, out, workspace, workspace_bytes, stream);
 }
 
 int gqa_layer_forward(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* norm_w, float eps,
@@ -537,8 +559,8 @@ int gqa_layer_forward(const gqa_bf16* x, int B, int T, int start_pos, const gqa_
                       gqa_bf16* h, void* workspace, size_t workspace_bytes, void* stream) {
   const int r = check_layer(x, norm_w, eps, h);
   if (r != GQA_OK) return r;
-  return block_call(x, B, T, start_pos, norm_w, eps, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, h,
-                    workspace, workspace_bytes, stream);
+  return block_call(x, B, T, start_pos, N_KV, norm_w, eps, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max,
+                    h, workspace, workspace_bytes, stream);
 }
 
 int gqa_prefill(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* wq, const gqa_bf16* wk,
@@ -548,12 +570,15 @@ int gqa_prefill(const gqa_bf16* x, int B, int T, int start_pos, const gqa_bf16* 
                            workspace, workspace_bytes, stream);
 }
 
-static int decode_call(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos,
+static int decode_call(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos, int n_kv,
                        const gqa_bf16* norm_w, float eps, const gqa_bf16* wq, const gqa_bf16* wk,
                        const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
                        gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
                        void* stream) {
-  if (!start_pos || max_start_pos < 0 || max_start_pos > (1 << 30)) return GQA_EINVAL;
+  if (!start_pos || max_start_pos < 0 || max_start_pos > (1 << 30) || !valid_n_kv(n_kv)) return GQA_EINVAL;
+  // the attention runs n_kv / 8 head groups of every sequence as units of their own
+  const int groups = n_kv / N_KV;
+  if (B > DECODE_MAX_B / groups) return GQA_EINVAL;
   Call c{};
   const int max_keys = max_start_pos + 1;
   int r = check_common(x, B, 1, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v, s_max, out, workspace, max_keys,
@@ -561,7 +586,8 @@ static int decode_call(const gqa_bf16* x, int B, const int32_t* start_pos, int m
   if (r != GQA_OK) return r;
   if ((reinterpret_cast<uintptr_t>(start_pos) & 3u) != 0) return GQA_EALIGN;
   // the attention splits its units over the grid in 32-bit arithmetic
-  const unsigned long long units = static_cast<unsigned long long>(B) * ((max_keys + DECODE_UNIT - 1) / DECODE_UNIT);
+  const unsigned long long units =
+      static_cast<unsigned long long>(B) * groups * ((max_keys + DECODE_UNIT - 1) / DECODE_UNIT);
   if ((units + 1) * (static_cast<unsigned long long>(attn_decode_ctas(launch_sms())) + 1) >= (1ull << 32))
     return GQA_EINVAL;
   c.norm_w = norm_w;
@@ -570,6 +596,7 @@ static int decode_call(const gqa_bf16* x, int B, const int32_t* start_pos, int m
   c.B = B;
   c.T = 1;
   c.sp = StartPos{start_pos, 0, max_start_pos};
+  c.n_kv = n_kv;
   c.max_keys = max_keys;
   c.wq = wq;
   c.wk = wk;
@@ -589,8 +616,16 @@ int gqa_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start
                const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows,
                gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace,
                size_t workspace_bytes, void* stream) {
-  return decode_call(x, B, start_pos, max_start_pos, nullptr, 0.f, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v,
-                     s_max, out, workspace, workspace_bytes, stream);
+  return decode_call(x, B, start_pos, max_start_pos, N_KV, nullptr, 0.f, wq, wk, wv, wo, rope, rope_rows, cache_k,
+                     cache_v, s_max, out, workspace, workspace_bytes, stream);
+}
+
+int gqa_decode_nkv(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos, int n_kv_heads,
+                   const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo, const float* rope,
+                   int rope_rows, gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  return decode_call(x, B, start_pos, max_start_pos, n_kv_heads, nullptr, 0.f, wq, wk, wv, wo, rope, rope_rows,
+                     cache_k, cache_v, s_max, out, workspace, workspace_bytes, stream);
 }
 
 int gqa_layer_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos, const gqa_bf16* norm_w,
@@ -599,8 +634,8 @@ int gqa_layer_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max
                      gqa_bf16* h, void* workspace, size_t workspace_bytes, void* stream) {
   const int r = check_layer(x, norm_w, eps, h);
   if (r != GQA_OK) return r;
-  return decode_call(x, B, start_pos, max_start_pos, norm_w, eps, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v,
-                     s_max, h, workspace, workspace_bytes, stream);
+  return decode_call(x, B, start_pos, max_start_pos, N_KV, norm_w, eps, wq, wk, wv, wo, rope, rope_rows, cache_k,
+                     cache_v, s_max, h, workspace, workspace_bytes, stream);
 }
 
 const char* gqa_strerror(int status) {

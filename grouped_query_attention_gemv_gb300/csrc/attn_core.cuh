@@ -34,6 +34,12 @@
 //   * units are requested before `gate` (the queries and the new rows may
 //     still be in the making) except a sequence's last unit, which holds the
 //     row the projection writes; queries are read after it.
+// The multi-head variant (32 KV heads, one query head each: repeat_kv is the
+// identity) runs the same units over groups of 8 KV heads: every sequence
+// becomes NG = 4 "virtual sequences" (sequence b, heads 8j..8j+7), so a unit
+// is still 16 positions x 8 heads and a warp still owns one KV head. NREP
+// (query heads per KV head: 4, or 1 for the multi-head variant) is a
+// template parameter of the phase.
 #pragma once
 
 #include <math.h>
@@ -55,7 +61,7 @@ constexpr float SCALE_LOG2 = 0.08838834764831845f * 1.4426950408889634f;
 constexpr int MERGE_SLOTS = 16;               // slots whose loads are in flight together in a merge
 
 struct Cursor {
-  int b, j;  // sequence, unit within it
+  int b, j;  // virtual sequence (sequence b / NG, head group b % NG), unit within it
 };
 
 __device__ __forceinline__ int units_of(const int* pre, int b) { return pre[b + 1] - pre[b]; }
@@ -90,19 +96,22 @@ __device__ __forceinline__ long long range_start(long long c, long long U, long 
   return static_cast<uint32_t>(U) * static_cast<uint32_t>(c) / static_cast<uint32_t>(C);
 }
 
-// Units per sequence prefix-summed into pre[0..B]; returns (on every lane) the
-// number of sequences with a valid start position. Run by one whole warp.
+// Units per virtual sequence (NG per sequence) prefix-summed into
+// pre[0..B*NG]; returns (on every lane) the number of virtual sequences with a
+// valid start position. Run by one whole warp.
+template <int NG>
 __device__ __forceinline__ int build_prefix(const DecodeAttnParams& a, int* pre) {
   const int lane = threadIdx.x & 31;
+  const int VB = a.B * NG;
   int run = 0, valid = 0;
   if (lane == 0) pre[0] = 0;
-  for (int base = 0; base < a.B; base += 32) {
+  for (int base = 0; base < VB; base += 32) {
     const int b = base + lane;
     int v = 0;
-    if (b < a.B) {
-      const int P = a.sp.get(b);
+    if (b < VB) {
+      const int P = a.sp.get(b / NG);
       if (a.sp.ok(P)) v = (P + 1 + UNIT - 1) / UNIT;
-      else if (blockIdx.x == 0) report(a.status, DEV_BAD_POSITION);
+      else if (blockIdx.x == 0 && b % NG == 0) report(a.status, DEV_BAD_POSITION);
     }
     valid += __popc(__ballot_sync(0xffffffffu, v > 0));
 #pragma unroll
@@ -110,7 +119,7 @@ __device__ __forceinline__ int build_prefix(const DecodeAttnParams& a, int* pre)
       const int x = __shfl_up_sync(0xffffffffu, v, o);
       if (lane >= o) v += x;
     }
-    if (b < a.B) pre[b + 1] = run + v;
+    if (b < VB) pre[b + 1] = run + v;
     run += __shfl_sync(0xffffffffu, v, 31);
   }
   return valid;
@@ -136,20 +145,22 @@ struct Shared {
 };
 
 // Ask L2 for this CTA's units [u0 + first, u0 + first + count). One thread.
+template <int NG>
 __device__ __forceinline__ void prefetch_units(const CUtensorMap* mk, const CUtensorMap* mv, const DecodeAttnParams& a,
                                                const int* pre, int first, int count) {
-  const long long U = pre[a.B], C = gridDim.x;
+  const int VB = a.B * NG;
+  const long long U = pre[VB], C = gridDim.x;
   const long long u0 = range_start(blockIdx.x, U, C), u1 = range_start(blockIdx.x + 1, U, C);
   const long long from = u0 + first, to = min(u1, u0 + first + count);
   if (from >= to) return;
-  Cursor cur = locate(from, pre, a.B);
+  Cursor cur = locate(from, pre, VB);
   for (long long u = from; u < to; ++u) {
-    const int pos = cur.j * UNIT;
-    tma_prefetch_4d(mk, 0, pos, 0, cur.b);
-    tma_prefetch_4d(mk, 64, pos, 0, cur.b);
-    tma_prefetch_4d(mv, 0, pos, 0, cur.b);
-    tma_prefetch_4d(mv, 64, pos, 0, cur.b);
-    advance(cur, pre, a.B);
+    const int pos = cur.j * UNIT, h0 = (cur.b % NG) * N_KV, sb = cur.b / NG;
+    tma_prefetch_4d(mk, 0, pos, h0, sb);
+    tma_prefetch_4d(mk, 64, pos, h0, sb);
+    tma_prefetch_4d(mv, 0, pos, h0, sb);
+    tma_prefetch_4d(mv, 64, pos, h0, sb);
+    advance(cur, pre, VB);
   }
 }
 
@@ -161,11 +172,12 @@ __device__ __forceinline__ void prefetch_units(const CUtensorMap* mk, const CUte
 // issued() runs on the producer lane once all its loads are requested.
 // Returns false (on the compute threads) when the phase gave up; on return
 // every unit is consumed and the ring is free.
-template <class GateLane, class GateWarp, class Issued>
+template <int NREP, class GateLane, class GateWarp, class Issued>
 __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeAttnParams& a,
                                            const Shared& sh, GateLane gate_lane, GateWarp gate_warp, Issued issued) {
+  constexpr int NG = N_REP / NREP;  // head groups of 8 KV heads
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int B = a.B;
+  const int B = a.B * NG;           // virtual sequences
   const int* pre = sh.pre;
   int* flags = sh.flags;
   const long long U = pre[B];
@@ -182,12 +194,12 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
       const int s = i % STAGES;
       const uint32_t dst = smem_u32(sh.ring + s * UNIT_BYTES);
       const uint32_t fb = smem_u32(&sh.full[s]);
-      const int pos = iss.j * UNIT;
+      const int pos = iss.j * UNIT, h0 = (iss.b % NG) * N_KV, sb = iss.b / NG;
       mbar_expect_tx(fb, UNIT_BYTES);
-      tma_load_4d(dst, &mk, fb, 0, pos, 0, iss.b);
-      tma_load_4d(dst + BOX_BYTES, &mk, fb, 64, pos, 0, iss.b);
-      tma_load_4d(dst + 2 * BOX_BYTES, &mv, fb, 0, pos, 0, iss.b);
-      tma_load_4d(dst + 3 * BOX_BYTES, &mv, fb, 64, pos, 0, iss.b);
+      tma_load_4d(dst, &mk, fb, 0, pos, h0, sb);
+      tma_load_4d(dst + BOX_BYTES, &mk, fb, 64, pos, h0, sb);
+      tma_load_4d(dst + 2 * BOX_BYTES, &mv, fb, 0, pos, h0, sb);
+      tma_load_4d(dst + 3 * BOX_BYTES, &mv, fb, 64, pos, h0, sb);
       advance(iss, pre, B);
     };
     int i = 0;
@@ -208,7 +220,7 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
   }
   if (warp > COMPUTE_WARPS) return true;
 
-  const int g = warp;  // KV head of this warp
+  const int g = warp;  // KV head of this warp within its group
   const int gr = lane >> 2, t = lane & 3;
   bool ok = true;
   if (n > 0) ok = compute_all(gate_warp());
@@ -219,17 +231,19 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
     float oacc[8][4];          // O^T tile d: (dim 16d + gr (+8), heads 2t, 2t+1)
     int seg_units = 0;
     long long seg_start = u0;
-    float* so = sh.stage_out + g * N_REP * HEAD_DIM;  // this warp's [4][128] staging
+    float* so = sh.stage_out + g * N_REP * HEAD_DIM;  // this warp's [4][128] staging (NREP rows used)
     for (int i = 0; i < n; ++i) {
       const long long u = u0 + i;
-      const int L = a.sp.get(cur.b) + 1;
+      const int L = a.sp.get(cur.b / NG) + 1;
       if (i == 0 || cur.j == 0) {
+        // query heads (8 (b % NG) + g) NREP + 0..NREP-1 of sequence b / NG
+        const int qh0 = ((cur.b % NG) * N_KV + g) * NREP;
         const uint32_t* q32 = reinterpret_cast<const uint32_t*>(
-            a.q + static_cast<size_t>(cur.b) * D_MODEL + static_cast<size_t>(g * N_REP + (gr & 3)) * HEAD_DIM);
+            a.q + static_cast<size_t>(cur.b / NG) * D_MODEL + static_cast<size_t>(qh0 + (gr % NREP)) * HEAD_DIM);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          qb[s][0] = gr < N_REP ? q32[s * 8 + t] : 0u;
-          qb[s][1] = gr < N_REP ? q32[s * 8 + 4 + t] : 0u;
+          qb[s][0] = gr < NREP ? q32[s * 8 + t] : 0u;
+          qb[s][1] = gr < NREP ? q32[s * 8 + 4 + t] : 0u;
         }
         m_run[0] = m_run[1] = -INFINITY;
         l_run[0] = l_run[1] = 0.f;
@@ -332,28 +346,34 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
       // lane -> head lane / 8, dims 16 (lane % 8) .. + 15
       const int hh = lane >> 3, d0 = (lane & 7) * 16;
       const float4* src = reinterpret_cast<const float4*>(so + hh * HEAD_DIM + d0);
+      const int qh = ((here.b % NG) * N_KV + g) * NREP + hh;  // query head of this lane's row
+      const bool real = hh < NREP;  // rows past NREP: padding of the multi-head variant
       if (whole) {
-        __nv_bfloat16* out = a.o + static_cast<size_t>(here.b) * D_MODEL + static_cast<size_t>(g * N_REP + hh) * HEAD_DIM + d0;
-        uint32_t w[8];
+        if (real) {
+          __nv_bfloat16* out = a.o + static_cast<size_t>(here.b / NG) * D_MODEL + static_cast<size_t>(qh) * HEAD_DIM + d0;
+          uint32_t w[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float4 v = src[e];
-          w[2 * e] = pack_bf16(v.x, v.y);
-          w[2 * e + 1] = pack_bf16(v.z, v.w);
+          for (int e = 0; e < 4; ++e) {
+            const float4 v = src[e];
+            w[2 * e] = pack_bf16(v.x, v.y);
+            w[2 * e + 1] = pack_bf16(v.z, v.w);
+          }
+          reinterpret_cast<uint4*>(out)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          reinterpret_cast<uint4*>(out)[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
-        reinterpret_cast<uint4*>(out)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        reinterpret_cast<uint4*>(out)[1] = make_uint4(w[4], w[5], w[6], w[7]);
       } else {
         const long long slot = 2LL * blockIdx.x + (seg_start == u0 ? 0 : 1);
-        float4* dst = reinterpret_cast<float4*>(a.part_o + (slot * N_HEADS + g * N_REP + hh) * HEAD_DIM + d0);
+        if (real) {
+          float4* dst = reinterpret_cast<float4*>(a.part_o + (slot * N_HEADS + g * NREP + hh) * HEAD_DIM + d0);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) __stcg(dst + e, src[e]);
-        // (max, sum) of query head g*4 + q is held by the lanes with t = q / 2
+          for (int e = 0; e < 4; ++e) __stcg(dst + e, src[e]);
+        }
+        // (max, sum) of the warp's query head q is held by the lanes with t = q / 2
         const int srcl = (lane >> 1) & 1;
         const float mq0 = __shfl_sync(0xffffffffu, m_run[0], srcl), mq1 = __shfl_sync(0xffffffffu, m_run[1], srcl);
         const float lq0 = __shfl_sync(0xffffffffu, l_run[0], srcl), lq1 = __shfl_sync(0xffffffffu, l_run[1], srcl);
-        if (lane < N_REP)
-          __stcg(reinterpret_cast<float2*>(a.part_ml + (slot * N_HEADS + g * N_REP + lane) * 2),
+        if (lane < NREP)
+          __stcg(reinterpret_cast<float2*>(a.part_ml + (slot * N_HEADS + g * NREP + lane) * 2),
                  (lane & 1) ? make_float2(mq1, lq1) : make_float2(mq0, lq0));
       }
       __syncwarp();  // the staging area is reused by the next sequence
@@ -371,9 +391,12 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
 // Called by the 256 compute threads of every CTA with `ok` from attn_units
 // (a CTA that gave up still meets, so that no other CTA waits in vain).
 // Returns false when any thread of the CTA gave up or the meeting timed out.
+template <int NREP>
 __device__ __forceinline__ bool attn_merge(const DecodeAttnParams& a, const Shared& sh, int* meet, bool ok) {
+  constexpr int NG = N_REP / NREP;   // virtual sequences per sequence
+  constexpr int HV = N_HEADS / NG;   // query heads of one virtual sequence
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int B = a.B;
+  const int B = a.B * NG;
   const int* pre = sh.pre;
   int* flags = sh.flags;
   const long long U = pre[B];
@@ -388,12 +411,12 @@ __device__ __forceinline__ bool attn_merge(const DecodeAttnParams& a, const Shar
     if (lane == 0) atomicExch(&flags[0], 1);
     return false;
   }
-  // merges: one warp per (sequence, query head) of every split sequence,
+  // merges: one warp per (virtual sequence, query head) of every split one,
   // spread over the SMs first (warp w of CTA c takes task w * C + c)
   const int hh4 = lane * 4;  // dims of this lane
-  for (long long task = static_cast<long long>(warp) * C + blockIdx.x; task < static_cast<long long>(B) * N_HEADS;
+  for (long long task = static_cast<long long>(warp) * C + blockIdx.x; task < static_cast<long long>(B) * HV;
        task += C * COMPUTE_WARPS) {
-    const int b = static_cast<int>(task / N_HEADS), h = static_cast<int>(task % N_HEADS);
+    const int b = static_cast<int>(task / HV), h = static_cast<int>(task % HV);
     const int nu = units_of(pre, b);
     if (nu == 0) continue;
     const long long ub = pre[b];
@@ -430,7 +453,7 @@ __device__ __forceinline__ bool attn_merge(const DecodeAttnParams& a, const Shar
       }
     }
     const float inv = 1.f / GL;
-    __nv_bfloat16* out = a.o + static_cast<size_t>(b) * D_MODEL + static_cast<size_t>(h) * HEAD_DIM + hh4;
+    __nv_bfloat16* out = a.o + static_cast<size_t>(b / NG) * D_MODEL + static_cast<size_t>((b % NG) * HV + h) * HEAD_DIM + hh4;
     *reinterpret_cast<uint2*>(out) = make_uint2(pack_bf16(go.x * inv, go.y * inv), pack_bf16(go.z * inv, go.w * inv));
   }
   fence_proxy_async_global();

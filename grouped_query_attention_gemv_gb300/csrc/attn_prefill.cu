@@ -7,7 +7,9 @@
 // One CTA owns 64 query positions of one sequence and the 4 query heads of
 // one KV group, as two 128-row Q tiles (32 positions x 4 heads each; row
 // r = position r/4, head r%4), so every 64-key K/V tile is staged once for
-// 8 x 32 query rows:
+// 8 x 32 query rows. In the multi-head variant (32 KV heads, one query head
+// each) a Q tile is 128 positions of one head and a CTA owns 256 positions:
+// the kernel is templated on the query heads per KV head, NREP.
 //   warp 8 (one lane)  TMA producer: both Q tiles once, then K_j / V_j
 //                      (128B swizzle, 4-stage rings on mbarriers)
 //   warps 9, 10        MMA issuers, one lane each, one per Q tile t: for key
@@ -42,9 +44,8 @@ namespace gqa {
 
 namespace {
 
-constexpr int QP = 32;                    // query positions per Q tile
+constexpr int ROWS = 128;                 // rows of a Q tile = MMA M
 constexpr int NQ = 2;                     // Q tiles per CTA
-constexpr int ROWS = QP * N_REP;          // 128 rows = MMA M
 constexpr int KT = PREFILL_TILE;          // keys per tile (= TMA box height)
 constexpr int STAGES = 4;                 // K tiles and V tiles in flight
 constexpr int Q_HALF = ROWS * 128;        // 128 rows x 64 dims
@@ -77,9 +78,12 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ bool aborted(const Bars& bs) { return *reinterpret_cast<const volatile int*>(&bs.abort) != 0; }
 
+template <int NREP>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, PrefillAttnParams a) {
+  constexpr int QP = ROWS / NREP;         // query positions per Q tile
+  constexpr int NKV = N_HEADS / NREP;     // KV heads
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars& bs = *reinterpret_cast<Bars*>(smem + BAR_OFF);
@@ -87,8 +91,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   // longest key ranges first: the pair of query tiles falls with blockIdx.x
   const int nqt = (a.T + QP - 1) / QP;
   const int npairs = (nqt + NQ - 1) / NQ;
-  const int g = blockIdx.x % N_KV;
-  const int rest = blockIdx.x / N_KV;
+  const int g = blockIdx.x % NKV;
+  const int rest = blockIdx.x / NKV;
   const int b = rest % a.B;
   const int pair = npairs - 1 - rest / a.B;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -146,8 +150,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_expect_tx(qb, NQ * Q_TILE);
       // a tile past T reads as zeros (its rows are never stored)
       for (int t = 0; t < NQ; ++t) {
-        tma_load_4d(sbase + t * Q_TILE, &mq, qb, 0, g * N_REP, q0 + t * QP, b);
-        tma_load_4d(sbase + t * Q_TILE + Q_HALF, &mq, qb, 64, g * N_REP, q0 + t * QP, b);
+        tma_load_4d(sbase + t * Q_TILE, &mq, qb, 0, g * NREP, q0 + t * QP, b);
+        tma_load_4d(sbase + t * Q_TILE + Q_HALF, &mq, qb, 64, g * NREP, q0 + t * QP, b);
       }
       int kn = 0, vn = 0;
       bool ok = true;
@@ -246,8 +250,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int t = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const int n_t = t ? nt[1] : nt[0];
-    const int pos = q0 + t * QP + (r >> 2);  // query index within the sequence
-    const int hh = r & 3;
+    const int pos = q0 + t * QP + r / NREP;  // query index within the sequence
+    const int hh = r % NREP;
     const int kv_end = start + min(q0 + t * QP + QP, a.T);
     const int lim = min(start + pos, kv_end - 1);  // last key this row sees
     const uint32_t lane_addr = tmem + t * TILE_COLS + (static_cast<uint32_t>((warp & 3) * 32) << 16);
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* dst = a.o + (static_cast<size_t>(b) * a.T + pos) * D_MODEL +
-                           static_cast<size_t>(g * N_REP + hh) * HEAD_DIM;
+                           static_cast<size_t>(g * NREP + hh) * HEAD_DIM;
 #pragma unroll 1
       for (int c = 0; c < HEAD_DIM; c += 32) {
         uint32_t o[32];
@@ -369,24 +373,35 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-}  // namespace
-
-cudaError_t launch_attn_prefill(const PrefillMaps& maps, const PrefillAttnParams& a, cudaStream_t s) {
+template <int NREP>
+cudaError_t launch_nrep(const PrefillMaps& maps, const PrefillAttnParams& a, cudaStream_t s) {
+  constexpr int QP = ROWS / NREP, NKV = N_HEADS / NREP;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  auto kern = attn_prefill_kernel<NREP>;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   if (a.B <= 0 || a.T <= 0) return cudaErrorInvalidValue;
-  const long long ctas = static_cast<long long>(((a.T + QP - 1) / QP + NQ - 1) / NQ) * N_KV * a.B;
+  const long long ctas = static_cast<long long>(((a.T + QP - 1) / QP + NQ - 1) / NQ) * NKV * a.B;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-  attn_prefill_kernel<<<static_cast<unsigned>(ctas), THREADS, SMEM_BYTES, s>>>(maps.q, maps.k, maps.v, a);
+  kern<<<static_cast<unsigned>(ctas), THREADS, SMEM_BYTES, s>>>(maps.q, maps.k, maps.v, a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_prefill(const PrefillMaps& maps, const PrefillAttnParams& a, cudaStream_t s) {
+  switch (a.n_kv) {
+    case N_KV: return launch_nrep<N_REP>(maps, a, s);
+    case N_HEADS: return launch_nrep<1>(maps, a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace gqa

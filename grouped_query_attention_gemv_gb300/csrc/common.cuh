@@ -17,6 +17,7 @@ constexpr int HEAD_DIM = 128;
 constexpr int N_REP = N_HEADS / N_KV;          // query heads per KV head
 constexpr int KV_ROW = N_KV * HEAD_DIM;       // elements of one cache position
 constexpr int QKV_ROWS = D_MODEL + 2 * KV_ROW;  // 6144 fused projection outputs
+constexpr int QKV_ROWS_MAX = 3 * D_MODEL;        // the multi-head variant's (32 KV heads)
 constexpr int ROPE_PAIRS = HEAD_DIM / 2;
 
 // Device status codes (mirrors GQA_DEV_* in gqa.h).

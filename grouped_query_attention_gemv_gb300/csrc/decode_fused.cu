@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
     for (int i = 0; i < 4; ++i) flags_a[i] = flags_b[i] = flags_c[i] = 0;
     fence_barrier_init();
   }
-  if (warp == rowsk::WARPS - 1) attnk::build_prefix(fp.at, pre);
+  if (warp == rowsk::WARPS - 1) attnk::build_prefix<1>(fp.at, pre);
   __syncthreads();
   const int grid = static_cast<int>(gridDim.x);
   int* const cnt = fp.counters;
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   rowsk::rows_phase<CfgA<NP>, true>(
       m.qkv, fp.pq, fp.qkv_plan, sha, []() { return true; }, []() { return true; },
       [&fp, &m, pre]() {
-        attnk::prefetch_units(&m.cache.k, &m.cache.v, fp.at, pre, attnk::STAGES, KV_PREFETCH_UNITS);
+        attnk::prefetch_units<1>(&m.cache.k, &m.cache.v, fp.at, pre, attnk::STAGES, KV_PREFETCH_UNITS);
       },
       [cnt]() { signal_counter(&cnt[0], 1); }, a_started);
   fence_proxy_async_smem();  // the ring's generic reads and writes precede phase B's TMA writes into it
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
                           reinterpret_cast<float*>(smem + attnk::RING)};
   bool units_ok = true;
   if (!aborted) {
-    units_ok = attnk::attn_units(
+    units_ok = attnk::attn_units<N_REP>(
         m.cache.k, m.cache.v, fp.at, shb,
         // one poller per CTA: the producer lane waits on the grid counter and
         // hands the outcome to the compute warps through shared memory
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   if (!aborted && flags_b[0]) {
     // this CTA's units gave up: it still meets the grid (no other CTA waits in vain)
     if (warp < attnk::COMPUTE_WARPS) {
-      attnk::attn_merge(fp.at, shb, &cnt[3], false);
+      attnk::attn_merge<N_REP>(fp.at, shb, &cnt[3], false);
       if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
     }
   } else if (!aborted) {
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
                                          return ok;
                                        },
                                        [&fp, &shb, cnt, units_ok]() {
-                                         const bool ok = attnk::attn_merge(fp.at, shb, &cnt[3], units_ok);
+                                         const bool ok = attnk::attn_merge<N_REP>(fp.at, shb, &cnt[3], units_ok);
                                          // this CTA's attention outputs (whole sequences, merges) are fenced
                                          if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
                                          return ok;
@@ -286,6 +286,7 @@ int decode_fused_np(int M) {
 }
 
 cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
+  if (a.at.n_kv != N_KV) return cudaErrorInvalidValue;  // 8 KV heads (the row split of phase A)
   switch (decode_fused_np(a.pq.M)) {
     case 8: return launch_fused_np<8>(a, s);
     case 16: return launch_fused_np<16>(a, s);

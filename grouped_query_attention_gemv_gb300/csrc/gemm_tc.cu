@@ -127,9 +127,9 @@ __device__ __forceinline__ void epilogue_tile(const ProjParams& p, uint32_t acc,
           dst = p.out + static_cast<size_t>(m) * D_MODEL + n0;
           rope = true;
         } else {
-          const size_t row = (static_cast<size_t>(b) * p.s_max + pos) * KV_ROW;
-          rope = n0 < D_MODEL + KV_ROW;
-          dst = rope ? p.cache_k + row + (n0 - D_MODEL) : p.cache_v + row + (n0 - D_MODEL - KV_ROW);
+          const size_t row = (static_cast<size_t>(b) * p.s_max + pos) * (p.r2 - p.r1);
+          rope = n0 < p.r2;
+          dst = rope ? p.cache_k + row + (n0 - D_MODEL) : p.cache_v + row + (n0 - p.r2);
         }
       } else if (t == 0 && n0 == 0) {
         report(p.status, DEV_BAD_POSITION);

@@ -9,7 +9,8 @@ namespace gqa {
 // One projection y = x W^T over M tokens (rows of x, stride 4096) and N
 // output features. The weight is up to three [rows, 4096] matrices stacked
 // along the output axis: rows [0, r1) from w0, [r1, r2) from w1, [r2, N) from
-// w2 (the fused Q|K|V projection uses wq, wk, wv with r1 = 4096, r2 = 5120).
+// w2 (the fused Q|K|V projection uses wq, wk, wv with r1 = 4096 and
+// r2 - r1 = N - r2 = the cache row: 1024 for 8 KV heads, 4096 for 32).
 struct ProjParams {
   const __nv_bfloat16* x;
   int M;   // tokens
@@ -57,9 +58,9 @@ __device__ __forceinline__ __nv_bfloat16* proj_dst(const ProjParams& p, int m, i
   }
   pos = start + t;
   if (f < D_MODEL) return p.out + static_cast<size_t>(m) * D_MODEL + f;
-  const size_t row = (static_cast<size_t>(b) * p.s_max + pos) * KV_ROW;
-  if (f < D_MODEL + KV_ROW) return p.cache_k + row + (f - D_MODEL);
-  return p.cache_v + row + (f - D_MODEL - KV_ROW);
+  const size_t row = (static_cast<size_t>(b) * p.s_max + pos) * (p.r2 - p.r1);
+  if (f < p.r2) return p.cache_k + row + (f - D_MODEL);
+  return p.cache_v + row + (f - p.r2);
 }
 
 // Epilogue for 16 consecutive features f..f+15 (f multiple of 16) of token m.
@@ -67,7 +68,7 @@ __device__ __forceinline__ void proj_store16(const ProjParams& p, int m, int f, 
   int pos;
   __nv_bfloat16* dst = proj_dst(p, m, f, pos);
   if (!dst) return;
-  if (p.qkv && f < D_MODEL + KV_ROW) {
+  if (p.qkv && f < p.r2) {
     const float4* cs = reinterpret_cast<const float4*>(
         p.rope + (static_cast<size_t>(pos) * ROPE_PAIRS + ((f & (HEAD_DIM - 1)) >> 1)) * 2);
 #pragma unroll
@@ -100,7 +101,7 @@ __device__ __forceinline__ void proj_store2(const ProjParams& p, int m, int f, f
   int pos;
   __nv_bfloat16* dst = proj_dst(p, m, f, pos);
   if (!dst) return;
-  if (p.qkv && f < D_MODEL + KV_ROW) rope_pair(p.rope, pos, f, a, b);
+  if (p.qkv && f < p.r2) rope_pair(p.rope, pos, f, a, b);
   *reinterpret_cast<uint32_t*>(dst) = pack_bf16(a, b);
 }
 
@@ -146,6 +147,7 @@ constexpr int PREFILL_TILE = 64;    // cache positions per TMA box of the prefil
 struct DecodeAttnParams {
   const __nv_bfloat16* q;  // [B][4096] rotated queries
   int B;
+  int n_kv;                // KV heads: 8, or 32 (the multi-head variant)
   StartPos sp;             // keys 0..sp(b) are read
   int ctas;                // grid size (one CTA per SM)
   float* part_o;           // [attn_decode_slots(ctas) / 8][32 query heads][128]
@@ -153,7 +155,7 @@ struct DecodeAttnParams {
   int* counters;           // [2] grid counters (meeting, exit), zero-filled, left zero-filled
   __nv_bfloat16* o;        // [B][4096]
   int* status;
-  const __nv_bfloat16* cache_k;  // [B][s_max][8][128], for L2 prefetches only
+  const __nv_bfloat16* cache_k;  // [B][s_max][n_kv][128], for L2 prefetches only
   const __nv_bfloat16* cache_v;
   int s_max;
 };
@@ -171,12 +173,13 @@ cudaError_t launch_attn_decode(const DecodeCacheMaps& maps, const DecodeAttnPara
 struct PrefillAttnParams {
   const __nv_bfloat16* q;  // [B*T][4096] rotated queries
   int B, T;
+  int n_kv;                // KV heads: 8, or 32 (the multi-head variant)
   StartPos sp;             // common start position (chunked prefill when > 0)
   __nv_bfloat16* o;        // [B*T][4096]
   int* status;
 };
 // Tensor maps of the prefill attention: q over (dim, head, token, sequence)
-// with boxes of 64 dims x 4 heads x 32 tokens; k / v over (dim, KV head,
+// with boxes of 64 dims x n_rep heads x 128 / n_rep tokens; k / v over (dim, KV head,
 // position, sequence) with boxes of 64 dims x 1 head x PREFILL_TILE positions
 // and a position extent of start_pos + T, so later positions read as zero.
 struct PrefillMaps {

@@ -98,7 +98,7 @@ __device__ __forceinline__ void store_tile(const ProjParams& p, int rt, int r, f
     float v = acc[m];
     if constexpr (QKV) {
       const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-      if (m < p.M && f < D_MODEL + KV_ROW) {
+      if (m < p.M && f < p.r2) {
         const int b = m / p.T;
         const int start = p.sp.get(b);
         if (p.sp.ok(start)) {
@@ -130,8 +130,8 @@ __device__ __forceinline__ void store_tile(const ProjParams& p, int rt, int r, f
       if (f0 < D_MODEL) {
         dst = p.out + static_cast<size_t>(m) * D_MODEL + f0;
       } else {
-        const size_t row = (static_cast<size_t>(b) * p.s_max + pos) * KV_ROW;
-        dst = f0 < D_MODEL + KV_ROW ? p.cache_k + row + (f0 - D_MODEL) : p.cache_v + row + (f0 - D_MODEL - KV_ROW);
+        const size_t row = (static_cast<size_t>(b) * p.s_max + pos) * (p.r2 - p.r1);
+        dst = f0 < p.r2 ? p.cache_k + row + (f0 - D_MODEL) : p.cache_v + row + (f0 - p.r2);
       }
     } else {
       dst = p.out + static_cast<size_t>(m) * p.N + rt * TILE_ROWS;

@@ -293,7 +293,7 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
       const int start = p.sp.get(b);
       if (p.sp.ok(start)) {
         pos_pf[k] = start + (m - b * p.T);
-        if (f < D_MODEL + KV_ROW)
+        if (f < p.r2)
           cs_pf[k] = *reinterpret_cast<const float2*>(
               p.rope + (static_cast<size_t>(pos_pf[k]) * ROPE_PAIRS + ((f & (HEAD_DIM - 1)) >> 1)) * 2);
       }
@@ -395,7 +395,7 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     if constexpr (QKV) {
       if (pos < 0) return;  // a start position out of range (reported by the attention)
       const int b = m / p.T;
-      if (f < D_MODEL + KV_ROW) {
+      if (f < p.r2) {
         const float y0 = x0 * cs.x - x1 * cs.y;
         const float y1 = x0 * cs.y + x1 * cs.x;
         x0 = y0;
@@ -404,8 +404,8 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
       if (f < D_MODEL) {
         dst = p.out + static_cast<size_t>(m) * D_MODEL + f;
       } else {
-        const size_t row = (static_cast<size_t>(b) * p.s_max + pos) * KV_ROW;
-        dst = f < D_MODEL + KV_ROW ? p.cache_k + row + (f - D_MODEL) : p.cache_v + row + (f - D_MODEL - KV_ROW);
+        const size_t row = (static_cast<size_t>(b) * p.s_max + pos) * (p.r2 - p.r1);
+        dst = f < p.r2 ? p.cache_k + row + (f - D_MODEL) : p.cache_v + row + (f - p.r2);
       }
     } else {
       dst = p.out + static_cast<size_t>(m) * p.N + f;
@@ -431,7 +431,7 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
       const int start = p.sp.get(b);
       if (p.sp.ok(start)) {
         pos = start + (m - b * p.T);
-        if (f < D_MODEL + KV_ROW)
+        if (f < p.r2)
           cs = *reinterpret_cast<const float2*>(
               p.rope + (static_cast<size_t>(pos) * ROPE_PAIRS + ((f & (HEAD_DIM - 1)) >> 1)) * 2);
       }

@@ -125,12 +125,41 @@ int gqa_block_forward(const gqa_bf16* x, int B, int T, int start_pos,
  * GQA_DEV_BAD_POSITION in the status word and sequence b is skipped: its
  * cache rows are not written and its output row is unspecified. Other
  * arguments as in
- * gqa_block_forward with x [B, 1, 4096] and out [B, 1, 4096]. */
+ * gqa_block_forward with x [B, 1, 4096] and out [B, 1, 4096]. The split
+ * work is counted in 32 bits: B x ceil((max_start_pos + 1) / 16) x (SMs + 1)
+ * must stay below 2^32 (about 28 million cache positions over the batch on
+ * 152 SMs, far past what one GPU's memory holds), else GQA_EINVAL. */
 int gqa_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos,
                const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo,
                const float* rope, int rope_rows, gqa_bf16* cache_k, gqa_bf16* cache_v,
                int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
                void* stream);
+
+/* The multi-head variant next to the grouped one: "Llama 3.1 8B ·
+ * Grouped-query attention" sets the model's 8 KV heads against MHA with 32
+ * K/V heads (its table of KV cache per token: 512 KiB over all layers
+ * against 128 KiB), and its repeat_kv excerpt returns the keys and values
+ * unchanged when n_rep = 1. n_kv_heads selects the KV heads:
+ *   8   the Llama 3.1 8B block (the same operation as gqa_block_forward /
+ *       gqa_decode)
+ *   32  one KV head per query head: wk, wv [4096, 4096]; cache_k, cache_v
+ *       [B, s_max, 32, 128] bf16 (8 KB of K and 8 KB of V per position);
+ *       query head h attends with KV head h
+ * Any other value is GQA_EINVAL. Every other argument, the workspace size
+ * (gqa_workspace_bytes covers both), the cache update and the error
+ * behaviour as in gqa_block_forward / gqa_decode; gqa_decode_nkv with 32 KV
+ * heads also requires B <= 512. The multi-head decode step runs as three
+ * kernels (the fused decode grid is sized for 8 KV heads). */
+int gqa_block_forward_nkv(const gqa_bf16* x, int B, int T, int start_pos, int n_kv_heads,
+                          const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv,
+                          const gqa_bf16* wo, const float* rope, int rope_rows,
+                          gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max, gqa_bf16* out,
+                          void* workspace, size_t workspace_bytes, void* stream);
+int gqa_decode_nkv(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos,
+                   int n_kv_heads, const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv,
+                   const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
+                   gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace,
+                   size_t workspace_bytes, void* stream);
 
 /* Causal prefill of T >= 1 new tokens per sequence after start_pos cached
  * rows (start_pos > 0 is a chunked prefill over an existing prefix).

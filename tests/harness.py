@@ -27,21 +27,23 @@ class Case:
     s_max: int
     seed: int = 0
     rope: I.RopeConfig = I.LLAMA31_ROPE
+    dims: I.Dims = I.LLAMA31_8B
     dev: dict = field(default_factory=dict)     # device tensors
     host: dict = field(default_factory=dict)    # CPU copies of the inputs
 
 
 def make_case(B: int, T: int, start: Sequence[int], s_max: int, seed: int = 0,
-              rope: I.RopeConfig = I.LLAMA31_ROPE, weights=None, cache_device=None) -> Case:
+              rope: I.RopeConfig = I.LLAMA31_ROPE, weights=None, cache_device=None,
+              dims: I.Dims = I.LLAMA31_8B) -> Case:
     """Seeded inputs on cuda:0 (weights may be shared between cases)."""
     start = [int(s) for s in start]
-    c = Case(B, T, start, s_max, seed, rope)
+    c = Case(B, T, start, s_max, seed, rope, dims)
     if weights is None:
-        gen, w = I.draw_weights(seed=seed)
+        gen, w = I.draw_weights(dims, seed=seed)
     else:
         gen, w = weights
     x = I.draw_x(gen, B, T)
-    ck, cv = I.draw_cache(B, s_max, start, seed=seed, device=cache_device)
+    ck, cv = I.draw_cache(B, s_max, start, dims, seed=seed, device=cache_device)
     c.host = {"x": x, **w}
     c.dev = {k: v.to("cuda") for k, v in c.host.items()}
     c.dev["cache_k"] = ck.to("cuda")
@@ -76,7 +78,7 @@ def oracle_sequence(c: Case, b: int, query_rows=None):
     ck = f64(c.dev["cache_k0"][b, :sp])
     cv = f64(c.dev["cache_v0"][b, :sp])
     return O.sequence_forward(f64(c.host["x"][b]), w["wq"], w["wk"], w["wv"], w["wo"], sp, ck, cv,
-                              freqs, 32, 8, query_rows)
+                              freqs, c.dims.n_heads, c.dims.n_kv_heads, query_rows)
 
 
 def oracle_layer_sequence(c: Case, b: int, g: torch.Tensor, eps: float, query_rows=None):

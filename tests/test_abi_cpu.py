@@ -132,3 +132,33 @@ def test_layer_entries_reject_bad_arguments(lib):
     bad = list(okd)
     bad[15] = FAKE
     assert d(*bad) == -1
+
+
+def test_kv_head_entries_reject_bad_arguments(lib):
+    """gqa_block_forward_nkv / gqa_decode_nkv take 8 or 32 KV heads only; the
+    multi-head decode caps the batch at 512 (its 4 head groups per sequence
+    are attention units of their own), and every decode call refuses a unit
+    count that the 32-bit split of the work could not hold."""
+    f = lib.gqa_block_forward_nkv
+    ok = [FAKE, 2, 1, 5, 8, FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, FAKE, 64, FAKE, FAKE, 1 << 40, None]
+    for n_kv in (0, 1, 4, 16, 64, -8):
+        bad = list(ok)
+        bad[4] = n_kv
+        assert f(*bad) == -1, n_kv
+    bad = list(ok)
+    bad[0] = None
+    assert f(*bad) == -1
+    d = lib.gqa_decode_nkv
+    okd = [FAKE, 4, FAKE, 10, 32, FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, FAKE, 64, FAKE, FAKE, 1 << 40, None]
+    bad = list(okd)
+    bad[4] = 16
+    assert d(*bad) == -1
+    bad = list(okd)
+    bad[1] = 513          # 32 KV heads: at most 512 sequences
+    assert d(*bad) == -1
+    big = (1 << 30) + 1   # 2^26 units per sequence: 32-bit unit arithmetic would overflow
+    for fn, a in ((lib.gqa_decode, [FAKE, 64, FAKE, 1 << 30, FAKE, FAKE, FAKE, FAKE, FAKE, big, FAKE, FAKE, big,
+                                    FAKE, FAKE, 1 << 40, None]),
+                  (d, [FAKE, 64, FAKE, 1 << 30, 32, FAKE, FAKE, FAKE, FAKE, FAKE, big, FAKE, FAKE, big, FAKE, FAKE,
+                       1 << 40, None])):
+        assert fn(*a) == -1

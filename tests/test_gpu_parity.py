@@ -405,3 +405,85 @@ def test_layer_decode_chained_layers_match_oracle(fused):
         # delta bar
         err = np.abs(got - h) - L * H.bf16_ulp(np.abs(h))
         assert float(err.max()) <= H.MAX_ABS_TOL
+
+
+# ------------------------------------------------------------ multi-head variant
+
+@pytest.fixture(scope="module")
+def mha_weights():
+    return I.draw_weights(I.LLAMA31_8B_MHA, seed=3)
+
+
+@pytest.mark.parametrize("B,starts,s_max", [
+    (1, [15], 16),                                    # few tokens: stream-K projections, one sequence
+    (4, [0, 17, 128, 300], 320),                      # ragged positions, split sequences
+    (80, [int(v) for v in np.random.default_rng(5).integers(0, 90, 80)], 96),  # tcgen05 GEMM projections
+])
+def test_mha_decode_matches_oracle(mha_weights, B, starts, s_max):
+    """32 KV heads (query head h with KV head h): the decode path over head
+    groups, against the oracle with n_kv_heads = 32."""
+    c = H.make_case(B, 1, starts, s_max, seed=3, weights=mha_weights, dims=I.LLAMA31_8B_MHA)
+    d = c.dev
+    sp = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    ws = G.make_workspace(B, 1, max(starts) + 1)
+    out = G.decode(d["x"], sp, max(starts), d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"],
+                   d["cache_v"], workspace=ws, n_kv_heads=32)
+    torch.cuda.synchronize()
+    assert G.device_status(ws) == 0
+    for b in range(0, B, max(1, B // 6)):
+        H.compare_sequence(c, out, b)
+    H.check_canaries(c)
+
+
+@pytest.mark.parametrize("B,T,start,s_max", [
+    (1, 5, 0, 8),          # few tokens
+    (2, 37, 0, 40),        # one ragged 128-position tile
+    (1, 300, 0, 304),      # two CTAs' worth of 256 positions, ragged
+    (1, 96, 300, 400),     # chunked: 96 tokens after 300 cached
+])
+def test_mha_prefill_matches_oracle(mha_weights, B, T, start, s_max):
+    c = H.make_case(B, T, [start] * B, s_max, seed=3, weights=mha_weights, dims=I.LLAMA31_8B_MHA)
+    d = c.dev
+    ws = G.make_workspace(B, T, start + T)
+    out = G.block_forward(d["x"], start, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"],
+                          d["cache_v"], workspace=ws, n_kv_heads=32)
+    torch.cuda.synchronize()
+    assert G.device_status(ws) == 0
+    rows = None if T <= 96 else sorted({0, 1, 127, 128, 129, 255, 256, T - 1})
+    for b in range(B):
+        H.compare_sequence(c, out, b, query_rows=rows, check_cache=rows is None)
+    if rows is not None:
+        # every new cache row, checked against the oracle's rows from one full pass
+        _, nk, nv = H.oracle_sequence(c, 0, [0])
+        H.check_rows_within_one_ulp(d["cache_k"][0, start:start + T], nk, "cache_k rows")
+        H.check_rows_within_one_ulp(d["cache_v"][0, start:start + T], nv, "cache_v rows")
+    H.check_canaries(c)
+
+
+def test_mha_with_duplicated_kv_heads_equals_gqa(weights):
+    """The multi-head path run on K/V heads duplicated 4 times (and the
+    matching weights) gives the grouped path's result: the repeat_kv map
+    h // 4 pinned on the GPU."""
+    B, starts, s_max = 3, [5, 40, 77], 80
+    c = H.make_case(B, 1, starts, s_max, weights=weights)
+    d = c.dev
+    rep4 = lambda w: w.view(8, 128, 4096).repeat_interleave(4, dim=0).reshape(4096, 4096).contiguous()
+    ck4 = d["cache_k0"].repeat_interleave(4, dim=2).contiguous()
+    cv4 = d["cache_v0"].repeat_interleave(4, dim=2).contiguous()
+    sp = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    rope = H.rope_for(c)
+    g = G.decode(d["x"], sp, max(starts), d["wq"], d["wk"], d["wv"], d["wo"], rope, d["cache_k"], d["cache_v"])
+    m = G.decode(d["x"], sp, max(starts), d["wq"], rep4(d["wk"]), rep4(d["wv"]), d["wo"], rope, ck4, cv4,
+                 n_kv_heads=32)
+    torch.cuda.synchronize()
+    # the two runs accumulate in different kernels (the grouped decode step is
+    # one fused grid): equal up to rounding, where a wrong head map is O(1) off
+    r2 = H.rel_l2(H.f64(m), H.f64(g))
+    assert r2 <= 5e-3, r2
+    for b in range(B):
+        for cm, cg in ((ck4, d["cache_k"]), (cv4, d["cache_v"])):
+            # each of the four copies of a KV head (summed in different k
+            # splits of the stream-K projection) within an ulp of the grouped row
+            new = cm[b, starts[b]].view(8, 4, 128)
+            for r in range(4):
+                H.check_rows_within_one_ulp(new[:, r], H.f64(cg[b, starts[b]]), f"new row {r} of sequence {b}")
