@@ -61,6 +61,7 @@ def args_():
     ap.add_argument("--replicas", type=int, default=4)
     ap.add_argument("--graph-steps", type=int, default=8, help="steps captured per CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample", type=float, default=None, help=argparse.SUPPRESS)  # internal: one-core leg
     ap.add_argument("--entry", choices=["block", "layer"], default="block",
                     help="block: delta = attention(x); layer: h = x + attention(RMSNorm(x)) (one more kernel)")
     ap.add_argument("--decode-kernels", choices=["fused", "three"], default="fused",
@@ -194,9 +195,11 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
-def cpu_baseline(w: I.Workload, budget_s: float = 12.0):
+def cpu_baseline(w: I.Workload, budget_s: float = 12.0, one_core: bool = True):
     """The oracle, as it stands, on a bounded sample: whole sequences of the
-    workload (projections, attention, output) until the budget is spent."""
+    workload (projections, attention, output) until the budget is spent. With
+    ``one_core`` the same sample also runs in a child process whose BLAS is
+    held to one thread (a shorter budget), reported as ``one_core_value``."""
     from oracle import gqa as O
     gen, wt = I.draw_weights(w.dims, seed=w.seed)
     x = I.draw_x(gen, w.B, w.T)
@@ -221,10 +224,21 @@ def cpu_baseline(w: I.Workload, budget_s: float = 12.0):
             break
     threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
     what = "layer steps (one sequence through one layer" if w.layers > 1 else "decode steps (whole sequences"
-    return {"value": n / el / w.layers, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n} single-sequence {what}: projections, attention over P+1 keys, output projection) of "
-                      f"{w.name}, {el:.1f} s, numpy float64"
-                      + (f"; value = that rate / {w.layers} layers" if w.layers > 1 else "")}
+    out = {"value": n / el / w.layers, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
+           "sample": f"{n} single-sequence {what}: projections, attention over P+1 keys, output projection) of "
+                     f"{w.name}, {el:.1f} s, numpy float64"
+                     + (f"; value = that rate / {w.layers} layers" if w.layers > 1 else "")}
+    if one_core:
+        env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--workload", w.name, "--oracle-sample",
+                            str(budget_s / 2)], env=env, capture_output=True, text=True, timeout=300)
+        if r.returncode == 0 and r.stdout.strip():
+            one = json.loads(r.stdout.strip().splitlines()[-1])
+            out["one_core_value"] = one["value"]
+            out["one_core_sample"] = one["sample"]
+        else:
+            out["one_core_value"] = None
+    return out
 
 
 def _oracle_unit(w: I.Workload, O, W, freqs, per):
@@ -326,6 +340,9 @@ def main():
     a = args_()
     rank, world, local = dist_env()
     w = I.workload(a.workload)
+    if a.oracle_sample is not None:   # the one-core leg of the CPU baseline (a child of cpu_baseline)
+        print(json.dumps(cpu_baseline(w, a.oracle_sample, one_core=False)))
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo" if a.impl == "reference" else "nccl")
