@@ -3,10 +3,14 @@
 // the "Query projection" page), K fixed at 4096.
 //
 // Persistent: one CTA per SM walks the 128 x 256 output tiles t = CTA,
-// CTA + grid, ... with the output features fastest: the CTAs in flight cover
-// a few token tiles against the whole weight matrix (50 MB for Q|K|V, which
-// L2 holds), so both x and W come from HBM once. (Token tiles fastest made
-// every wave sweep all of x: at 8192 tokens its 67 MB were read ~10 times.)
+// CTA + grid, ... with the output features fastest within groups of at most
+// 24 feature tiles (48 MB of weights): the CTAs in flight cover a few token
+// tiles against one group, which L2 holds while every token tile passes over
+// it, so W comes from HBM once and x once per group. Q|K|V with 8 KV heads
+// (24 tiles) and W_O (16) are one group; the multi-head Q|K|V (48 tiles,
+// 100 MB) is two, where one group over all of it read W ~5 times at 2048
+// tokens. (Token tiles fastest made every wave sweep all of x: at 8192 tokens
+// its 67 MB were read ~10 times.)
 //   warp 0 (one lane)   TMA producer: 128x64 x tile and 256x64 W tile per
 //                       stage, 128B-swizzled, 4-stage ring on mbarriers, one
 //                       ring across the CTA's tiles
@@ -38,6 +42,16 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
 constexpr int EPI_WARPS = 4;
+constexpr int GROUP_N = 24;  // feature tiles per group of the tile walk
+
+// Tile t of the walk -> its first token m0 and first output feature n0.
+__device__ __forceinline__ void tile_of(int t, int tiles_m, int tiles_n, int& m0, int& n0) {
+  const int per_group = tiles_m * GROUP_N;
+  const int g = t / per_group, r = t - g * per_group;
+  const int gw = min(GROUP_N, tiles_n - g * GROUP_N);
+  m0 = (r / gw) * BM;
+  n0 = (g * GROUP_N + r % gw) * BN;
+}
 
 struct Bars {
   uint64_t full[STAGES], empty[STAGES];
@@ -180,7 +194,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int tiles_n = p.N / BN;
-  const int tiles = ((p.M + BM - 1) / BM) * tiles_n;
+  const int tiles_m = (p.M + BM - 1) / BM;
+  const int tiles = tiles_m * tiles_n;
   const int G = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
@@ -217,7 +232,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < tiles; t += G) {
-        const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
+        int m0, n0;
+        tile_of(t, tiles_m, tiles_n, m0, n0);
         int brow;
         const CUtensorMap* mb = weight_of(p, &map_b0, &map_b1, &map_b2, n0, brow);
         for (int kb = 0; kb < NKB; ++kb, ++it) {
@@ -294,7 +310,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int m0 = (t / tiles_n) * BM, n0 = (t % tiles_n) * BN;
+      int m0, n0;
+      tile_of(t, tiles_m, tiles_n, m0, n0);
       epilogue_tile(p, lane_addr + buf * BN, m0 + quarter * 32 + lane, n0);
       tc_fence_before();
       __syncwarp();

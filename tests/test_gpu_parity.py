@@ -487,3 +487,39 @@ def test_mha_with_duplicated_kv_heads_equals_gqa(weights):
             new = cm[b, starts[b]].view(8, 4, 128)
             for r in range(4):
                 H.check_rows_within_one_ulp(new[:, r], H.f64(cg[b, starts[b]]), f"new row {r} of sequence {b}")
+
+
+@pytest.mark.parametrize("name,rows", [("prefill_chunk_b1_t1024_p7168", 64), ("mha_prefill_b1_t2048", 96)])
+def test_next_prefill_workloads_full(weights, mha_weights, name, rows):
+    """The bench's chunked and multi-head prefill workloads at full size, on
+    sampled query rows (plus the first and last, and the rows either side of a
+    128-position tile edge)."""
+    w = I.workload(name)
+    wts = mha_weights if w.n_kv_heads == 32 else weights
+    seed = 3 if w.n_kv_heads == 32 else 0
+    c = H.make_case(w.B, w.T, w.start_positions().tolist(), w.cache_rows(), seed=seed, weights=wts, dims=w.dims)
+    d = c.dev
+    ws = G.make_workspace(w.B, w.T, c.start[0] + w.T)
+    out = G.block_forward(d["x"], c.start[0], d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"],
+                          d["cache_v"], workspace=ws, n_kv_heads=w.n_kv_heads)
+    torch.cuda.synchronize()
+    assert G.device_status(ws) == 0
+    g = np.random.default_rng(2)
+    q = sorted(set(g.choice(w.T, rows, replace=False).tolist()) | {0, 127, 128, w.T - 1})
+    H.compare_sequence(c, out, 0, query_rows=q)
+    H.check_canaries(c)
+
+
+def test_mha_decode_workload_full(mha_weights):
+    w = I.workload("mha_decode_b16_p1000")
+    c = H.make_case(w.B, 1, w.start_positions().tolist(), w.cache_rows(), seed=3, weights=mha_weights, dims=w.dims)
+    d = c.dev
+    sp = torch.tensor(c.start, dtype=torch.int32, device="cuda")
+    ws = G.make_workspace(w.B, 1, max(c.start) + 1)
+    out = G.decode(d["x"], sp, max(c.start), d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"],
+                   d["cache_v"], workspace=ws, n_kv_heads=32)
+    torch.cuda.synchronize()
+    assert G.device_status(ws) == 0
+    for b in range(w.B):
+        H.compare_sequence(c, out, b)
+    H.check_canaries(c)
