@@ -59,6 +59,7 @@ constexpr int RING = STAGES * UNIT_BYTES;
 constexpr int STAGE_OUT_BYTES = COMPUTE_WARPS * N_REP * HEAD_DIM * 4;  // per-warp o staging
 constexpr float SCALE_LOG2 = 0.08838834764831845f * 1.4426950408889634f;
 constexpr int MERGE_SLOTS = 16;               // slots whose loads are in flight together in a merge
+constexpr int PRE_GATE_UNITS = STAGES;        // units requested before the gate (at most STAGES)
 
 struct Cursor {
   int b, j;  // virtual sequence (sequence b / NG, head group b % NG), unit within it
@@ -204,7 +205,7 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
     };
     int i = 0;
     // before the gate: units that do not hold a sequence's new row
-    while (i < n && i < STAGES && iss.j + 1 < units_of(pre, iss.b)) issue(i++);
+    while (i < n && i < PRE_GATE_UNITS && iss.j + 1 < units_of(pre, iss.b)) issue(i++);
     bool ok = gate_lane();
     for (; ok && i < n; ++i) {
       if (i >= STAGES && !mbar_wait(smem_u32(&sh.empty[i % STAGES]), ((i / STAGES) & 1) ^ 1)) {

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   rowsk::rows_phase<CfgA<NP>, true>(
       m.qkv, fp.pq, fp.qkv_plan, sha, []() { return true; }, []() { return true; },
       [&fp, &m, pre]() {
-        attnk::prefetch_units<1>(&m.cache.k, &m.cache.v, fp.at, pre, attnk::STAGES, KV_PREFETCH_UNITS);
+        attnk::prefetch_units<1>(&m.cache.k, &m.cache.v, fp.at, pre, attnk::PRE_GATE_UNITS, KV_PREFETCH_UNITS);
       },
       [cnt]() { signal_counter(&cnt[0], 1); }, a_started);
   fence_proxy_async_smem();  // the ring's generic reads and writes precede phase B's TMA writes into it
