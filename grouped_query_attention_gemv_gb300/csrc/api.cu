@@ -96,32 +96,82 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Every tensor map of this library: bf16, 128-byte swizzle, no interleave,
+// 256-byte L2 promotion, zero fill. Encoding one costs the host about a
+// microsecond and a decode call needs ~16, so each thread keeps the last
+// ones it encoded (a map depends only on these arguments; the buffers behind
+// the pointers are the caller's and are not read).
+struct MapKey {
+  const void* ptr;
+  cuuint32_t rank;
+  cuuint64_t dims[4];
+  cuuint64_t strides[3];
+  cuuint32_t box[4];
+  bool operator==(const MapKey& o) const {
+    if (ptr != o.ptr || rank != o.rank) return false;
+    for (cuuint32_t i = 0; i < rank; ++i)
+      if (dims[i] != o.dims[i] || box[i] != o.box[i] || (i + 1 < rank && strides[i] != o.strides[i])) return false;
+    return true;
+  }
+};
+constexpr int MAP_CACHE = 256;
+struct MapCacheEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool used;
+};
+
+bool encode_bf16(CUtensorMap* m, cuuint32_t rank, const void* ptr, const cuuint64_t* dims, const cuuint64_t* strides,
+                 const cuuint32_t* box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || rank < 1 || rank > 4) return false;
+  MapKey k{};
+  k.ptr = ptr;
+  k.rank = rank;
+  uint64_t h = reinterpret_cast<uintptr_t>(ptr) * 0x9E3779B97F4A7C15ull ^ rank;
+  for (cuuint32_t i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    h = (h ^ dims[i]) * 0x100000001B3ull;
+    h = (h ^ box[i]) * 0x100000001B3ull;
+    if (i + 1 < rank) {
+      k.strides[i] = strides[i];
+      h = (h ^ strides[i]) * 0x100000001B3ull;
+    }
+  }
+  thread_local MapCacheEntry cache[MAP_CACHE];
+  MapCacheEntry& e = cache[(h >> 32) % MAP_CACHE];
+  if (e.used && e.key == k) {
+    *m = e.map;
+    return true;
+  }
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  e.key = k;
+  e.map = *m;
+  e.used = true;
+  return true;
+}
+
 // bf16 [outer, 4096] row-major, boxes of box_rows x 64 (128B swizzle).
 bool map_rows(CUtensorMap* m, const void* ptr, long long rows, int box_rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D_MODEL), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D_MODEL) * 2};
   const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_bf16(m, 2, ptr, dims, strides, box);
 }
 
 // bf16 [rows, 4096] row-major viewed as (64 values, row, 64 k blocks), boxes
 // of 64 x box_rows x kblocks: one box reads kblocks*128 contiguous bytes of
 // each of box_rows rows.
 bool map_rows_kblocks(CUtensorMap* m, const void* ptr, long long rows, int box_rows, int kblocks) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
   const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), D_MODEL / 64};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D_MODEL) * 2, 128};
   const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(kblocks)};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_bf16(m, 3, ptr, dims, strides, box);
 }
 
 // Decode view of the KV cache [B, s_max, n_kv, 128] bf16: dims (d, pos, g, b)
@@ -129,49 +179,35 @@ bool map_rows_kblocks(CUtensorMap* m, const void* ptr, long long rows, int box_r
 // position rows of 8 KV heads (all of them, or one group of the multi-head
 // variant). Positions past s_max read as zero.
 bool map_cache_by_position(CUtensorMap* m, const void* ptr, int B, int s_max, int n_kv, int box_pos) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
   const cuuint64_t row = static_cast<cuuint64_t>(n_kv) * HEAD_DIM * 2;  // bytes of one cache position
   const cuuint64_t dims[4] = {HEAD_DIM, static_cast<cuuint64_t>(s_max), static_cast<cuuint64_t>(n_kv),
                               static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {row, HEAD_DIM * 2, static_cast<cuuint64_t>(s_max) * row};
   const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_pos), N_KV, 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_bf16(m, 4, ptr, dims, strides, box);
 }
 
 // KV cache [B, s_max, n_kv, 128] bf16 as a 4-D tensor (d, g, pos, b); boxes
 // of 64 dims x 1 head x box_pos positions. Positions at or past `rows`
 // (<= s_max) read as zero.
 bool map_cache(CUtensorMap* m, const void* ptr, int B, int s_max, int n_kv, int rows, int box_pos) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc || rows <= 0 || rows > s_max) return false;
+  if (rows <= 0 || rows > s_max) return false;
   const cuuint64_t row = static_cast<cuuint64_t>(n_kv) * HEAD_DIM * 2;
   const cuuint64_t dims[4] = {HEAD_DIM, static_cast<cuuint64_t>(n_kv), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {HEAD_DIM * 2, row, static_cast<cuuint64_t>(s_max) * row};
   const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_pos), 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_bf16(m, 4, ptr, dims, strides, box);
 }
 
 // Rotated queries [B*T, 4096] bf16 as a 4-D tensor (d, head, t, b); boxes of
 // 64 dims x n_rep heads (one KV group) x 128 / n_rep tokens (128 rows). Tokens
 // past T read as zero.
 bool map_q_prefill(CUtensorMap* m, const void* ptr, int B, int T, int n_rep) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
   const cuuint64_t dims[4] = {HEAD_DIM, N_HEADS, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {HEAD_DIM * 2, D_MODEL * 2, static_cast<cuuint64_t>(T) * D_MODEL * 2};
   const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(n_rep), static_cast<cuuint32_t>(128 / n_rep), 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_bf16(m, 4, ptr, dims, strides, box);
 }
 
 int sm_count() {

@@ -136,6 +136,15 @@ __device__ __forceinline__ bool compute_all(bool v) {
   return r != 0;
 }
 
+// OR of `v` over the 256 compute threads, with a barrier.
+__device__ __forceinline__ bool compute_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 3, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r) : "r"(static_cast<uint32_t>(v)) : "memory");
+  return r != 0;
+}
+
 struct Shared {
   uint8_t* ring;     // RING bytes, 1024-aligned
   uint64_t* full;    // [STAGES], count 1
@@ -391,6 +400,9 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
 // then every warp merges one (sequence, query head) of the split sequences.
 // Called by the 256 compute threads of every CTA with `ok` from attn_units
 // (a CTA that gave up still meets, so that no other CTA waits in vain).
+// When no CTA boundary falls inside a sequence (every sequence was finished
+// whole by one CTA: a small batch of short sequences) there is nothing to
+// merge and the grid does not meet.
 // Returns false when any thread of the CTA gave up or the meeting timed out.
 template <int NREP>
 __device__ __forceinline__ bool attn_merge(const DecodeAttnParams& a, const Shared& sh, int* meet, bool ok) {
@@ -403,6 +415,15 @@ __device__ __forceinline__ bool attn_merge(const DecodeAttnParams& a, const Shar
   const long long U = pre[B];
   const long long C = gridDim.x;
   const bool all_ok = compute_all(ok);
+  bool cut = false;  // a CTA boundary inside a sequence: its partials need merging
+  for (long long c = threadIdx.x + 1; c < C; c += COMPUTE_WARPS * 32) {
+    const long long u = range_start(c, U, C);
+    if (u > 0 && u < U) cut = cut || locate(u, pre, B).j != 0;
+  }
+  if (!compute_any(cut)) {
+    if (!all_ok && lane == 0) atomicExch(&flags[0], 1);
+    return all_ok;
+  }
   if (threadIdx.x == 0) {
     atomicAdd(meet, 1);
     flags[3] = wait_counter(meet, static_cast<int>(C)) ? 1 : 0;
