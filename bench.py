@@ -496,12 +496,10 @@ def main():
     torch.cuda.synchronize()
     per_kernel = {k: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs) for j, k in enumerate(kernels)}
 
-    # ---- end to end through the public API with host buffers: pinned x in,
-    # delta out, copies inside the timed region. Two timings: serial (copy
-    # in, step, copy out, one stream) and pipelined as a serving loop runs
-    # it: the copies go on a second stream, step i+1's input is uploaded
-    # while step i runs (one input buffer per replica) and step i's output is
-    # read back while step i+1 runs
+    # ---- end to end with host buffers: pinned x in, delta out, copies inside
+    # the timed region. Two timings: serial through the device entry (torch
+    # copy in, step, torch copy out, one stream) and through the host-buffer
+    # entry
     xh = x0.pin_memory()
     oh = torch.empty_like(x0).pin_memory()
     for i in range(min(a.warmup, 5)):
@@ -521,34 +519,35 @@ def main():
     _barrier(world)
     ems_serial = _max_over_ranks(f0.elapsed_time(f1), world, dev)
     ems = ems_serial
-    pipelined = L == 1 and R >= 2
-    if pipelined:
-        cs = torch.cuda.Stream(device=dev)
-        ev_in = [torch.cuda.Event() for _ in range(a.steps + 1)]
-        ev_done = [torch.cuda.Event() for _ in range(a.steps)]
+    # the host-buffer C-ABI entry (x in, result out in host memory; the
+    # library uploads the next step's input on its copy stream while a step
+    # runs): one call per step, every copy inside the timed region
+    host_entry = L == 1 and not layer
+    if host_entry:
+        stage = G.make_host_stage(w.B, w.T, dev)
+
+        def host_step(i):
+            r = reps[i % R]
+            if decode:
+                G.decode_host(xh, sp, max_start, r["wq"], r["wk"], r["wv"], r["wo"], rope, r["ck"], r["cv"],
+                              out_host=oh, stage=stage, workspace=r["ws"], n_kv_heads=nkv)
+            else:
+                G.block_forward_host(xh, starts[0], r["wq"], r["wk"], r["wv"], r["wo"], rope, r["ck"], r["cv"],
+                                     out_host=oh, stage=stage, workspace=r["ws"], n_kv_heads=nkv)
+        for i in range(min(a.warmup, 5)):
+            host_step(i)
+        G.host_stage_wait(stage)
         _barrier(world)
         torch.cuda.synchronize()
         f0.record(stream)
-        cs.wait_event(f0)
-        with torch.cuda.stream(cs):
-            in_buf(0).copy_(xh, non_blocking=True)
-            ev_in[0].record(cs)
         for i in range(a.steps):
-            stream.wait_event(ev_in[i])
-            step(i)
-            ev_done[i].record(stream)
-            with torch.cuda.stream(cs):
-                if i + 1 < a.steps:   # the next replica's input buffer: its last step (i + 1 - R) is done
-                    in_buf(i + 1).copy_(xh, non_blocking=True)
-                    ev_in[i + 1].record(cs)
-                cs.wait_event(ev_done[i])
-                oh.copy_(out_buf(i), non_blocking=True)
-        ev_in[a.steps].record(cs)
-        stream.wait_event(ev_in[a.steps])
+            host_step(i)
+        G.host_stage_wait(stage)   # the last read-backs are inside the region
         f1.record(stream)
         torch.cuda.synchronize()
         _barrier(world)
         ems = _max_over_ranks(f0.elapsed_time(f1), world, dev)
+        G.release_host_stage(stage)
     for r in reps:
         assert G.device_status(r["ws"]) == 0, "device status set during the end-to-end steps"
     if rank != 0:
@@ -595,7 +594,10 @@ def main():
         "kernels_ms": per_kernel,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": x0.numel() * 2,
                 "d2h_bytes_per_step": x0.numel() * 2,
-                "copies": "second stream, overlapped with the neighbouring steps" if pipelined else "serial",
+                "call": ("the host-buffer C-ABI entry per step (gqa_decode_host / gqa_block_forward_host: "
+                         "uploads and read-backs on the library's copy streams, overlapping the neighbouring "
+                         "steps; joined by gqa_host_stage_wait before the end event)") if host_entry
+                        else "torch copies and the device entry per step, one stream",
                 "serial_value": e2e_serial},
         "gpu_launches": launches,
         "timing": f"device region replays CUDA graphs of {GS} consecutive steps (the same C-ABI call captured, "

@@ -49,6 +49,13 @@ _SIGNATURES = {
                                _vp, _sz, _vp]),
     "gqa_layer_decode": (_i, [_vp, _i, _vp, _i, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp,
                               _vp, _sz, _vp]),
+    "gqa_host_stage_bytes": (_sz, [_i, _i]),
+    "gqa_block_forward_host": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz,
+                                    _vp, _sz, _vp]),
+    "gqa_decode_host": (_i, [_vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _sz, _vp,
+                             _sz, _vp]),
+    "gqa_host_stage_wait": (_i, [_vp, _vp]),
+    "gqa_host_stage_release": (_i, [_vp]),
     "gqa_strerror": (ctypes.c_char_p, [_i]),
     "gqa_last_launch_count": (_i, []),
     "gqa_set_decode_fusion": (_i, [_i]),
@@ -95,25 +102,34 @@ def exported_symbols():
 
 
 def _p(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: ctypes passes it as the void* the signature declares
+    return None if t is None else t.data_ptr()
 
 
-def _s(stream) -> ctypes.c_void_p:
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _s(stream, device=None):
+    """The CUDA stream handle: ``stream`` or, when None, torch's current
+    stream on ``device`` (the raw handle lookup is a few times cheaper than
+    building a Stream object on every call)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None and device is not None and device.index is not None:
+        return _raw_stream(device.index)
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _check(t: torch.Tensor, name: str, dtype, shape=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    if t.dtype != dtype:
-        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_contiguous():
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
         raise ValueError(f"{name} must be contiguous")
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if shape is not None and t.shape != shape:
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
@@ -135,7 +151,7 @@ def rope_table(rows: int, theta: float = 500000.0, scaled: bool = True, factor: 
     """fp32 [rows, 64, 2] table of (cos, sin), built on the device."""
     out = torch.empty(rows, 64, 2, dtype=torch.float32, device=device or "cuda")
     r = lib().gqa_rope_table(_p(out), rows, theta, int(scaled), factor, low_freq_factor,
-                             high_freq_factor, original_context, _s(stream))
+                             high_freq_factor, original_context, _s(stream, out.device))
     if r:
         raise GQAError(r, "gqa_rope_table")
     return out
@@ -143,9 +159,17 @@ def rope_table(rows: int, theta: float = 500000.0, scaled: bool = True, factor: 
 
 def _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, T, n_kv=N_KV_HEADS):
     B = x.shape[0]
+    _check(x, "x", torch.bfloat16, (B, T, D_MODEL))
+    _weight_args(B, wq, wk, wv, wo, rope, cache_k, cache_v, n_kv)
+    if out is None:
+        out = torch.empty_like(x)
+    _check(out, "out", torch.bfloat16, (B, T, D_MODEL))
+    return B, out
+
+
+def _weight_args(B, wq, wk, wv, wo, rope, cache_k, cache_v, n_kv):
     if n_kv not in (N_KV_HEADS, N_HEADS):
         raise ValueError(f"n_kv_heads must be {N_KV_HEADS} or {N_HEADS}, got {n_kv}")
-    _check(x, "x", torch.bfloat16, (B, T, D_MODEL))
     _check(wq, "wq", torch.bfloat16, (N_HEADS * HEAD_DIM, D_MODEL))
     _check(wk, "wk", torch.bfloat16, (n_kv * HEAD_DIM, D_MODEL))
     _check(wv, "wv", torch.bfloat16, (n_kv * HEAD_DIM, D_MODEL))
@@ -157,10 +181,6 @@ def _block_args(x, wq, wk, wv, wo, rope, cache_k, cache_v, out, T, n_kv=N_KV_HEA
     _check(cache_v, "cache_v", torch.bfloat16, cache_k.shape)
     if cache_k.dim() != 4 or cache_k.shape[0] != B or cache_k.shape[2:] != (n_kv, HEAD_DIM):
         raise ValueError(f"cache must be [B, S_max, {n_kv}, 128], got {tuple(cache_k.shape)}")
-    if out is None:
-        out = torch.empty_like(x)
-    _check(out, "out", torch.bfloat16, (B, T, D_MODEL))
-    return B, out
 
 
 def _ws(workspace, B, T, max_keys, device):
@@ -180,12 +200,12 @@ def block_forward(x, start_pos: int, wq, wk, wv, wo, rope, cache_k, cache_v, out
     if n_kv_heads == N_KV_HEADS:
         r = lib().gqa_block_forward(_p(x), B, T, int(start_pos), _p(wq), _p(wk), _p(wv), _p(wo), _p(rope),
                                     rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
-                                    _p(workspace), workspace.numel(), _s(stream))
+                                    _p(workspace), workspace.numel(), _s(stream, x.device))
         where = "gqa_block_forward"
     else:
         r = lib().gqa_block_forward_nkv(_p(x), B, T, int(start_pos), int(n_kv_heads), _p(wq), _p(wk), _p(wv),
                                         _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1],
-                                        _p(out), _p(workspace), workspace.numel(), _s(stream))
+                                        _p(out), _p(workspace), workspace.numel(), _s(stream, x.device))
         where = "gqa_block_forward_nkv"
     if r:
         raise GQAError(r, where)
@@ -199,7 +219,7 @@ def prefill(x, start_pos: int, wq, wk, wv, wo, rope, cache_k, cache_v, out=None,
     workspace = _ws(workspace, B, T, start_pos + T, x.device)
     r = lib().gqa_prefill(_p(x), B, T, int(start_pos), _p(wq), _p(wk), _p(wv), _p(wo), _p(rope),
                           rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
-                          _p(workspace), workspace.numel(), _s(stream))
+                          _p(workspace), workspace.numel(), _s(stream, x.device))
     if r:
         raise GQAError(r, "gqa_prefill")
     return out
@@ -215,12 +235,12 @@ def decode(x, start_pos: torch.Tensor, max_start_pos: int, wq, wk, wv, wo, rope,
     if n_kv_heads == N_KV_HEADS:
         r = lib().gqa_decode(_p(x), B, _p(start_pos), int(max_start_pos), _p(wq), _p(wk), _p(wv), _p(wo),
                              _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
-                             _p(workspace), workspace.numel(), _s(stream))
+                             _p(workspace), workspace.numel(), _s(stream, x.device))
         where = "gqa_decode"
     else:
         r = lib().gqa_decode_nkv(_p(x), B, _p(start_pos), int(max_start_pos), int(n_kv_heads), _p(wq), _p(wk),
                                  _p(wv), _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1],
-                                 _p(out), _p(workspace), workspace.numel(), _s(stream))
+                                 _p(out), _p(workspace), workspace.numel(), _s(stream, x.device))
         where = "gqa_decode_nkv"
     if r:
         raise GQAError(r, where)
@@ -235,7 +255,7 @@ def rms_norm(x, norm_w, eps: float, out=None, stream=None) -> torch.Tensor:
         raise ValueError("x: last dimension must be 4096")
     out = torch.empty_like(x) if out is None else out
     _check(out, "out", torch.bfloat16, tuple(x.shape))
-    r = lib().gqa_rms_norm(_p(x), x.numel() // 4096, _p(norm_w), float(eps), _p(out), _s(stream))
+    r = lib().gqa_rms_norm(_p(x), x.numel() // 4096, _p(norm_w), float(eps), _p(out), _s(stream, x.device))
     if r:
         raise GQAError(r, "gqa_rms_norm")
     return out
@@ -249,7 +269,7 @@ def layer_forward(x, start_pos: int, norm_w, eps: float, wq, wk, wv, wo, rope, c
     workspace = _ws(workspace, B, x.shape[1], int(start_pos) + x.shape[1], x.device)
     r = lib().gqa_layer_forward(_p(x), B, x.shape[1], int(start_pos), _p(norm_w), float(eps), _p(wq), _p(wk),
                                 _p(wv), _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1],
-                                _p(out), _p(workspace), workspace.numel(), _s(stream))
+                                _p(out), _p(workspace), workspace.numel(), _s(stream, x.device))
     if r:
         raise GQAError(r, "gqa_layer_forward")
     return out
@@ -264,7 +284,7 @@ def layer_decode(x, start_pos: torch.Tensor, max_start_pos: int, norm_w, eps: fl
     workspace = _ws(workspace, B, 1, max_start_pos + 1, x.device)
     r = lib().gqa_layer_decode(_p(x), B, _p(start_pos), int(max_start_pos), _p(norm_w), float(eps), _p(wq),
                                _p(wk), _p(wv), _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v),
-                               cache_k.shape[1], _p(out), _p(workspace), workspace.numel(), _s(stream))
+                               cache_k.shape[1], _p(out), _p(workspace), workspace.numel(), _s(stream, x.device))
     if r:
         raise GQAError(r, "gqa_layer_decode")
     return out
@@ -319,7 +339,7 @@ def decode_static(x, start_pos: torch.Tensor, max_start_pos: int, wq, wk, wv, wo
     _check(start_pos, "start_pos", torch.int32, (B,))
     r = lib().gqa_decode_static(_p(x), B, _p(start_pos), int(max_start_pos), _p(wq), _p(wk), _p(wv), _p(wo),
                                 _p(rope), rope.shape[0], _p(cache_k), _p(cache_v), cache_k.shape[1], _p(out),
-                                _s(stream))
+                                _s(stream, x.device))
     if r:
         raise GQAError(r, "gqa_decode_static")
     return out
@@ -332,3 +352,80 @@ def static_device_status(clear: bool = False) -> int:
     if r not in (0, -5):
         raise GQAError(r, "gqa_static_device_status")
     return st.value
+
+
+# ------------------------------------------------------------ host-buffer entries
+
+def make_host_stage(B: int, T: int, device=None) -> torch.Tensor:
+    """Device stage of the host-buffer entries (two input and two output buffers)."""
+    n = int(lib().gqa_host_stage_bytes(B, T))
+    if n == 0:
+        raise ValueError(f"invalid stage request B={B} T={T}")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def host_stage_wait(stage: torch.Tensor, stream=None) -> None:
+    """Order ``stream`` after the read-backs of every call made on ``stage``:
+    their results are in host memory once ``stream`` reaches this point."""
+    r = lib().gqa_host_stage_wait(_p(stage), _s(stream, stage.device))
+    if r:
+        raise GQAError(r, "gqa_host_stage_wait")
+
+
+def release_host_stage(stage: torch.Tensor) -> None:
+    """Free the copy stream and events the library keeps for ``stage``."""
+    r = lib().gqa_host_stage_release(_p(stage))
+    if r:
+        raise GQAError(r, "gqa_host_stage_release")
+
+
+def _host_args(x_host, out_host, T):
+    if not isinstance(x_host, torch.Tensor) or x_host.is_cuda:
+        raise ValueError("x_host must be a CPU tensor")
+    B = x_host.shape[0]
+    if x_host.dtype != torch.bfloat16 or not x_host.is_contiguous() or x_host.shape != (B, T, D_MODEL):
+        raise ValueError(f"x_host must be a contiguous bf16 [B, {T}, {D_MODEL}] tensor")
+    if out_host is None:
+        out_host = torch.empty(x_host.shape, dtype=torch.bfloat16).pin_memory()
+    if out_host.is_cuda or out_host.dtype != torch.bfloat16 or not out_host.is_contiguous() \
+            or out_host.shape != x_host.shape:
+        raise ValueError("out_host must be a contiguous bf16 CPU tensor shaped like x_host")
+    return B, out_host
+
+
+def decode_host(x_host, start_pos: torch.Tensor, max_start_pos: int, wq, wk, wv, wo, rope, cache_k, cache_v,
+                out_host=None, stage=None, workspace=None, stream=None, n_kv_heads: int = N_KV_HEADS) -> torch.Tensor:
+    """``decode`` with x and the result in host memory (pinned for asynchronous
+    copies); out_host holds the result once ``stream`` has reached a later
+    ``host_stage_wait(stage)``."""
+    B, out_host = _host_args(x_host, out_host, 1)
+    _weight_args(B, wq, wk, wv, wo, rope, cache_k, cache_v, n_kv_heads)
+    dev = start_pos.device
+    _check(start_pos, "start_pos", torch.int32, (B,))
+    workspace = _ws(workspace, B, 1, max_start_pos + 1, dev)
+    stage = make_host_stage(B, 1, dev) if stage is None else stage
+    r = lib().gqa_decode_host(x_host.data_ptr(), B, _p(start_pos), int(max_start_pos), int(n_kv_heads), _p(wq),
+                              _p(wk), _p(wv), _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v),
+                              cache_k.shape[1], out_host.data_ptr(), _p(stage), stage.numel(), _p(workspace),
+                              workspace.numel(), _s(stream, dev))
+    if r:
+        raise GQAError(r, "gqa_decode_host")
+    return out_host
+
+
+def block_forward_host(x_host, start_pos: int, wq, wk, wv, wo, rope, cache_k, cache_v, out_host=None, stage=None,
+                       workspace=None, stream=None, n_kv_heads: int = N_KV_HEADS) -> torch.Tensor:
+    """``block_forward`` with x and delta_attn in host memory."""
+    T = x_host.shape[1]
+    B, out_host = _host_args(x_host, out_host, T)
+    _weight_args(B, wq, wk, wv, wo, rope, cache_k, cache_v, n_kv_heads)
+    dev = wq.device
+    workspace = _ws(workspace, B, T, start_pos + T, dev)
+    stage = make_host_stage(B, T, dev) if stage is None else stage
+    r = lib().gqa_block_forward_host(x_host.data_ptr(), B, T, int(start_pos), int(n_kv_heads), _p(wq), _p(wk),
+                                     _p(wv), _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v),
+                                     cache_k.shape[1], out_host.data_ptr(), _p(stage), stage.numel(), _p(workspace),
+                                     workspace.numel(), _s(stream, dev))
+    if r:
+        raise GQAError(r, "gqa_block_forward_host")
+    return out_host

@@ -520,11 +520,12 @@ int gqa_rope_table(float* rope, int rows, double theta, int scaled, double facto
 
 static bool valid_n_kv(int n_kv) { return n_kv == N_KV || n_kv == N_HEADS; }
 
+// dry: validate only (GQA_OK when the call would be launched)
 static int block_call(const gqa_bf16* x, int B, int T, int start_pos, int n_kv, const gqa_bf16* norm_w, float eps,
                       const gqa_bf16* wq, const gqa_bf16* wk,
                       const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
                       gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+                      void* stream, bool dry = false) {
   if (start_pos < 0 || T <= 0 || start_pos > (1 << 30) || !valid_n_kv(n_kv)) return GQA_EINVAL;
   Call c{};
   const int max_keys = start_pos + T;
@@ -550,7 +551,7 @@ static int block_call(const gqa_bf16* x, int B, int T, int start_pos, int n_kv, 
   c.out = out;
   c.ws = static_cast<uint8_t*>(workspace);
   c.stream = static_cast<cudaStream_t>(stream);
-  return run_block(c);
+  return dry ? GQA_OK : run_block(c);
 }
 
 // Arguments of the layer entries beyond the block's.
@@ -610,7 +611,7 @@ static int decode_call(const gqa_bf16* x, int B, const int32_t* start_pos, int m
                        const gqa_bf16* norm_w, float eps, const gqa_bf16* wq, const gqa_bf16* wk,
                        const gqa_bf16* wv, const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
                        gqa_bf16* cache_v, int s_max, gqa_bf16* out, void* workspace, size_t workspace_bytes,
-                       void* stream) {
+                       void* stream, bool dry = false) {
   if (!start_pos || max_start_pos < 0 || max_start_pos > (1 << 30) || !valid_n_kv(n_kv)) return GQA_EINVAL;
   // the attention runs n_kv / 8 head groups of every sequence as units of their own
   const int groups = n_kv / N_KV;
@@ -645,7 +646,7 @@ static int decode_call(const gqa_bf16* x, int B, const int32_t* start_pos, int m
   c.out = out;
   c.ws = static_cast<uint8_t*>(workspace);
   c.stream = static_cast<cudaStream_t>(stream);
-  return run_block(c);
+  return dry ? GQA_OK : run_block(c);
 }
 
 int gqa_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start_pos, const gqa_bf16* wq,
@@ -772,4 +773,177 @@ extern "C" int gqa_static_device_status(int* status, int clear) {
   int r = static_scratch(&scratch);
   if (r != GQA_OK) return r;
   return gqa_device_status(scratch, status, clear);
+}
+
+// ---------------------------------------------------------------------------
+// Host-buffer entries: x and the result in host memory. A caller-provided
+// device stage holds two input and two output buffers; call k uses pair
+// k % 2. Per stage the library keeps an upload and a read-back stream: call
+// k's input is uploaded while call k-1 computes, its block runs on the
+// caller's stream, and its result is read back while call k+1 computes.
+// gqa_host_stage_wait joins the read-backs into the caller's stream.
+// ---------------------------------------------------------------------------
+#include <map>
+
+namespace {
+
+struct HostPipe {
+  int dev = -1;
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaEvent_t uploaded[2] = {nullptr, nullptr};   // on `up`, after pair k's input is in
+  cudaEvent_t computed[2] = {nullptr, nullptr};   // on the caller's stream, after pair k's block
+  cudaEvent_t read_back[2] = {nullptr, nullptr};  // on `down`, after pair k's result is out
+  bool used[2] = {false, false};
+  int next = 0;
+};
+
+std::mutex g_pipe_mu;
+std::map<const void*, HostPipe> g_pipes;
+
+size_t stage_bytes_for(int B, int T) {
+  if (B <= 0 || T <= 0) return 0;
+  const size_t m = static_cast<size_t>(B) * T * D_MODEL * 2;
+  const size_t slot = (m + 255) & ~static_cast<size_t>(255);
+  return 4 * slot;
+}
+
+void release_pipe(HostPipe& p) {
+  for (int i = 0; i < 2; ++i) {
+    for (cudaEvent_t ev : {p.uploaded[i], p.computed[i], p.read_back[i]})
+      if (ev) cudaEventDestroy(ev);
+  }
+  if (p.up) cudaStreamDestroy(p.up);
+  if (p.down) cudaStreamDestroy(p.down);
+}
+
+// The stage's pipe on the current device (created on first use).
+int get_pipe(const void* stage, HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e);
+  auto it = g_pipes.find(stage);
+  if (it != g_pipes.end()) {
+    if (it->second.dev != dev) return GQA_EINVAL;  // a stage belongs to one device
+    *out = &it->second;
+    return GQA_OK;
+  }
+  HostPipe p;
+  p.dev = dev;
+  e = cudaStreamCreateWithFlags(&p.up, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.down, cudaStreamNonBlocking);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+    e = cudaEventCreateWithFlags(&p.uploaded[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.computed[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.read_back[i], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) {
+    release_pipe(p);
+    return fail_cuda(e);
+  }
+  *out = &g_pipes.emplace(stage, p).first->second;
+  return GQA_OK;
+}
+
+// Upload x_host into pair k's input buffer, run(x_dev, out_dev) on `stream`,
+// read out_dev back into out_host.
+template <class Run>
+int host_call(const gqa_bf16* x_host, gqa_bf16* out_host, int B, int T, void* stage, size_t stage_bytes,
+              void* stream, Run run) {
+  // run(x_dev, out_dev, dry): dry validates the block's arguments only
+  if (!x_host || !out_host || !stage) return GQA_EINVAL;
+  const size_t need = stage_bytes_for(B, T);
+  if (need == 0) return GQA_EINVAL;
+  if (!aligned16(stage)) return GQA_EALIGN;
+  if (stage_bytes < need) return GQA_EWORKSPACE;
+  const size_t bytes = static_cast<size_t>(B) * T * D_MODEL * 2;
+  const size_t slot = need / 4;
+  uint8_t* base = static_cast<uint8_t*>(stage);
+  // every argument checked before anything is created or enqueued
+  int r = run(reinterpret_cast<gqa_bf16*>(base), reinterpret_cast<gqa_bf16*>(base + 2 * slot), true);
+  if (r != GQA_OK) return r;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe* p = nullptr;
+  r = get_pipe(stage, &p);
+  if (r != GQA_OK) return r;
+  const int k = p->next;
+  gqa_bf16* x_dev = reinterpret_cast<gqa_bf16*>(base + k * slot);
+  gqa_bf16* out_dev = reinterpret_cast<gqa_bf16*>(base + (2 + k) * slot);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  // pair k was last used two calls ago: its block must be done before the
+  // upload overwrites its input, its read-back before this block writes
+  if (p->used[k]) e = cudaStreamWaitEvent(p->up, p->computed[k], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, p->up);
+  if (e == cudaSuccess) e = cudaEventRecord(p->uploaded[k], p->up);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, p->uploaded[k], 0);
+  if (e == cudaSuccess && p->used[k]) e = cudaStreamWaitEvent(s, p->read_back[k], 0);
+  if (e != cudaSuccess) return fail_cuda(e);
+  r = run(x_dev, out_dev, false);
+  const int launches = t_launches;
+  if (r != GQA_OK) return r;
+  e = cudaEventRecord(p->computed[k], s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(p->down, p->computed[k], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, p->down);
+  if (e == cudaSuccess) e = cudaEventRecord(p->read_back[k], p->down);
+  if (e != cudaSuccess) return fail_cuda(e);
+  p->used[k] = true;
+  p->next = k ^ 1;
+  t_launches = launches;
+  return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t gqa_host_stage_bytes(int B, int T) { return stage_bytes_for(B, T); }
+
+extern "C" int gqa_block_forward_host(const gqa_bf16* x_host, int B, int T, int start_pos, int n_kv_heads,
+                                      const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv, const gqa_bf16* wo,
+                                      const float* rope, int rope_rows, gqa_bf16* cache_k, gqa_bf16* cache_v,
+                                      int s_max, gqa_bf16* out_host, void* stage, size_t stage_bytes,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  return host_call(x_host, out_host, B, T, stage, stage_bytes, stream, [&](gqa_bf16* x, gqa_bf16* out, bool dry) {
+    return block_call(x, B, T, start_pos, n_kv_heads, nullptr, 0.f, wq, wk, wv, wo, rope, rope_rows, cache_k, cache_v,
+                      s_max, out, workspace, workspace_bytes, stream, dry);
+  });
+}
+
+extern "C" int gqa_decode_host(const gqa_bf16* x_host, int B, const int32_t* start_pos, int max_start_pos,
+                               int n_kv_heads, const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv,
+                               const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
+                               gqa_bf16* cache_v, int s_max, gqa_bf16* out_host, void* stage, size_t stage_bytes,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return host_call(x_host, out_host, B, 1, stage, stage_bytes, stream, [&](gqa_bf16* x, gqa_bf16* out, bool dry) {
+    return decode_call(x, B, start_pos, max_start_pos, n_kv_heads, nullptr, 0.f, wq, wk, wv, wo, rope, rope_rows,
+                       cache_k, cache_v, s_max, out, workspace, workspace_bytes, stream, dry);
+  });
+}
+
+extern "C" int gqa_host_stage_wait(void* stage, void* stream) {
+  if (!stage) return GQA_EINVAL;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  auto it = g_pipes.find(stage);
+  if (it == g_pipes.end()) return GQA_OK;  // no call made on it: nothing to wait for
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != it->second.dev) return GQA_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int k = 0; k < 2; ++k) {
+    if (!it->second.used[k]) continue;
+    const cudaError_t e = cudaStreamWaitEvent(s, it->second.read_back[k], 0);
+    if (e != cudaSuccess) return fail_cuda(e);
+  }
+  return GQA_OK;
+}
+
+extern "C" int gqa_host_stage_release(void* stage) {
+  if (!stage) return GQA_EINVAL;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  auto it = g_pipes.find(stage);
+  if (it == g_pipes.end()) return GQA_EINVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != it->second.dev) return GQA_EINVAL;
+  cudaError_t e = cudaStreamSynchronize(it->second.up);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(it->second.down);
+  release_pipe(it->second);
+  g_pipes.erase(it);
+  return e == cudaSuccess ? GQA_OK : fail_cuda(e);
 }

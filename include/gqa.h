@@ -264,6 +264,44 @@ int gqa_decode_static(const gqa_bf16* x, int B, const int32_t* start_pos, int ma
  * gqa_device_status: synchronises, returns GQA_EDEVICE when non-zero). */
 int gqa_static_device_status(int* status, int clear);
 
+/* Host-buffer entries: the block input in host memory and the result
+ * written back to host memory, for a caller whose tokens live on the host
+ * (a serving loop reading requests, a test harness).
+ *   x_host    [B, T, 4096] bf16 in host memory; pinned (page-locked) memory
+ *             lets the copies run asynchronously (pageable memory works, the
+ *             driver then stages the copy). It must stay unchanged until
+ *             `stream` has reached the call.
+ *   out_host  [B, T, 4096] bf16 in host memory: delta_attn
+ *   stage     device buffer of gqa_host_stage_bytes(B, T) bytes, 16-byte
+ *             aligned, owned by the caller and used on one device: two input
+ *             and two output buffers. Call k on a stage uses pair k % 2.
+ * Per stage the library keeps an upload stream and a read-back stream: call
+ * k's input is uploaded while call k-1's block runs, the block runs on
+ * `stream` (after the upload, and after call k-2's read-back released the
+ * pair), and the result is read back while call k+1's block runs. The
+ * results of every call made so far on a stage are in host memory once
+ * `stream` has reached a later gqa_host_stage_wait(stage, stream).
+ * Every other argument, the cache update and the error behaviour as in
+ * gqa_block_forward_nkv / gqa_decode_nkv (all arguments are checked before
+ * anything is enqueued; GQA_EWORKSPACE also when stage_bytes is too small).
+ * Not for stream capture (the copy streams are outside any capture).
+ * gqa_host_stage_release(stage) waits for the stage's copy streams and
+ * frees them and their events; GQA_EINVAL for a stage it does not know. */
+size_t gqa_host_stage_bytes(int B, int T);
+int gqa_block_forward_host(const gqa_bf16* x_host, int B, int T, int start_pos, int n_kv_heads,
+                           const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv,
+                           const gqa_bf16* wo, const float* rope, int rope_rows,
+                           gqa_bf16* cache_k, gqa_bf16* cache_v, int s_max, gqa_bf16* out_host,
+                           void* stage, size_t stage_bytes, void* workspace,
+                           size_t workspace_bytes, void* stream);
+int gqa_decode_host(const gqa_bf16* x_host, int B, const int32_t* start_pos, int max_start_pos,
+                    int n_kv_heads, const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv,
+                    const gqa_bf16* wo, const float* rope, int rope_rows, gqa_bf16* cache_k,
+                    gqa_bf16* cache_v, int s_max, gqa_bf16* out_host, void* stage,
+                    size_t stage_bytes, void* workspace, size_t workspace_bytes, void* stream);
+int gqa_host_stage_wait(void* stage, void* stream);
+int gqa_host_stage_release(void* stage);
+
 #ifdef __cplusplus
 }
 #endif

@@ -162,3 +162,36 @@ def test_kv_head_entries_reject_bad_arguments(lib):
                   (d, [FAKE, 64, FAKE, 1 << 30, 32, FAKE, FAKE, FAKE, FAKE, FAKE, big, FAKE, FAKE, big, FAKE, FAKE,
                        1 << 40, None])):
         assert fn(*a) == -1
+
+
+def test_host_entries_reject_bad_arguments(lib):
+    """The host-buffer entries check their own arguments (host pointers, the
+    stage's size and alignment) and the block's before anything is created
+    or enqueued."""
+    sb = lib.gqa_host_stage_bytes
+    assert sb(0, 1) == 0 and sb(1, 0) == 0
+    assert sb(16, 1) == 4 * 16 * 4096 * 2 and sb(3, 5) % 256 == 0
+    d = lib.gqa_decode_host
+    ok = [FAKE, 4, FAKE, 10, 8, FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, FAKE, 64, FAKE + 4096, FAKE, sb(4, 1),
+          FAKE, 1 << 40, None]
+    for i, v, code in ((0, None, -1),            # no host input
+                       (14, None, -1),           # no host output
+                       (15, None, -1),           # no stage
+                       (15, FAKE + 8, -2),       # stage misaligned
+                       (16, 64, -3),             # stage too small
+                       (4, 16, -1),              # n_kv_heads
+                       (2, None, -1),            # no start positions
+                       (3, 64, -1),              # max_start_pos + 1 > s_max
+                       (18, 16, -3)):            # workspace too small
+        bad = list(ok)
+        bad[i] = v
+        assert d(*bad) == code, (i, v)
+    f = lib.gqa_block_forward_host
+    okf = [FAKE, 1, 8, 0, 32, FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, FAKE, 64, FAKE + 4096, FAKE, sb(1, 8),
+           FAKE, 1 << 40, None]
+    for i, v, code in ((0, None, -1), (16, 100, -3), (3, 60, -1), (4, 9, -1)):
+        bad = list(okf)
+        bad[i] = v
+        assert f(*bad) == code, (i, v)
+    assert lib.gqa_host_stage_release(None) == -1
+    assert lib.gqa_host_stage_wait(None, None) == -1

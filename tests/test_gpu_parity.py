@@ -523,3 +523,48 @@ def test_mha_decode_workload_full(mha_weights):
     for b in range(w.B):
         H.compare_sequence(c, out, b)
     H.check_canaries(c)
+
+
+# ------------------------------------------------------------ host-buffer entries
+
+def test_host_buffer_entries_match_device_entries(weights):
+    """decode_host / block_forward_host (x and the result in host memory,
+    uploads on the library's copy stream, two stage buffers in turn) give the
+    device entries' results bit for bit over consecutive calls."""
+    B, starts, s_max = 4, [3, 40, 77, 120], 128
+    c = H.make_case(B, 1, starts, s_max, weights=weights)
+    d = c.dev
+    ck2, cv2 = d["cache_k0"].clone(), d["cache_v0"].clone()
+    sp = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    rope = H.rope_for(c)
+    stage = G.make_host_stage(B, 1)
+    ws = G.make_workspace(B, 1, max(starts) + 1)
+    g = torch.Generator().manual_seed(7)
+    xs = [I.draw_x(g, B, 1).pin_memory() for _ in range(3)]
+    outs = []
+    for xh in xs:   # three calls: both stage pairs, then the first again
+        outs.append(G.decode_host(xh, sp, max(starts), d["wq"], d["wk"], d["wv"], d["wo"], rope, ck2, cv2,
+                                  stage=stage))
+    G.host_stage_wait(stage)
+    torch.cuda.current_stream().synchronize()
+    for xh, oh in zip(xs, outs):
+        ref = G.decode(xh.cuda(), sp, max(starts), d["wq"], d["wk"], d["wv"], d["wo"], rope, d["cache_k"],
+                       d["cache_v"], workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(oh, ref.cpu())
+    assert torch.equal(ck2, d["cache_k"]) and torch.equal(cv2, d["cache_v"])
+    G.release_host_stage(stage)
+
+    cp = H.make_case(1, 40, [0], 48, weights=weights)
+    dp = cp.dev
+    ck3, cv3 = dp["cache_k0"].clone(), dp["cache_v0"].clone()
+    stage = G.make_host_stage(1, 40)
+    oh = G.block_forward_host(cp.host["x"].pin_memory(), 0, dp["wq"], dp["wk"], dp["wv"], dp["wo"], H.rope_for(cp),
+                              ck3, cv3, stage=stage)
+    G.host_stage_wait(stage)
+    ref = G.block_forward(dp["x"], 0, dp["wq"], dp["wk"], dp["wv"], dp["wo"], H.rope_for(cp), dp["cache_k"],
+                          dp["cache_v"])
+    torch.cuda.synchronize()
+    assert torch.equal(oh, ref.cpu())
+    assert torch.equal(ck3, dp["cache_k"])
+    G.release_host_stage(stage)
