@@ -86,6 +86,7 @@ __device__ __forceinline__ Cursor locate(long long u, const int* pre, int B) {
 }
 
 // Units split over the grid: CTA c takes units [U c / C, U (c + 1) / C).
+// With U >= C every CTA has a unit; with U < C each has at most one.
 // Calls are refused unless (units + 1) x (CTAs + 1) < 2^32, so 32-bit
 // unsigned arithmetic is exact here (a 64-bit division is a long software
 // sequence, and a merge takes one per partial it reads).
@@ -95,6 +96,18 @@ __device__ __forceinline__ int cta_of(long long u, long long U, long long C) {
 }
 __device__ __forceinline__ long long range_start(long long c, long long U, long long C) {
   return static_cast<uint32_t>(U) * static_cast<uint32_t>(c) / static_cast<uint32_t>(C);
+}
+
+// The CTAs that hold units of a sequence (first unit ub, nu units), in
+// order: participant p is cf + p when every CTA has units, else the owner of
+// the sequence's p-th unit (one unit per CTA; the CTAs between own none and
+// write no partial).
+__device__ __forceinline__ int participants(long long ub, int nu, long long U, long long C) {
+  return U >= C ? cta_of(ub + nu - 1, U, C) - cta_of(ub, U, C) + 1 : nu;
+}
+// cf = cta_of(ub): the first participant
+__device__ __forceinline__ int participant(long long ub, int cf, int p, long long U, long long C) {
+  return U >= C ? cf + p : cta_of(ub + p, U, C);
 }
 
 // Units per virtual sequence (NG per sequence) prefix-summed into
@@ -442,17 +455,17 @@ __device__ __forceinline__ bool attn_merge(const DecodeAttnParams& a, const Shar
     const int nu = units_of(pre, b);
     if (nu == 0) continue;
     const long long ub = pre[b];
-    const int cf = cta_of(ub, U, C), cl = cta_of(ub + nu - 1, U, C);
-    if (cf == cl) continue;  // finished by its CTA
+    const int np = participants(ub, nu, U, C), cf = cta_of(ub, U, C);
+    if (np == 1) continue;  // finished by its CTA
     float GM = -INFINITY, GL = 0.f;
     float4 go = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = cf; c0 <= cl; c0 += MERGE_SLOTS) {
+    for (int p0 = 0; p0 < np; p0 += MERGE_SLOTS) {
       float2 mlv[MERGE_SLOTS];
       float4 ov[MERGE_SLOTS];
 #pragma unroll
       for (int k = 0; k < MERGE_SLOTS; ++k) {
-        const int cc = c0 + k;
-        if (cc <= cl) {
+        if (p0 + k < np) {
+          const int cc = participant(ub, cf, p0 + k, U, C);
           const long long sl = 2LL * cc + (range_start(cc, U, C) >= ub ? 0 : 1);
           mlv[k] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + (sl * N_HEADS + h) * 2));
           ov[k] = __ldcg(reinterpret_cast<const float4*>(a.part_o + (sl * N_HEADS + h) * HEAD_DIM + hh4));

@@ -568,3 +568,22 @@ def test_host_buffer_entries_match_device_entries(weights):
     assert torch.equal(oh, ref.cpu())
     assert torch.equal(ck3, dp["cache_k"])
     G.release_host_stage(stage)
+
+
+def test_decode_reused_workspace_across_batch_shapes(weights):
+    """One workspace for a large step (every CTA leaves partials) and then a
+    small one whose few units leave most CTAs empty: the small step's merges
+    read the partials of the CTAs that hold its units only, never the slots
+    the large step left behind."""
+    big = H.make_case(16, 1, list(range(200, 1800, 100)), 1800, weights=weights)
+    ws = G.make_workspace(16, 1, 1800)
+    run_decode(big, ws=ws)
+    for fused in (True, False):
+        small = H.make_case(3, 1, [0, 5, 130], 160, seed=1)
+        prev = G.set_decode_fusion(fused)
+        try:
+            out, _ = run_decode(small, ws=ws)
+        finally:
+            G.set_decode_fusion(prev)
+        for b in range(3):
+            H.compare_sequence(small, out, b)
