@@ -16,8 +16,7 @@ constexpr int N_KV = 8;
 constexpr int HEAD_DIM = 128;
 constexpr int N_REP = N_HEADS / N_KV;          // query heads per KV head
 constexpr int KV_ROW = N_KV * HEAD_DIM;       // elements of one cache position
-constexpr int QKV_ROWS = D_MODEL + 2 * KV_ROW;  // 6144 fused projection outputs
-constexpr int QKV_ROWS_MAX = 3 * D_MODEL;        // the multi-head variant's (32 KV heads)
+constexpr int QKV_ROWS_MAX = 3 * D_MODEL;        // fused Q|K|V outputs at most (32 KV heads)
 constexpr int ROPE_PAIRS = HEAD_DIM / 2;
 
 // Device status codes (mirrors GQA_DEV_* in gqa.h).
@@ -135,17 +134,6 @@ __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uin
 // tile written by TMA with 128B swizzling (tile base 1024-byte aligned).
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
-}
-
-// 16-byte global -> shared copy through L2 (not L1); src_bytes = 0 writes
-// zeros and reads nothing.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-// Arrive on `bar` once every cp.async this thread issued before has landed
-// (the arrival counts toward the barrier's expected count).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
 // ----------------------------------------------------------------- mbarrier
@@ -269,15 +257,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
       :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z) : "memory");
-}
-// Ask L2 for the box of a 2-D tensor map at the given coordinates.
-__device__ __forceinline__ void tma_prefetch_2d(const void* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" :: "l"(map), "r"(x), "r"(y) : "memory");
-}
-// Ask L2 for the box of a 3-D tensor map at the given coordinates.
-__device__ __forceinline__ void tma_prefetch_3d(const void* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" :: "l"(map), "r"(x), "r"(y), "r"(z)
-               : "memory");
 }
 // Ask L2 for the box of a 4-D tensor map at the given coordinates.
 __device__ __forceinline__ void tma_prefetch_4d(const void* map, int x, int y, int z, int w) {
