@@ -5,10 +5,14 @@ built in-tree by ``python -m grouped_query_attention_gemv_gb300.build``).
 It only checks and marshals arguments: every step of the block runs in the
 library's CUDA kernels. PyTorch supplies device memory and streams.
 
-Functions mirror the C entry points: ``block_forward``, ``decode``,
-``prefill``, ``rope_table``, ``workspace_bytes``, ``device_status``,
-``last_launch_count``. If the library has not been built every call raises
-``ImportError``; there is no fallback path.
+Functions mirror the C entry points: ``block_forward`` / ``decode`` /
+``prefill`` (``n_kv_heads`` 8, or 32 for the multi-head variant), the layer
+entries ``layer_forward`` / ``layer_decode`` / ``rms_norm``, the host-buffer
+entries ``block_forward_host`` / ``decode_host`` (with ``make_host_stage``,
+``host_stage_wait``, ``release_host_stage``), ``decode_static``,
+``rope_table``, ``workspace_bytes``, ``device_status``, ``last_launch_count``.
+If the library has not been built every call raises ``ImportError``; there is
+no fallback path.
 """
 from __future__ import annotations
 
@@ -23,7 +27,9 @@ __all__ = [
     "GQAError", "D_MODEL", "N_HEADS", "N_KV_HEADS", "HEAD_DIM", "library_path", "lib",
     "exported_symbols", "workspace_bytes", "make_workspace", "rope_table", "block_forward",
     "decode", "prefill", "device_status", "last_launch_count", "set_profile_events",
-    "set_decode_fusion", "decode_static", "rms_norm", "layer_forward", "layer_decode", "static_device_status", "STATIC_SCRATCH_BYTES",
+    "set_decode_fusion", "decode_static", "rms_norm", "layer_forward", "layer_decode", "static_device_status",
+    "STATIC_SCRATCH_BYTES", "make_host_stage", "host_stage_wait", "release_host_stage", "decode_host",
+    "block_forward_host",
 ]
 
 D_MODEL, N_HEADS, N_KV_HEADS, HEAD_DIM = 4096, 32, 8, 128
