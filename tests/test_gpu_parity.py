@@ -587,3 +587,38 @@ def test_decode_reused_workspace_across_batch_shapes(weights):
             G.set_decode_fusion(prev)
         for b in range(3):
             H.compare_sequence(small, out, b)
+
+
+@pytest.mark.parametrize("kind", ["decode_fused", "decode_three", "prefill"])
+def test_workspace_and_output_guards_untouched(weights, kind):
+    """Bytes past the workspace size the library asks for, and past the
+    output rows, keep their pattern: no kernel writes outside its buffers."""
+    guard = 1 << 16
+    B, T, starts, s_max = (4, 1, [3, 40, 77, 120], 128) if kind != "prefill" else (2, 37, [0, 0], 40)
+    c = H.make_case(B, T, starts, s_max, weights=weights)
+    d = c.dev
+    need = G.workspace_bytes(B, T, max(starts) + T)
+    ws_full = torch.zeros(need + guard, dtype=torch.uint8, device="cuda")
+    ws_full[need:] = 0xA5
+    out_full = torch.full((B * T * 4096 + guard // 2,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = out_full[:B * T * 4096].view(B, T, 4096)
+    ws = ws_full[:need]
+    rope = H.rope_for(c)
+    if kind == "prefill":
+        G.block_forward(d["x"], 0, d["wq"], d["wk"], d["wv"], d["wo"], rope, d["cache_k"], d["cache_v"], out=out,
+                        workspace=ws)
+    else:
+        sp = torch.tensor(starts, dtype=torch.int32, device="cuda")
+        prev = G.set_decode_fusion(kind == "decode_fused")
+        try:
+            G.decode(d["x"], sp, max(starts), d["wq"], d["wk"], d["wv"], d["wo"], rope, d["cache_k"], d["cache_v"],
+                     out=out, workspace=ws)
+        finally:
+            G.set_decode_fusion(prev)
+    torch.cuda.synchronize()
+    assert G.device_status(ws) == 0
+    assert bool((ws_full[need:] == 0xA5).all()), "a write past the workspace"
+    assert bool((out_full[B * T * 4096:] == 7.0).all()), "a write past the output"
+    for b in range(B):
+        H.compare_sequence(c, out, b)
+    H.check_canaries(c)
