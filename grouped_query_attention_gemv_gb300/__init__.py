@@ -28,7 +28,8 @@ __all__ = [
     "exported_symbols", "workspace_bytes", "make_workspace", "rope_table", "block_forward",
     "decode", "prefill", "device_status", "last_launch_count", "set_profile_events",
     "set_decode_fusion", "decode_static", "rms_norm", "layer_forward", "layer_decode", "static_device_status",
-    "STATIC_SCRATCH_BYTES", "make_host_stage", "host_stage_wait", "release_host_stage", "decode_host",
+    "STATIC_SCRATCH_BYTES", "make_host_stage", "default_host_stage", "host_stage_wait", "release_host_stage",
+    "decode_host",
     "block_forward_host",
 ]
 
@@ -370,6 +371,28 @@ def make_host_stage(B: int, T: int, device=None) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
+_default_stages = {}
+
+
+def _default_stage(B: int, T: int, device) -> torch.Tensor:
+    """One stage per (device, B, T), kept for the calls that pass none (the
+    library keeps copy streams per stage: a fresh stage per call would make
+    new ones every time)."""
+    d = torch.device(device)
+    index = d.index if d.index is not None else torch.cuda.current_device()
+    key = (index, B, T)
+    st = _default_stages.get(key)
+    if st is None:
+        st = _default_stages[key] = make_host_stage(B, T, torch.device("cuda", index))
+    return st
+
+
+def default_host_stage(B: int, T: int, device=None) -> torch.Tensor:
+    """The stage the host-buffer calls of this device and shape use when they
+    are given none."""
+    return _default_stage(B, T, device or "cuda")
+
+
 def host_stage_wait(stage: torch.Tensor, stream=None) -> None:
     """Order ``stream`` after the read-backs of every call made on ``stage``:
     their results are in host memory once ``stream`` reaches this point."""
@@ -403,13 +426,14 @@ def decode_host(x_host, start_pos: torch.Tensor, max_start_pos: int, wq, wk, wv,
                 out_host=None, stage=None, workspace=None, stream=None, n_kv_heads: int = N_KV_HEADS) -> torch.Tensor:
     """``decode`` with x and the result in host memory (pinned for asynchronous
     copies); out_host holds the result once ``stream`` has reached a later
-    ``host_stage_wait(stage)``."""
+    ``host_stage_wait(stage)`` (with ``stage=None``: the default stage of this
+    device and shape, ``host_stage_wait(default_host_stage(B, 1, device))``)."""
     B, out_host = _host_args(x_host, out_host, 1)
     _weight_args(B, wq, wk, wv, wo, rope, cache_k, cache_v, n_kv_heads)
     dev = start_pos.device
     _check(start_pos, "start_pos", torch.int32, (B,))
     workspace = _ws(workspace, B, 1, max_start_pos + 1, dev)
-    stage = make_host_stage(B, 1, dev) if stage is None else stage
+    stage = _default_stage(B, 1, dev) if stage is None else stage
     r = lib().gqa_decode_host(x_host.data_ptr(), B, _p(start_pos), int(max_start_pos), int(n_kv_heads), _p(wq),
                               _p(wk), _p(wv), _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v),
                               cache_k.shape[1], out_host.data_ptr(), _p(stage), stage.numel(), _p(workspace),
@@ -427,7 +451,7 @@ def block_forward_host(x_host, start_pos: int, wq, wk, wv, wo, rope, cache_k, ca
     _weight_args(B, wq, wk, wv, wo, rope, cache_k, cache_v, n_kv_heads)
     dev = wq.device
     workspace = _ws(workspace, B, T, start_pos + T, dev)
-    stage = make_host_stage(B, T, dev) if stage is None else stage
+    stage = _default_stage(B, T, dev) if stage is None else stage
     r = lib().gqa_block_forward_host(x_host.data_ptr(), B, T, int(start_pos), int(n_kv_heads), _p(wq), _p(wk),
                                      _p(wv), _p(wo), _p(rope), rope.shape[0], _p(cache_k), _p(cache_v),
                                      cache_k.shape[1], out_host.data_ptr(), _p(stage), stage.numel(), _p(workspace),
