@@ -35,6 +35,13 @@ MUTANTS = {
     "rms_eps_outside_sqrt": ("return x / np.sqrt(ms + eps) * weight", "return x / (np.sqrt(ms) + eps) * weight"),
     "rms_weight_dropped": ("return x / np.sqrt(ms + eps) * weight", "return x / np.sqrt(ms + eps)"),
     "residual_on_normalised_input": ("    return x + delta, ck, cv", "    return rms_norm(x, norm_weight, eps) + delta, ck, cv"),
+    # positions counted from the chunk, not the sequence (a chunked-prefill slip)
+    "rope_position_from_chunk": ("    pos = start_pos + np.arange(T)", "    pos = np.arange(T)"),
+    "keys_not_rotated": ("    k = rope_rotate(k, cos[:, None, :], sin[:, None, :])\n", ""),
+    # heads merged as d * n_heads + h instead of h * d_h + d
+    "head_merge_transposed": ("delta = o.reshape(len(rows), n_heads * head_dim) @ wo.T",
+                              "delta = o.transpose(0, 2, 1).reshape(len(rows), n_heads * head_dim) @ wo.T"),
+    "new_rows_written_at_zero": ("        ck[b, sp[b]:sp[b] + T] = nk", "        ck[b, :T] = nk"),
 }
 
 
