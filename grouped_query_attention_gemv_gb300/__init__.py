@@ -372,6 +372,7 @@ def make_host_stage(B: int, T: int, device=None) -> torch.Tensor:
 
 
 _default_stages = {}
+_MAX_DEFAULT_STAGES = 8
 
 
 def _default_stage(B: int, T: int, device) -> torch.Tensor:
@@ -383,6 +384,13 @@ def _default_stage(B: int, T: int, device) -> torch.Tensor:
     key = (index, B, T)
     st = _default_stages.get(key)
     if st is None:
+        if len(_default_stages) >= _MAX_DEFAULT_STAGES:   # drop the oldest shape's stage
+            old_key = next(iter(_default_stages))
+            with torch.cuda.device(old_key[0]):
+                stage = _default_stages.pop(old_key)
+                r = lib().gqa_host_stage_release(_p(stage))
+                if r not in (0, -1):          # -1: no call ever ran on it
+                    raise GQAError(r, "gqa_host_stage_release")
         st = _default_stages[key] = make_host_stage(B, T, torch.device("cuda", index))
     return st
 
