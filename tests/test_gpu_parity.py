@@ -622,3 +622,21 @@ def test_workspace_and_output_guards_untouched(weights, kind):
     for b in range(B):
         H.compare_sequence(c, out, b)
     H.check_canaries(c)
+
+
+def test_host_buffer_entry_with_the_default_stage(weights):
+    """decode_host without a stage uses the binding's default stage for the
+    device and shape; host_stage_wait on it joins the read-back."""
+    B, starts, s_max = 2, [10, 90], 96
+    c = H.make_case(B, 1, starts, s_max, weights=weights)
+    d = c.dev
+    ck2, cv2 = d["cache_k0"].clone(), d["cache_v0"].clone()
+    sp = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    rope = H.rope_for(c)
+    xh = c.host["x"].pin_memory()
+    oh = G.decode_host(xh, sp, max(starts), d["wq"], d["wk"], d["wv"], d["wo"], rope, ck2, cv2)
+    G.host_stage_wait(G.default_host_stage(B, 1))
+    torch.cuda.current_stream().synchronize()
+    ref = G.decode(d["x"], sp, max(starts), d["wq"], d["wk"], d["wv"], d["wo"], rope, d["cache_k"], d["cache_v"])
+    torch.cuda.synchronize()
+    assert torch.equal(oh, ref.cpu())
