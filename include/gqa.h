@@ -16,16 +16,20 @@
  *   delta = o Wo^T, o features ordered h*128 + d          (head merge + wo)
  *
  * Fixed dimensions (the Llama 3.1 8B catalogue entry): d_model 4096, 32 query
- * heads, 8 KV heads, head_dim 128.
+ * heads, 8 KV heads, head_dim 128. The *_nkv and *_host entries also take 32
+ * KV heads (the multi-head variant).
  *
  * Conventions shared by every entry point
  *   - bf16 tensors are raw 16-bit bfloat16 storage (gqa_bf16); all tensors are
  *     dense row-major with the shapes given; device pointers unless stated.
  *   - Every device pointer must be 16-byte aligned (128-bit loads and TMA).
- *   - The caller owns all memory. The library never allocates, frees or
- *     synchronises: it validates the arguments on the host, then enqueues
- *     kernels on `stream` (a cudaStream_t; NULL = legacy default stream) and
- *     returns. Results are ready when the stream reaches that point.
+ *   - The caller owns all memory. The library never allocates device memory,
+ *     frees it or synchronises: it validates the arguments on the host, then
+ *     enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns. Results are ready when the stream reaches that
+ *     point. The exceptions are named where they occur: gqa_device_status and
+ *     gqa_host_stage_release synchronise; the host-buffer entries create an
+ *     upload and a read-back stream with their events per stage on first use.
  *   - Validation happens before any launch; on a non-zero return nothing was
  *     enqueued (except GQA_ECUDA, which reports a failed launch).
  *   - Conditions only the device can see (a per-sequence start position out of
