@@ -195,24 +195,41 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
-def cpu_baseline(w: I.Workload, budget_s: float = 12.0, one_core: bool = True):
-    """The oracle, as it stands, on a bounded sample: whole sequences of the
-    workload (projections, attention, output) until the budget is spent. With
-    ``one_core`` the same sample also runs in a child process whose BLAS is
-    held to one thread (a shorter budget), reported as ``one_core_value``."""
+def _oracle_inputs(w: I.Workload):
+    """Seeded inputs of the workload for the oracle, in float64: (oracle module,
+    weights, RoPE frequencies, per-sequence (x, cached K, cached V, start)).
+    A workload whose cache would take over 256 MB of host memory keeps the
+    caches of its first sequences only (at their own positions)."""
     from oracle import gqa as O
     gen, wt = I.draw_weights(w.dims, seed=w.seed)
     x = I.draw_x(gen, w.B, w.T)
     starts = w.start_positions().tolist()
-    ck, cv = I.draw_cache(w.B, w.cache_rows(), starts, w.dims, seed=w.seed, device="cpu")
+    kv_row = w.n_kv_heads * 128
+    nseq = w.B
+    while nseq > 1 and nseq * w.cache_rows() * kv_row * 4 > (256 << 20):
+        nseq //= 2
+    ck, cv = I.draw_cache(nseq, w.cache_rows(), starts[:nseq], w.dims, seed=w.seed, device="cpu")
     W = {k: v.to(torch.float64).numpy() for k, v in wt.items()}
     r = I.LLAMA31_ROPE
     freqs = O.rope_frequencies(128, r.theta, r.scaled, r.factor, r.low_freq_factor, r.high_freq_factor,
                                r.original_context)
-    per = []
-    for b in range(w.B):
-        per.append((x[b].to(torch.float64).numpy(), ck[b, :starts[b]].to(torch.float64).numpy(),
-                    cv[b, :starts[b]].to(torch.float64).numpy(), starts[b]))
+    per = [(x[b].to(torch.float64).numpy(), ck[b, :starts[b]].to(torch.float64).numpy(),
+            cv[b, :starts[b]].to(torch.float64).numpy(), starts[b]) for b in range(nseq)]
+    return O, W, freqs, per
+
+
+def cpu_baseline(w: I.Workload, budget_s: float = 12.0, one_core: bool = True):
+    """The oracle, as it stands, on a bounded sample: whole sequences of the
+    workload (projections, attention, output) until the budget is spent. With
+    ``one_core`` the same sample also runs in a child process whose BLAS is
+    held to one thread (a shorter budget), reported as ``one_core_value``.
+    Decode workloads report seq-steps/s, prefill workloads TFLOP/s (the
+    algorithmic FLOPs of the sequences done). For a workload whose cache
+    would not fit the sample's host memory budget (over 256 MB) the sample
+    draws the cache of its first sequences only, at their own positions."""
+    O, W, freqs, per = _oracle_inputs(w)
+    nseq = len(per)
+    kv_row = w.n_kv_heads * 128
     unit_step = _oracle_unit(w, O, W, freqs, per)
     n = 0
     t0 = time.perf_counter()
@@ -223,11 +240,18 @@ def cpu_baseline(w: I.Workload, budget_s: float = 12.0, one_core: bool = True):
         if el > budget_s or n >= 64 * w.B:
             break
     threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
-    what = "layer steps (one sequence through one layer" if w.layers > 1 else "decode steps (whole sequences"
-    out = {"value": n / el / w.layers, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
-           "sample": f"{n} single-sequence {what}: projections, attention over P+1 keys, output projection) of "
-                     f"{w.name}, {el:.1f} s, numpy float64"
-                     + (f"; value = that rate / {w.layers} layers" if w.layers > 1 else "")}
+    if w.T > 1:
+        flops = sum(step_flops(1, w.T, per[i % nseq][3], kv_row)["step"] for i in range(n))
+        out = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} sequences of {w.name} ({w.T} tokens each: projections, causal attention, output "
+                         f"projection), {el:.1f} s, numpy float64"}
+    else:
+        what = "layer steps (one sequence through one layer" if w.layers > 1 else "decode steps (whole sequences"
+        out = {"value": n / el / w.layers, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} single-sequence {what}: projections, attention over P+1 keys, output projection) "
+                         f"of {w.name}, {el:.1f} s, numpy float64"
+                         + (f"; value = that rate / {w.layers} layers" if w.layers > 1 else "")
+                         + (f"; the caches of its first {nseq} sequences" if nseq < w.B else "")}
     if one_core:
         env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
         r = subprocess.run([sys.executable, os.path.abspath(__file__), "--workload", w.name, "--oracle-sample",
@@ -248,12 +272,12 @@ def _oracle_unit(w: I.Workload, O, W, freqs, per):
         g = I.draw_norm_weight(seed=w.seed).to(torch.float64).numpy()
 
         def unit(i):
-            xb, kb, vb, sp = per[i % w.B]
+            xb, kb, vb, sp = per[i % len(per)]
             O.layer_sequence_forward(xb, g, I.NORM_EPS, W["wq"], W["wk"], W["wv"], W["wo"], sp, kb, vb, freqs, 32, 8)
         return unit
 
     def unit(i):
-        xb, kb, vb, sp = per[i % w.B]
+        xb, kb, vb, sp = per[i % len(per)]
         O.sequence_forward(xb, W["wq"], W["wk"], W["wv"], W["wo"], sp, kb, vb, freqs, 32, w.n_kv_heads)
     return unit
 
@@ -261,17 +285,8 @@ def _oracle_unit(w: I.Workload, O, W, freqs, per):
 def run_reference(a, w: I.Workload, rank: int, world: int):
     if rank != 0:
         return
-    from oracle import gqa as O
-    gen, wt = I.draw_weights(w.dims, seed=w.seed)
-    x = I.draw_x(gen, w.B, w.T)
+    O, W, freqs, per = _oracle_inputs(w)
     starts = w.start_positions().tolist()
-    ck, cv = I.draw_cache(w.B, w.cache_rows(), starts, w.dims, seed=w.seed, device="cpu")
-    W = {k: v.to(torch.float64).numpy() for k, v in wt.items()}
-    r = I.LLAMA31_ROPE
-    freqs = O.rope_frequencies(128, r.theta, r.scaled, r.factor, r.low_freq_factor, r.high_freq_factor,
-                               r.original_context)
-    per = [(x[b].to(torch.float64).numpy(), ck[b, :starts[b]].to(torch.float64).numpy(),
-            cv[b, :starts[b]].to(torch.float64).numpy(), starts[b]) for b in range(w.B)]
 
     unit = _oracle_unit(w, O, W, freqs, per)
 
@@ -285,15 +300,21 @@ def run_reference(a, w: I.Workload, rank: int, world: int):
     for i in range(a.steps):
         step(i)
     el = time.perf_counter() - t0
-    val = a.steps / el
+    if w.T > 1:   # the arm's own metric: TFLOP/s of the sequences done
+        kv_row = w.n_kv_heads * 128
+        val = sum(step_flops(1, w.T, per[i % len(per)][3], kv_row)["step"] for i in range(a.steps)) / el / 1e12
+        unit = "TFLOP/s"
+    else:
+        val = a.steps / el
+        unit = "seq-steps/s"
     threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": val, "unit": "seq-steps/s", "n_gpus": world,
+        "impl": "reference", "metric": METRIC, "value": val, "unit": unit, "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * el / a.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w, a, starts), "e2e": {"value": val, "unit": "seq-steps/s", "h2d_bytes_per_step": 0,
+        "config": config_dict(w, a, starts), "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0,
                                              "d2h_bytes_per_step": 0},
-        "cpu_baseline": {"value": val, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": val, "unit": unit, "cores": threads, "kind": "oracle",
                          "sample": f"each step: one sequence of {w.name} through the CPU oracle "
                                    f"(numpy float64, whole sequence, {w.layers} layer(s))"},
     }))
@@ -606,7 +627,7 @@ def main():
     }
     if L > 1:
         line["timing"] += f"; a step chains {L} layer calls (one replica per layer), kernels_ms is one layer's launch"
-    if not a.no_cpu_baseline and world == 1 and decode:
+    if not a.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line))
     if world > 1:
