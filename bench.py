@@ -54,7 +54,7 @@ KERNELS = ("qkv_projection", "decode_attention", "o_projection")
 def args_():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=6000)  # ~0.25 s timed at B=16: several clock samples
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_b16_p1000")
