@@ -66,6 +66,8 @@ def args_():
                     help="block: delta = attention(x); layer: h = x + attention(RMSNorm(x)) (one more kernel)")
     ap.add_argument("--decode-kernels", choices=["fused", "three"], default="fused",
                     help="decode step as one persistent grid (default) or as three kernels")
+    ap.add_argument("--attention-split", choices=["auto", "position", "head"], default="auto",
+                    help="work split of the fused grid's attention (auto: chosen per call by the library)")
     return ap.parse_args()
 
 
@@ -332,6 +334,8 @@ def config_dict(w: I.Workload, a, starts):
                    "streamed back to back within a step")
     if w.T == 1:
         c["decode_kernels"] = a.decode_kernels
+        if a.decode_kernels == "fused":
+            c["attention_split"] = getattr(a, "attention_split", "auto")
     if getattr(a, "entry", "block") != "block":
         c["entry"] = a.entry
     if w.start_pos is not None:
@@ -381,6 +385,7 @@ def main():
     dev = torch.device("cuda", local)
     decode = w.T == 1
     G.set_decode_fusion(a.decode_kernels == "fused")
+    G.set_decode_attention_split(a.attention_split)
 
     starts = w.start_positions().tolist()
     s_max = w.cache_rows()

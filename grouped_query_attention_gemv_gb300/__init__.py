@@ -27,7 +27,7 @@ __all__ = [
     "GQAError", "D_MODEL", "N_HEADS", "N_KV_HEADS", "HEAD_DIM", "library_path", "lib",
     "exported_symbols", "workspace_bytes", "make_workspace", "rope_table", "block_forward",
     "decode", "prefill", "device_status", "last_launch_count", "set_profile_events",
-    "set_decode_fusion", "decode_static", "rms_norm", "layer_forward", "layer_decode", "static_device_status",
+    "set_decode_fusion", "set_decode_attention_split", "decode_static", "rms_norm", "layer_forward", "layer_decode", "static_device_status",
     "STATIC_SCRATCH_BYTES", "make_host_stage", "default_host_stage", "host_stage_wait", "release_host_stage",
     "decode_host",
     "block_forward_host",
@@ -66,6 +66,7 @@ _SIGNATURES = {
     "gqa_strerror": (ctypes.c_char_p, [_i]),
     "gqa_last_launch_count": (_i, []),
     "gqa_set_decode_fusion": (_i, [_i]),
+    "gqa_set_decode_attention_split": (_i, [_i]),
     "gqa_set_profile_events": (_i, [ctypes.POINTER(_vp), _i]),
     "gqa_decode_static": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp]),
     "gqa_static_device_status": (_i, [ctypes.POINTER(_i), _i]),
@@ -315,6 +316,20 @@ def set_decode_fusion(enable: bool) -> bool:
     persistent kernel (True, the default) or as three kernels (False).
     Returns the previous setting."""
     return bool(lib().gqa_set_decode_fusion(1 if enable else 0))
+
+
+_SPLITS = {"auto": 0, "position": 1, "head": 2}
+
+
+def set_decode_attention_split(mode: str) -> str:
+    """How the one-kernel decode step splits its attention on this thread:
+    "auto" (chosen per call, the default), "position" (16-position units over
+    the grid, split sequences merged) or "head" (one (sequence, KV head) pair
+    per CTA where the batch fits, nothing merged). Returns the previous mode."""
+    if mode not in _SPLITS:
+        raise ValueError(f"split must be one of {sorted(_SPLITS)}, not {mode!r}")
+    prev = lib().gqa_set_decode_attention_split(_SPLITS[mode])
+    return {v: k for k, v in _SPLITS.items()}[prev]
 
 
 _prof_keep = None

@@ -17,6 +17,7 @@ thread_local char t_msg[256];
 thread_local void* const* t_prof_events = nullptr;
 thread_local int t_prof_count = 0;
 thread_local int t_fused = 1;
+thread_local int t_attn_split = 0;  // fused decode attention: 0 chosen per call, 1 position-major, 2 head-major
 
 thread_local int t_prof_base = 0;  // 1 while a layer call's norm kernel occupies events[0..1]
 void prof_mark(int i, cudaStream_t s) {
@@ -410,6 +411,21 @@ bool row_maps(const gqa_bf16* const* w, const RowPlan& plan, const void* x, int 
   return np > 0 && map_rows_kblocks(&m->x, x, M, np, 4);
 }
 
+// Work split of the fused grid's attention for one call. Head-major (one
+// (sequence, KV head) pair per CTA) streams each head of a sequence on one
+// SM, at about 50 GB/s per SM (measured with 128 SMs streaming at B = 16,
+// P = 1000); position-major units spread the batch over every SM (about
+// 6.8 TB/s) but pay a grid meeting and a merge round, about 5 us at B = 16,
+// when sequences are split between CTAs. Head-major wins while one head's
+// stream is shorter than the whole batch's stream plus that overhead: small
+// batches of short contexts.
+bool head_major_pays(int B, int max_keys, int ctas) {
+  if (B * N_KV > ctas) return false;
+  const double item_us = max_keys * 512.0 / 5.0e4;                 // 512 B of K and V per position and head
+  const double split_us = static_cast<double>(B) * max_keys * 4096.0 / 6.8e6 + 5.0;
+  return item_us < split_us;
+}
+
 // The whole decode step as one persistent grid (B <= FUSED_MAX_B). Returns
 // GQA_EINVAL without launching anything when this GPU cannot run it (too few
 // SMs for the row split); the caller then takes the three-kernel path.
@@ -426,10 +442,20 @@ int run_decode_fused(const Call& c) {
   const gqa_bf16* wqkv[3] = {c.wq, c.wk, c.wv};
   const gqa_bf16* wo[1] = {c.wo};
   const int np = decode_fused_np(a.pq.M);
+  a.head_major = t_attn_split == 2 ? (c.B * N_KV <= a.ctas)
+                 : t_attn_split == 1 ? 0
+                                     : head_major_pays(c.B, c.max_keys, a.ctas);
   if (!row_maps(wqkv, a.qkv_plan, a.pq.x, a.pq.M, np, &a.qkv_maps) ||
       !row_maps(wo, a.o_plan, a.po.x, a.po.M, np, &a.o_maps) ||
       !decode_cache_maps(c, &a.cache))
     return fail_cuda(cudaErrorInvalidValue);
+  if (a.head_major) {
+    if (!map_cache(&a.cache_hm.k, c.cache_k, c.B, c.s_max, c.n_kv, c.s_max, DECODE_ITEM_POS) ||
+        !map_cache(&a.cache_hm.v, c.cache_v, c.B, c.s_max, c.n_kv, c.s_max, DECODE_ITEM_POS))
+      return fail_cuda(cudaErrorInvalidValue);
+  } else {
+    a.cache_hm = a.cache;  // unused
+  }
   a.at = decode_attn_params(c);
   if (a.at.ctas != a.ctas || attn_decode_slots(a.ctas) > c.L.att_slots) return fail_cuda(cudaErrorInvalidConfiguration);
   a.counters = reinterpret_cast<int*>(c.ws + c.L.status + COUNTERS_OFFSET);
@@ -697,6 +723,13 @@ int gqa_last_launch_count(void) { return t_launches; }
 int gqa_set_decode_fusion(int enable) {
   const int prev = t_fused;
   t_fused = enable ? 1 : 0;
+  return prev;
+}
+
+int gqa_set_decode_attention_split(int mode) {
+  if (mode < 0 || mode > 2) return -1;
+  const int prev = t_attn_split;
+  t_attn_split = mode;
   return prev;
 }
 

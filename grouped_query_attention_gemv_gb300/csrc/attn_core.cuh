@@ -60,6 +60,8 @@ constexpr int STAGE_OUT_BYTES = COMPUTE_WARPS * N_REP * HEAD_DIM * 4;  // per-wa
 constexpr float SCALE_LOG2 = 0.08838834764831845f * 1.4426950408889634f;
 constexpr int MERGE_SLOTS = 16;               // slots whose loads are in flight together in a merge
 constexpr int PRE_GATE_UNITS = STAGES;        // units requested before the gate (at most STAGES)
+constexpr int ITEM_POS = DECODE_ITEM_POS;      // positions per stage of the head-major phase (16 per warp)
+static_assert(ITEM_POS == COMPUTE_WARPS * UNIT, "a head-major stage gives every compute warp 16 keys");
 
 struct Cursor {
   int b, j;  // virtual sequence (sequence b / NG, head group b % NG), unit within it
@@ -167,23 +169,76 @@ struct Shared {
   float* stage_out;  // STAGE_OUT_BYTES
 };
 
-// Ask L2 for this CTA's units [u0 + first, u0 + first + count). One thread.
-template <int NG>
-__device__ __forceinline__ void prefetch_units(const CUtensorMap* mk, const CUtensorMap* mv, const DecodeAttnParams& a,
-                                               const int* pre, int first, int count) {
-  const int VB = a.B * NG;
-  const long long U = pre[VB], C = gridDim.x;
-  const long long u0 = range_start(blockIdx.x, U, C), u1 = range_start(blockIdx.x + 1, U, C);
-  const long long from = u0 + first, to = min(u1, u0 + first + count);
-  if (from >= to) return;
-  Cursor cur = locate(from, pre, VB);
-  for (long long u = from; u < to; ++u) {
-    const int pos = cur.j * UNIT, h0 = (cur.b % NG) * N_KV, sb = cur.b / NG;
-    tma_prefetch_4d(mk, 0, pos, h0, sb);
-    tma_prefetch_4d(mk, 64, pos, h0, sb);
-    tma_prefetch_4d(mv, 0, pos, h0, sb);
-    tma_prefetch_4d(mv, 64, pos, h0, sb);
-    advance(cur, pre, VB);
+// One warp's 16 keys of one KV head against its query heads (NREP real,
+// padded to 8 on the N side of m16n8k16): S^T = K Q^T, an online-softmax
+// update of the running (max, sum) per query head (base 2, scale folded in),
+// and O^T += V^T P^T with P^T moved into B-operand layout by movmatrix.
+// kt / vt: shared addresses of the keys' K and V rows (dims 0-63; dims 64-127
+// one box further, BOX_BYTES), 128-byte swizzled rows; key0: position of the
+// first key, L: keys of the sequence (keys >= L are masked). At least one of
+// the 16 keys must be below L. qb: Q^T as B fragments; m_run, l_run: running
+// max and sum of query heads 2t, 2t+1 (t = lane % 4); oacc: O^T tiles
+// (dim 16d + lane/4 (+8), heads 2t, 2t+1).
+template <int NREP>
+__device__ __forceinline__ void block16(uint32_t kt, uint32_t vt, int key0, int L, const uint32_t (&qb)[8][2],
+                                        float (&m_run)[2], float (&l_run)[2], float (&oacc)[8][4]) {
+  const int lane = threadIdx.x & 31;
+  const int gr = lane >> 2, t = lane & 3;
+  float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(kt + (ks >> 2) * BOX_BYTES + sw128(lane & 15, 2 * (ks & 3) + (lane >> 4)), a0, a1, a2, a3);
+    mma16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+  }
+  // sc: (key gr, heads 2t, 2t+1), (key gr + 8, heads 2t, 2t+1)
+  const bool v0 = key0 + gr < L, v1 = key0 + gr + 8 < L;
+  sc[0] = v0 ? sc[0] * SCALE_LOG2 : -INFINITY;
+  sc[1] = v0 ? sc[1] * SCALE_LOG2 : -INFINITY;
+  sc[2] = v1 ? sc[2] * SCALE_LOG2 : -INFINITY;
+  sc[3] = v1 ? sc[3] * SCALE_LOG2 : -INFINITY;
+  float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+  }
+  const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);  // finite: key0 < L
+  const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
+  const float p0 = exp2f(sc[0] - mn0), p1 = exp2f(sc[1] - mn1);
+  const float p2 = exp2f(sc[2] - mn0), p3 = exp2f(sc[3] - mn1);
+  float ps0 = p0 + p2, ps1 = p1 + p3;
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    ps0 += __shfl_xor_sync(0xffffffffu, ps0, o);
+    ps1 += __shfl_xor_sync(0xffffffffu, ps1, o);
+  }
+  l_run[0] = l_run[0] * al0 + ps0;
+  l_run[1] = l_run[1] * al1 + ps1;
+  m_run[0] = mn0;
+  m_run[1] = mn1;
+#pragma unroll
+  for (int d = 0; d < 8; ++d) {
+    oacc[d][0] *= al0;
+    oacc[d][1] *= al1;
+    oacc[d][2] *= al0;
+    oacc[d][3] *= al1;
+  }
+  // P^T as the B operand: (head gr, keys 2t, 2t+1) and (head gr, keys 2t+8, 2t+9)
+  const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
+  const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
+  uint32_t mask_a = 0xffffffffu, mask_b = 0xffffffffu;
+  if (key0 + UNIT > L) {  // value rows past the sequence may hold anything
+    const int ka = key0 + 2 * t, kb = ka + 8;
+    mask_a = (ka < L ? 0x0000ffffu : 0u) | (ka + 1 < L ? 0xffff0000u : 0u);
+    mask_b = (kb < L ? 0x0000ffffu : 0u) | (kb + 1 < L ? 0xffff0000u : 0u);
+  }
+  const int vr = (lane & 7) + ((lane >> 4) << 3);  // key row of this lane's ldmatrix address
+#pragma unroll
+  for (int d = 0; d < 8; ++d) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4_t(vt + (d >> 2) * BOX_BYTES + sw128(vr, 2 * (d & 3) + ((lane >> 3) & 1)), a0, a1, a2, a3);
+    mma16816(oacc[d], a0 & mask_a, a1 & mask_a, a2 & mask_b, a3 & mask_b, pb0, pb1);
   }
 }
 
@@ -286,64 +341,7 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
       }
       // this warp's head inside the four boxes: rows g*16 + r (r = key within the unit)
       const uint32_t kt = smem_u32(sh.ring + s * UNIT_BYTES) + g * HEAD_BYTES;
-      const uint32_t vt = kt + 2 * BOX_BYTES;
-      const int key0 = cur.j * UNIT;
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(kt + (ks >> 2) * BOX_BYTES + sw128(lane & 15, 2 * (ks & 3) + (lane >> 4)), a0, a1, a2, a3);
-        mma16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-      }
-      // sc: (key gr, heads 2t, 2t+1), (key gr + 8, heads 2t, 2t+1)
-      const bool v0 = key0 + gr < L, v1 = key0 + gr + 8 < L;
-      sc[0] = v0 ? sc[0] * SCALE_LOG2 : -INFINITY;
-      sc[1] = v0 ? sc[1] * SCALE_LOG2 : -INFINITY;
-      sc[2] = v1 ? sc[2] * SCALE_LOG2 : -INFINITY;
-      sc[3] = v1 ? sc[3] * SCALE_LOG2 : -INFINITY;
-      float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-      }
-      const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);  // finite: key0 < L
-      const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
-      const float p0 = exp2f(sc[0] - mn0), p1 = exp2f(sc[1] - mn1);
-      const float p2 = exp2f(sc[2] - mn0), p3 = exp2f(sc[3] - mn1);
-      float ps0 = p0 + p2, ps1 = p1 + p3;
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        ps0 += __shfl_xor_sync(0xffffffffu, ps0, o);
-        ps1 += __shfl_xor_sync(0xffffffffu, ps1, o);
-      }
-      l_run[0] = l_run[0] * al0 + ps0;
-      l_run[1] = l_run[1] * al1 + ps1;
-      m_run[0] = mn0;
-      m_run[1] = mn1;
-#pragma unroll
-      for (int d = 0; d < 8; ++d) {
-        oacc[d][0] *= al0;
-        oacc[d][1] *= al1;
-        oacc[d][2] *= al0;
-        oacc[d][3] *= al1;
-      }
-      // P^T as the B operand: (head gr, keys 2t, 2t+1) and (head gr, keys 2t+8, 2t+9)
-      const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
-      const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
-      uint32_t mask_a = 0xffffffffu, mask_b = 0xffffffffu;
-      if (key0 + UNIT > L) {  // value rows past the sequence may hold anything
-        const int ka = key0 + 2 * t, kb = ka + 8;
-        mask_a = (ka < L ? 0x0000ffffu : 0u) | (ka + 1 < L ? 0xffff0000u : 0u);
-        mask_b = (kb < L ? 0x0000ffffu : 0u) | (kb + 1 < L ? 0xffff0000u : 0u);
-      }
-      const int vr = (lane & 7) + ((lane >> 4) << 3);  // key row of this lane's ldmatrix address
-#pragma unroll
-      for (int d = 0; d < 8; ++d) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(vt + (d >> 2) * BOX_BYTES + sw128(vr, 2 * (d & 3) + ((lane >> 3) & 1)), a0, a1, a2, a3);
-        mma16816(oacc[d], a0 & mask_a, a1 & mask_a, a2 & mask_b, a3 & mask_b, pb0, pb1);
-      }
+      block16<NREP>(kt, kt + 2 * BOX_BYTES, cur.j * UNIT, L, qb, m_run, l_run, oacc);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
       ++seg_units;
@@ -404,6 +402,148 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
   }
   // its outputs and partials are out
   fence_proxy_async_global();  // a later phase of the same grid reads o by TMA
+  __threadfence();
+  return ok;
+}
+
+// Head-major decode attention, for a batch whose (sequence, KV head) pairs
+// fit the grid one per CTA: CTA c < 8B takes item (b = c / 8, g = c % 8), all
+// cache rows 0..P_b of KV head g of sequence b, so no sequence is split
+// between CTAs and nothing is merged across them. The producer lane streams
+// stages of ITEM_POS positions (boxes of 64 dims x 1 head x 128 positions
+// over a (dim, head, position, sequence) view, K and V in two halves each,
+// 64 KB per stage); compute warp w takes keys 16w..16w+15 of every stage,
+// all against the pair's 4 query heads (the same 16-row tile shape as a
+// position-major unit, so block16 serves both). At the end the 8 warps'
+// (max, sum, o) states are combined in shared memory by the log-sum-exp rule
+// in warp order and o[b, heads 4g..4g+3] written as bf16. The stages that do
+// not hold position P_b (the row the projection writes) are requested before
+// `gate_lane`. Roles, gates and the return value as in attn_units; the
+// standalone kernel does not use this phase (its queries are ready at launch
+// and its batches are larger).
+template <class GateLane, class GateWarp>
+__device__ __forceinline__ bool attn_items(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeAttnParams& a,
+                                           const Shared& sh, GateLane gate_lane, GateWarp gate_warp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x;
+  if (item >= a.B * N_KV) return true;
+  const int b = item / N_KV, g = item % N_KV;
+  const int P = a.sp.get(b);
+  if (!a.sp.ok(P)) {
+    if (g == 0 && threadIdx.x == 0) report(a.status, DEV_BAD_POSITION);
+    return true;
+  }
+  const int L = P + 1;
+  const int n = (L + ITEM_POS - 1) / ITEM_POS;
+  int* flags = sh.flags;
+
+  if (warp == COMPUTE_WARPS) {
+    if (lane != 0) return true;
+    tma_prefetch_desc(&mk);
+    tma_prefetch_desc(&mv);
+    auto issue = [&](int i) {
+      const int s = i % STAGES;
+      const uint32_t dst = smem_u32(sh.ring + s * UNIT_BYTES);
+      const uint32_t fb = smem_u32(&sh.full[s]);
+      const int pos = i * ITEM_POS;
+      mbar_expect_tx(fb, UNIT_BYTES);
+      tma_load_4d(dst, &mk, fb, 0, g, pos, b);
+      tma_load_4d(dst + BOX_BYTES, &mk, fb, 64, g, pos, b);
+      tma_load_4d(dst + 2 * BOX_BYTES, &mv, fb, 0, g, pos, b);
+      tma_load_4d(dst + 3 * BOX_BYTES, &mv, fb, 64, g, pos, b);
+    };
+    int i = 0;
+    while (i + 1 < n && i < PRE_GATE_UNITS) issue(i++);  // stages before the one holding row P
+    bool ok = gate_lane();
+    for (; ok && i < n; ++i) {
+      if (i >= STAGES && !mbar_wait(smem_u32(&sh.empty[i % STAGES]), ((i / STAGES) & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      issue(i);
+    }
+    if (!ok) atomicExch(&flags[0], 1);
+    flags[2] = i;
+    return true;
+  }
+  if (warp > COMPUTE_WARPS) return true;
+
+  const int gr = lane >> 2, t = lane & 3;
+  bool ok = compute_all(gate_warp());
+  uint32_t qb[8][2];
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float oacc[8][4];
+#pragma unroll
+  for (int d = 0; d < 8; ++d) oacc[d][0] = oacc[d][1] = oacc[d][2] = oacc[d][3] = 0.f;
+  if (ok) {
+    // query heads 4g + gr (gr < 4; rows 4-7 of the N tile are padding)
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(
+        a.q + static_cast<size_t>(b) * D_MODEL + static_cast<size_t>(g * N_REP + (gr % N_REP)) * HEAD_DIM);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      qb[s][0] = gr < N_REP ? q32[s * 8 + t] : 0u;
+      qb[s][1] = gr < N_REP ? q32[s * 8 + 4 + t] : 0u;
+    }
+    for (int i = 0; i < n; ++i) {
+      const int s = i % STAGES;
+      const bool landed = mbar_wait(smem_u32(&sh.full[s]), (i / STAGES) & 1);
+      if (!__all_sync(0xffffffffu, landed)) {
+        if (lane == 0) atomicExch(&flags[0], 1);
+        ok = false;
+        break;
+      }
+      const int key0 = i * ITEM_POS + warp * UNIT;
+      if (key0 < L) {  // warp-uniform: a warp whose keys all lie past the sequence skips the stage
+        const uint32_t kt = smem_u32(sh.ring + s * UNIT_BYTES) + warp * HEAD_BYTES;
+        block16<N_REP>(kt, kt + 2 * BOX_BYTES, key0, L, qb, m_run, l_run, oacc);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
+    }
+  }
+  ok = compute_all(ok);
+  if (ok) {
+    // stage the warp's unnormalised o [4 heads][128] and (max, sum) per head;
+    // every stage is consumed, so the ring's first bytes hold the (max, sum)
+    float* so = sh.stage_out + warp * N_REP * HEAD_DIM;
+    float* ml = reinterpret_cast<float*>(sh.ring);  // [8 warps][4 heads][2]
+    if (t < 2) {
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        float* o0 = so + 2 * t * HEAD_DIM + 16 * d + gr;
+        o0[0] = oacc[d][0];
+        o0[HEAD_DIM] = oacc[d][1];
+        o0[8] = oacc[d][2];
+        o0[HEAD_DIM + 8] = oacc[d][3];
+      }
+      if (gr == 0) {
+        ml[(warp * N_REP + 2 * t) * 2] = m_run[0];
+        ml[(warp * N_REP + 2 * t) * 2 + 1] = l_run[0];
+        ml[(warp * N_REP + 2 * t + 1) * 2] = m_run[1];
+        ml[(warp * N_REP + 2 * t + 1) * 2 + 1] = l_run[1];
+      }
+    }
+    asm volatile("bar.sync 3, 256;" ::: "memory");
+    // thread -> query head hh, dims d2, d2 + 1; warp 0 always holds key 0, so M is finite
+    const int hh = threadIdx.x >> 6, d2 = (threadIdx.x & 63) * 2;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < COMPUTE_WARPS; ++w) M = fmaxf(M, ml[(w * N_REP + hh) * 2]);
+    float den = 0.f, o0 = 0.f, o1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < COMPUTE_WARPS; ++w) {
+      const float f = exp2f(ml[(w * N_REP + hh) * 2] - M);  // 0 for a warp without keys (max -inf)
+      den += f * ml[(w * N_REP + hh) * 2 + 1];
+      const float2 v = *reinterpret_cast<const float2*>(sh.stage_out + (w * N_REP + hh) * HEAD_DIM + d2);
+      o0 += f * v.x;
+      o1 += f * v.y;
+    }
+    const float inv = 1.f / den;
+    *reinterpret_cast<uint32_t*>(a.o + static_cast<size_t>(b) * D_MODEL + static_cast<size_t>(g * N_REP + hh) * HEAD_DIM +
+                                 d2) = pack_bf16(o0 * inv, o1 * inv);
+  }
+  // its output is out (a later phase of the same grid reads o by TMA)
+  fence_proxy_async_global();
   __threadfence();
   return ok;
 }

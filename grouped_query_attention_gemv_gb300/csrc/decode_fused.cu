@@ -11,11 +11,20 @@
 //   * both projections are row-owner phases (proj_rows.cuh): a CTA finishes
 //     its rows without waiting on any other CTA;
 //   * phase B needs the rotated queries and the new K/V rows: a CTA leaving
-//     phase A at once requests its first KV units (all but a sequence's last
-//     one) and waits until every CTA has published its phase A rows;
+//     phase A at once requests its first KV stages (all but the one holding a
+//     sequence's new row) and waits until every CTA has published its phase
+//     A rows;
+//   * phase B runs one of two work splits (attn_core.cuh): position-major
+//     units spread evenly over the grid, whose CTAs meet once and merge the
+//     partials of sequences split between them; or, for a small batch of
+//     short contexts, one (sequence, KV head) pair per CTA, with nothing to
+//     merge across CTAs (the host picks; see the launch arguments);
 //   * phase C needs every sequence's attention output: a CTA leaving phase B
-//     (whose CTAs meet once before their merges) at once requests its first
-//     W_O stages and waits until every CTA has published its outputs.
+//     at once requests its first W_O stages and waits until every CTA has
+//     published its outputs.
+// Each phase keeps at most a few weight stages in flight per SM: deeper
+// queues do not raise the stream's rate, and every counter poll and grid
+// hand-over waits behind the bytes an SM has in flight.
 // Waits are bounded (DEV_WAIT_TIMEOUT in the status word, then a clean exit).
 // The last CTA out resets the counters, so the workspace is ready for the
 // next call.
@@ -57,14 +66,10 @@ namespace {
 // attention); 9 loads the projections' token rows
 constexpr int THREADS = (rowsk::WARPS + 2) * 32;
 static_assert(attnk::COMPUTE_WARPS == rowsk::WARPS, "phases share the compute warps");
-// KV units per CTA that phase A asks L2 for (beyond the ones phase B loads
-// before its gate): 152 x 4 x 64 KB = 39 MB at most, so that a long context
-// does not flush L2
-constexpr int KV_PREFETCH_UNITS = 4;
-
 struct FusedMaps {
   RowMaps qkv, o;
-  DecodeCacheMaps cache;
+  DecodeCacheMaps cache;     // position-major view (units of 16 positions x 8 heads)
+  DecodeCacheMaps cache_hm;  // head-major view (stages of 128 positions of one head)
 };
 
 struct FusedParams {
@@ -73,14 +78,17 @@ struct FusedParams {
   DecodeAttnParams at;
   int* counters;   // [0] CTAs whose Q|K|V rows are published, [1] CTAs whose attention outputs are published,
                    // [2] CTAs done, [3] the attention's meeting before its merges
+  int head_major;  // phase B: one (sequence, KV head) pair per CTA (1) or position-major units (0)
 };
 
 // Phase A streams its weights from HBM as soon as the grid starts: the
 // default (short) token ring. Phase C requests its first weight stages while
-// the grid merges the attention outputs; its tokens, the attention output,
-// only become ready at the gate: a deep token ring (128 KB at 16 tokens).
+// the grid finishes the attention; its tokens, the attention output, only
+// become ready at the gate: a deep token ring (128 KB at 16 tokens).
 // (Asking L2 for the rest of W_O at the same time measured 1.5 us slower per
 // step at B = 16: the requests queue ahead of the merge and the gate.)
+// Both keep 4 weight stages in flight per SM (about 13 MB over the grid,
+// 2 us of HBM time).
 template <int NP>
 using CfgA = rowsk::Cfg<NP>;
 template <int NP>
@@ -153,14 +161,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   int* const cnt = fp.counters;
 
   // ---------------- phase A: Q|K|V projection, RoPE, cache append
-  // once its weight stream is requested, the CTA asks L2 for its first KV
-  // stages after the ones phase B loads before its gate: HBM would otherwise
-  // idle through this phase's epilogue and the grid wait
   rowsk::rows_phase<CfgA<NP>, true>(
-      m.qkv, fp.pq, fp.qkv_plan, sha, []() { return true; }, []() { return true; },
-      [&fp, &m, pre]() {
-        attnk::prefetch_units<1>(&m.cache.k, &m.cache.v, fp.at, pre, attnk::PRE_GATE_UNITS, KV_PREFETCH_UNITS);
-      },
+      m.qkv, fp.pq, fp.qkv_plan, sha, []() { return true; }, []() { return true; }, []() {},
       [cnt]() { signal_counter(&cnt[0], 1); }, a_started);
   fence_proxy_async_smem();  // the ring's generic reads and writes precede phase B's TMA writes into it
   __syncthreads();
@@ -171,22 +173,23 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
                           reinterpret_cast<float*>(smem + attnk::RING)};
   bool units_ok = true;
   if (!aborted) {
-    units_ok = attnk::attn_units<N_REP>(
-        m.cache.k, m.cache.v, fp.at, shb,
-        // one poller per CTA: the producer lane waits on the grid counter and
-        // hands the outcome to the compute warps through shared memory
-        [cnt, grid, flags_b]() {
-          const bool ok = wait_counter(&cnt[0], grid);
-          fence_proxy_async_global();  // the new K/V rows were written by plain stores
-          st_release_cta(&flags_b[1], ok ? 1 : 2);
-          return ok;
-        },
-        [flags_b]() {
-          int v = 0;
-          if ((threadIdx.x & 31) == 0) v = wait_flag_cta(&flags_b[1]);
-          return __shfl_sync(0xffffffffu, v, 0) == 1;
-        },
-        []() {});
+    // one poller per CTA: the producer lane waits on the grid counter and
+    // hands the outcome to the compute warps through shared memory
+    auto gate_lane = [cnt, grid, flags_b]() {
+      const bool ok = wait_counter(&cnt[0], grid);
+      fence_proxy_async_global();  // the new K/V rows were written by plain stores
+      st_release_cta(&flags_b[1], ok ? 1 : 2);
+      return ok;
+    };
+    auto gate_warp = [flags_b]() {
+      int v = 0;
+      if ((threadIdx.x & 31) == 0) v = wait_flag_cta(&flags_b[1]);
+      return __shfl_sync(0xffffffffu, v, 0) == 1;
+    };
+    if (fp.head_major)
+      units_ok = attnk::attn_items(m.cache_hm.k, m.cache_hm.v, fp.at, shb, gate_lane, gate_warp);
+    else
+      units_ok = attnk::attn_units<N_REP>(m.cache.k, m.cache.v, fp.at, shb, gate_lane, gate_warp, []() {});
     fence_proxy_async_smem();  // ldmatrix reads of the ring precede phase C's TMA writes into it
   }
   __syncthreads();
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   if (!aborted && flags_b[0]) {
     // this CTA's units gave up: it still meets the grid (no other CTA waits in vain)
     if (warp < attnk::COMPUTE_WARPS) {
-      attnk::attn_merge<N_REP>(fp.at, shb, &cnt[3], false);
+      if (!fp.head_major) attnk::attn_merge<N_REP>(fp.at, shb, &cnt[3], false);
       if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
     }
   } else if (!aborted) {
@@ -209,7 +212,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
                                          return ok;
                                        },
                                        [&fp, &shb, cnt, units_ok]() {
-                                         const bool ok = attnk::attn_merge<N_REP>(fp.at, shb, &cnt[3], units_ok);
+                                         // head-major outputs need no merge (attn_items fenced them)
+                                         const bool ok = fp.head_major
+                                                             ? units_ok
+                                                             : attnk::attn_merge<N_REP>(fp.at, shb, &cnt[3], units_ok);
                                          // this CTA's attention outputs (whole sequences, merges) are fenced
                                          if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
                                          return ok;
@@ -225,14 +231,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
     if (flags_c[0]) rowsk::rows_drain<CfgC<NP>>(shc, fp.o_plan);
   }
   if (threadIdx.x == 0) {
-    // the last CTA out resets the grid counters for the next call
-    __threadfence();
+    // the last CTA out resets the grid counters for the next call (every
+    // CTA has passed its last wait when it arrives here; the next call sees
+    // the reset through the kernel boundary, so no fence is needed)
     if (atomicAdd(&cnt[2], 1) == grid - 1) {
       cnt[0] = 0;
       cnt[1] = 0;
       cnt[2] = 0;
       cnt[3] = 0;
-      __threadfence();
     }
   }
 }
@@ -259,6 +265,7 @@ cudaError_t launch_fused_np(const DecodeFusedArgs& a, cudaStream_t s) {
   m.qkv = a.qkv_maps;
   m.o = a.o_maps;
   m.cache = a.cache;
+  m.cache_hm = a.cache_hm;
   FusedParams fp;
   fp.pq = a.pq;
   fp.po = a.po;
@@ -266,6 +273,8 @@ cudaError_t launch_fused_np(const DecodeFusedArgs& a, cudaStream_t s) {
   fp.o_plan = a.o_plan;
   fp.at = a.at;
   fp.counters = a.counters;
+  fp.head_major = a.head_major;
+  if (a.head_major && a.at.B * N_KV > a.ctas) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ctas);
   cfg.blockDim = dim3(THREADS);

@@ -144,6 +144,7 @@ cudaError_t launch_proj_stream(const ProjStreamArgs& a, cudaStream_t s, bool pdl
 constexpr int DECODE_MAX_B = 2048;  // sequences per launch (prefix sums live in shared memory)
 constexpr int DECODE_UNIT = 16;     // cache positions per unit (TMA box) of the decode attention
 constexpr int PREFILL_TILE = 64;    // cache positions per TMA box of the prefill kernel
+constexpr int DECODE_ITEM_POS = 128; // cache positions per TMA box of the head-major decode attention
 struct DecodeAttnParams {
   const __nv_bfloat16* q;  // [B][4096] rotated queries
   int B;
@@ -215,7 +216,11 @@ constexpr int FUSED_MAX_B = 64;
 struct DecodeFusedArgs {
   RowMaps qkv_maps, o_maps;
   RowPlan qkv_plan, o_plan;
-  DecodeCacheMaps cache;
+  DecodeCacheMaps cache;     // position-major view (DecodeCacheMaps above)
+  DecodeCacheMaps cache_hm;  // head-major view: (dim, KV head, position, sequence), boxes of 64 dims x 1 head x
+                             // 128 positions (used when head_major)
+  int head_major;            // attention split: one (sequence, KV head) pair per CTA (B * 8 <= ctas) or
+                             // position-major units with merges
   ProjParams pq, po;       // Q|K|V (qkv = 1) and W_O (qkv = 0) projections
   DecodeAttnParams at;
   int* counters;           // [3] grid progress counters, zero-filled, left zero-filled

@@ -64,10 +64,14 @@ constexpr int XS_MAX = NST;              // token stages at most (all of a phase
 // NP padded tokens; XS token stages in flight. A phase whose weights come
 // from HBM wants most of shared memory for them (few token stages); one whose
 // weights are already in L2 but whose tokens only become ready when it starts
-// wants the tokens in flight instead.
-template <int NP_, int XS_ = (NP_ <= 16 ? 4 : (NP_ == 32 ? 3 : 2))>
+// wants the tokens in flight instead. INFL: weight stages requested but not
+// yet landed, at most (the ring may hold more landed ones): with every SM
+// streaming, 4 stages keep HBM busy, and each SM's reads and counter polls
+// queue behind what it has in flight, so more only adds latency.
+template <int NP_, int XS_ = (NP_ <= 16 ? 4 : (NP_ == 32 ? 3 : 2)), int INFL_ = 4>
 struct Cfg {
   static constexpr int NP = NP_;
+  static constexpr int INFL = INFL_;
   static constexpr int B_BYTES = NP * KBLK * 2;      // one k block of the token tile
   static constexpr int X_STAGE = KC * B_BYTES;       // the token rows of one weight stage
   static constexpr int XS = XS_;                     // token stages
@@ -156,8 +160,9 @@ __device__ __forceinline__ int rows_start(const RowMaps& maps, const RowPlan& pl
   const int rot = (blockIdx.x * 7) % NST;
   if ((threadIdx.x >> 5) == WARPS) {
     const int S = ring_stages(C_::W_RING, plan);
-    for (int i = 0; i < S; ++i) issue_w_stage(&maps.w[mr.mat][mr.hi], sh, i, S, wstage_bytes(plan), mr, rot);
-    return S;
+    const int D = min(S, C_::INFL);
+    for (int i = 0; i < D; ++i) issue_w_stage(&maps.w[mr.mat][mr.hi], sh, i, S, wstage_bytes(plan), mr, rot);
+    return D;
   }
   for (int i = 0; i < C_::XS; ++i) issue_x_stage<C_>(&maps.x, sh, i, rot);
   return C_::XS;
@@ -196,6 +201,12 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     int i = started;
     for (; i < NST; ++i) {
       if (i >= S && !mbar_wait(smem_u32(&sh.empty[i % S]), ((i / S) & 1) ^ 1)) {
+        atomicExch(&flags[0], 1);
+        break;
+      }
+      // at most INFL stages in flight: stage i - INFL must have landed
+      if (i >= C_::INFL && C_::INFL < S &&
+          !mbar_wait(smem_u32(&sh.full[(i - C_::INFL) % S]), ((i - C_::INFL) / S) & 1)) {
         atomicExch(&flags[0], 1);
         break;
       }
@@ -438,8 +449,12 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     }
     item(idx, pos, cs);
   }
-  fence_proxy_async_global();  // later phases of the grid read these rows by TMA
-  __threadfence();
+  if constexpr (QKV) {
+    // later phases of the grid read these rows by TMA; the W_O phase is the
+    // grid's last, and its rows are only read after the kernel boundary
+    fence_proxy_async_global();
+    __threadfence();
+  }
   asm volatile("bar.sync 4, 256;" ::: "memory");
   if (threadIdx.x == 0) rows_done();
 }

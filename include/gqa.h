@@ -223,6 +223,23 @@ int gqa_last_launch_count(void);
  * Both compute the same function. Returns the previous setting. */
 int gqa_set_decode_fusion(int enable);
 
+/* Selects, for the calling thread, how the one-kernel decode step (see
+ * gqa_set_decode_fusion) splits its attention over the grid:
+ *   0  (the default) chosen per call: head-major when the batch has at most
+ *      SMs / 8 sequences and one head's cache rows stream faster on one SM
+ *      than the whole batch's rows over every SM plus a merge round (small
+ *      batches of short contexts: B = 16 at 1,001 keys is head-major, B = 8
+ *      at 131,072 keys and every batch above 19 position-major);
+ *   1  position-major: the cache rows of the batch in 16-position units
+ *      spread evenly over the grid; sequences split between CTAs are merged
+ *      by the log-sum-exp rule after a grid-wide meeting;
+ *   2  head-major where the batch fits (B * 8 <= SMs; else position-major):
+ *      one CTA per (sequence, KV head) pair reads all of that head's rows,
+ *      nothing is merged across CTAs.
+ * Every mode computes the same function (reassociated fp32 sums). Returns
+ * the previous setting, or -1 (nothing changed) for another value. */
+int gqa_set_decode_attention_split(int mode);
+
 /* Measurement hook; it changes nothing the block computes. While set, every
  * block call on the calling thread records events[0] on its stream before its
  * first kernel and events[i] right after its i-th kernel (for i < count), so

@@ -98,6 +98,17 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
         G.lib()
 
 
+def test_decode_static_scratch_holds_every_batch_up_to_64_at_any_length(lib):
+    # the header promises that any batch of up to 64 sequences fits the static
+    # scratch at any cached length: a decode workspace does not grow with the
+    # length, and B = 64 is the largest (the few-token projection's partials)
+    need = [G.workspace_bytes(B, 1, 1 << 30) for B in range(1, 65)]
+    assert all(n > 0 for n in need)
+    assert max(need) <= G.STATIC_SCRATCH_BYTES
+    assert need[-1] == max(need)
+    assert all(G.workspace_bytes(64, 1, k) == need[-1] for k in (1, 1001, 131072))
+
+
 def test_decode_static_rejects_requests_beyond_its_scratch(lib):
     # B = 2048 needs far more than the static scratch: rejected on the host
     # before any device work

@@ -30,6 +30,23 @@ def weights():
     return I.draw_weights(seed=0)
 
 
+class attention_split:
+    """Run the block's fused decode grid with the given attention split
+    ("position", "head" or "auto") inside the with-block."""
+
+    def __init__(self, mode):
+        self.mode = mode
+
+    def __enter__(self):
+        self.prev = G.set_decode_attention_split(self.mode)
+
+    def __exit__(self, *exc):
+        G.set_decode_attention_split(self.prev)
+
+
+SPLITS = ["position", "head"]
+
+
 def run_decode(c, max_start=None, ws=None, rope=None):
     d = c.dev
     sp = torch.tensor(c.start, dtype=torch.int32, device="cuda")
@@ -79,12 +96,14 @@ def test_rope_table_matches_oracle(scaled):
     (64, None, 520),                      # largest few-token projection
     (80, None, 300),                      # tensor-core projection (M > 64)
 ])
-def test_decode_small_matches_oracle(weights, B, starts, s_max):
+@pytest.mark.parametrize("split", SPLITS)
+def test_decode_small_matches_oracle(weights, B, starts, s_max, split):
     if starts is None:
         g = torch.Generator().manual_seed(B)
         starts = torch.randint(0, s_max, (B,), generator=g).tolist()
     c = H.make_case(B, 1, starts, s_max, weights=weights)
-    out, _ = run_decode(c)
+    with attention_split(split):
+        out, _ = run_decode(c)
     assert G.last_launch_count() == (1 if B <= 64 else 3)   # one fused grid up to 64 sequences
     for b in range(B):
         H.compare_sequence(c, out, b)
@@ -114,22 +133,25 @@ def test_decode_three_kernel_path_matches_oracle(weights, B, starts, s_max):
     H.check_canaries(c)
 
 
-def test_decode_every_start_position_invalid_is_reported(weights):
+@pytest.mark.parametrize("split", SPLITS)
+def test_decode_every_start_position_invalid_is_reported(weights, split):
     """No valid sequence: the fused grid must still finish (its last phase
     waits on no sequence) and leave every cache row untouched."""
     c = H.make_case(2, 1, [3, 4], 16, weights=weights)
     d = c.dev
     sp = torch.tensor([11, 12], dtype=torch.int32, device="cuda")   # both > max_start_pos 9
     ws = G.make_workspace(2, 1, 10)
-    G.decode(d["x"], sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"],
-             workspace=ws)
+    with attention_split(split):
+        G.decode(d["x"], sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"],
+                 workspace=ws)
     torch.cuda.synchronize()
     assert G.device_status(ws, clear=True) == 1
     assert torch.equal(d["cache_k"], d["cache_k0"]) and torch.equal(d["cache_v"], d["cache_v0"])
     # the workspace (its grid counters included) is ready for the next call
     sp.copy_(torch.tensor([3, 4], dtype=torch.int32))
-    out = G.decode(d["x"], sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"],
-                   workspace=ws)
+    with attention_split(split):
+        out = G.decode(d["x"], sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"],
+                       d["cache_v"], workspace=ws)
     torch.cuda.synchronize()
     assert G.device_status(ws) == 0
     for b in range(2):
@@ -146,14 +168,16 @@ def test_decode_is_repeatable_with_a_reused_workspace(weights):
         H.compare_sequence(c, out2, b)
 
 
-def test_decode_bad_start_position_is_reported_and_skipped(weights):
+@pytest.mark.parametrize("split", SPLITS)
+def test_decode_bad_start_position_is_reported_and_skipped(weights, split):
     c = H.make_case(3, 1, [5, 9, 7], 16, weights=weights)
     d = c.dev
     sp = torch.tensor([5, 12, 7], dtype=torch.int32, device="cuda")   # 12 > max_start_pos 9
     ws = G.make_workspace(3, 1, 10)
     out = torch.full_like(d["x"], float("nan"))
-    G.decode(d["x"], sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"],
-             out=out, workspace=ws)
+    with attention_split(split):
+        G.decode(d["x"], sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"],
+                 out=out, workspace=ws)
     assert G.device_status(ws, clear=True) == 1
     assert torch.equal(d["cache_k"][1], d["cache_k0"][1])   # skipped sequence untouched
     c.start = [5, 9, 7]
@@ -162,14 +186,53 @@ def test_decode_bad_start_position_is_reported_and_skipped(weights):
 
 
 @pytest.mark.parametrize("name", ["decode_b1_p15", "decode_b16_p1000"])
-def test_decode_workloads_full(weights, name):
+@pytest.mark.parametrize("split", SPLITS)
+def test_decode_workloads_full(weights, name, split):
     w = I.workload(name)
     c = H.make_case(w.B, 1, w.start_positions().tolist(), w.cache_rows(), weights=weights)
-    out, _ = run_decode(c)
+    with attention_split(split):
+        out, _ = run_decode(c)
     worst = 0.0
     for b in range(w.B):
         worst = max(worst, H.compare_sequence(c, out, b)[0])
     H.check_canaries(c)
+
+
+@pytest.mark.parametrize("B,starts,s_max", [
+    (1, [0], 2),                                  # one key per head: o_h = v_{h//4}
+    (2, [127, 128], 130),                         # a stage of 128 keys whole, and one key past it
+    (5, [126, 255, 256, 383, 1], 400),            # stage edges from both sides, ragged
+    (19, [int(v) for v in np.random.default_rng(19).integers(0, 900, 19)], 900),  # every SM holds a pair
+])
+def test_decode_head_major_edges(weights, B, starts, s_max):
+    """The head-major split at the edges of its 128-position stages: warps
+    whose 16 keys lie past the sequence skip the stage, and the warps'
+    states are combined in shared memory."""
+    c = H.make_case(B, 1, starts, s_max, weights=weights)
+    with attention_split("head"):
+        out, _ = run_decode(c)
+    for b in range(B):
+        H.compare_sequence(c, out, b)
+    H.check_canaries(c)
+
+
+def test_decode_splits_alternate_on_one_workspace(weights):
+    """Calls switching between the two attention splits share one workspace:
+    each leaves the grid counters ready for the other."""
+    c = H.make_case(6, 1, [1000, 3, 517, 64, 0, 130], 1100, weights=weights)
+    ws = G.make_workspace(6, 1, 1001)
+    for split in ("head", "position", "head", "auto", "position"):
+        with attention_split(split):
+            out, _ = run_decode(c, ws=ws)
+        for b in range(6):
+            H.compare_sequence(c, out, b)
+
+
+def test_decode_split_setting_is_validated():
+    assert G.lib().gqa_set_decode_attention_split(3) == -1
+    assert G.lib().gqa_set_decode_attention_split(-1) == -1
+    with pytest.raises(ValueError):
+        G.set_decode_attention_split("rows")
 
 
 def test_block_forward_decode_matches_oracle(weights):
@@ -293,9 +356,10 @@ def test_large_decode_workloads_sampled(weights, name, sample):
 # ------------------------------------------------------------------ the layer: h = x + attention(norm(x))
 
 @pytest.mark.parametrize("B,starts,s_max,fused", [
-    (16, [3, 40, 17, 100] * 4, 128, True),    # the fused decode grid
-    (16, [3, 40, 17, 100] * 4, 128, False),   # three kernels
-    (80, list(range(5, 85)), 100, True),      # above the fused grid's batch: tensor-core projections
+    (16, [3, 40, 17, 100] * 4, 128, "position"),   # the fused decode grid, both attention splits
+    (16, [3, 40, 17, 100] * 4, 128, "head"),
+    (16, [3, 40, 17, 100] * 4, 128, False),        # three kernels
+    (80, list(range(5, 85)), 100, "auto"),         # above the fused grid's batch: tensor-core projections
 ])
 def test_layer_decode_matches_oracle(weights, B, starts, s_max, fused):
     c = H.make_case(B, 1, starts, s_max, weights=weights)
@@ -303,17 +367,17 @@ def test_layer_decode_matches_oracle(weights, B, starts, s_max, fused):
     d = c.dev
     sp = torch.tensor(starts, dtype=torch.int32, device="cuda")
     ws = G.make_workspace(B, 1, max(starts) + 1)
-    prev = G.set_decode_fusion(fused)
+    prev = G.set_decode_fusion(bool(fused))
     try:
-        h = G.layer_decode(d["x"], sp, max(starts), g, I.NORM_EPS, d["wq"], d["wk"], d["wv"], d["wo"],
-                           H.rope_for(c), d["cache_k"], d["cache_v"], workspace=ws)
+        with attention_split(fused if fused else "auto"):
+            h = G.layer_decode(d["x"], sp, max(starts), g, I.NORM_EPS, d["wq"], d["wk"], d["wv"], d["wo"],
+                               H.rope_for(c), d["cache_k"], d["cache_v"], workspace=ws)
         torch.cuda.synchronize()
     finally:
         G.set_decode_fusion(prev)
     assert G.device_status(ws) == 0
-    xn = G.rms_norm(d["x"], g, I.NORM_EPS)
     for b in range(0, B, max(1, B // 8)):
-        H.compare_layer_sequence(c, h, b, g, I.NORM_EPS, xn)
+        H.compare_layer_sequence(c, h, b, g, I.NORM_EPS)
     H.check_canaries(c)
 
 
@@ -331,9 +395,8 @@ def test_layer_prefill_matches_oracle(weights, B, T, start, s_max):
                         d["cache_k"], d["cache_v"], workspace=ws)
     torch.cuda.synchronize()
     assert G.device_status(ws) == 0
-    xn = G.rms_norm(d["x"], g, I.NORM_EPS)
     for b in range(B):
-        H.compare_layer_sequence(c, h, b, g, I.NORM_EPS, xn)
+        H.compare_layer_sequence(c, h, b, g, I.NORM_EPS)
     H.check_canaries(c)
     # the residual is really there: h - x is the normalised block's delta, not h
     assert float((h.float() - d["x"].float()).abs().max()) < float(h.float().abs().max())
@@ -358,10 +421,13 @@ def test_rms_norm_matches_oracle():
 def test_layer_decode_chained_layers_match_oracle(fused):
     """Three consecutive layers of one decode step, each with its own weights
     and KV cache, one shared workspace, the output of one the input of the
-    next: every layer against the oracle layer on that layer's GPU input, and
-    the whole chain against the oracle chained in fp64 (h rounded to bf16
-    between layers, as the block stores it; the max-abs bar widened by one
-    bf16 ulp of h per layer for those roundings)."""
+    next, against the oracle chained in fp64 from the same seeded input (h
+    rounded to bf16 between layers, as the block stores it). Layer 0 (whose
+    input is the seeded x) is held to the layer bars of
+    ``compare_layer_sequence``; the cache rows of later layers, whose inputs
+    are earlier layers' outputs, to the delta bar; the final h to the delta
+    bar, its max-abs bar widened by one bf16 ulp of h per layer for the
+    roundings between layers."""
     B, starts, s_max, L = 4, [0, 17, 128, 300], 320, 3
     cases = [H.make_case(B, 1, starts, s_max, seed=10 + l) for l in range(L)]
     gs = [I.draw_norm_weight(seed=10 + l).cuda() for l in range(L)]
@@ -378,24 +444,27 @@ def test_layer_decode_chained_layers_match_oracle(fused):
     finally:
         G.set_decode_fusion(prev)
     assert G.device_status(ws) == 0
-    for l, c in enumerate(cases):
-        c.host["x"] = xs[l].cpu()          # this layer's input, as the GPU saw it
-        xn = G.rms_norm(xs[l], gs[l], I.NORM_EPS)
-        for b in range(B):
-            H.compare_layer_sequence(c, xs[l + 1], b, gs[l], I.NORM_EPS, xn)
+    for b in range(B):
+        H.compare_layer_sequence(cases[0], xs[1], b, gs[0], I.NORM_EPS)
+    for c in cases:
         H.check_canaries(c)
     r = I.LLAMA31_ROPE
     freqs = O.rope_frequencies(128, r.theta, r.scaled, r.factor, r.low_freq_factor, r.high_freq_factor,
                                r.original_context)
     for b in range(B):
-        h = H.f64(cases[0].dev["x"][b])
+        h = H.f64(cases[0].host["x"][b])
         for l, c in enumerate(cases):
             w = H.weights64(c)
             sp_b = starts[b]
-            h, _, _ = O.layer_sequence_forward(h, H.f64(gs[l]), I.NORM_EPS, w["wq"], w["wk"], w["wv"], w["wo"], sp_b,
-                                               H.f64(c.dev["cache_k0"][b, :sp_b]), H.f64(c.dev["cache_v0"][b, :sp_b]),
-                                               freqs, 32, 8)
+            h, nk, nv = O.layer_sequence_forward(h, H.f64(gs[l]), I.NORM_EPS, w["wq"], w["wk"], w["wv"], w["wo"],
+                                                 sp_b, H.f64(c.dev["cache_k0"][b, :sp_b]),
+                                                 H.f64(c.dev["cache_v0"][b, :sp_b]), freqs, 32, 8)
             h = O.bf16_round(h)
+            if l > 0:
+                for name, ref in (("cache_k", nk), ("cache_v", nv)):
+                    got = H.f64(c.dev[name][b, sp_b:sp_b + 1])
+                    assert H.rel_l2(got, ref) <= H.REL_L2_TOL, f"layer {l} {name} row of sequence {b}"
+                    assert float(np.abs(got - ref).max()) <= H.MAX_ABS_TOL, f"layer {l} {name} row of sequence {b}"
         got = H.f64(xs[-1][b])
         assert H.rel_l2(got, h) <= H.REL_L2_TOL
         # both sides round h to bf16 after every layer: where they land on
@@ -577,19 +646,21 @@ def test_decode_reused_workspace_across_batch_shapes(weights):
     the large step left behind."""
     big = H.make_case(16, 1, list(range(200, 1800, 100)), 1800, weights=weights)
     ws = G.make_workspace(16, 1, 1800)
-    run_decode(big, ws=ws)
-    for fused in (True, False):
+    with attention_split("position"):
+        run_decode(big, ws=ws)
+    for fused, split in ((True, "position"), (True, "head"), (False, "auto")):
         small = H.make_case(3, 1, [0, 5, 130], 160, seed=1)
         prev = G.set_decode_fusion(fused)
         try:
-            out, _ = run_decode(small, ws=ws)
+            with attention_split(split):
+                out, _ = run_decode(small, ws=ws)
         finally:
             G.set_decode_fusion(prev)
         for b in range(3):
             H.compare_sequence(small, out, b)
 
 
-@pytest.mark.parametrize("kind", ["decode_fused", "decode_three", "prefill"])
+@pytest.mark.parametrize("kind", ["decode_fused", "decode_fused_head", "decode_three", "prefill"])
 def test_workspace_and_output_guards_untouched(weights, kind):
     """Bytes past the workspace size the library asks for, and past the
     output rows, keep their pattern: no kernel writes outside its buffers."""
@@ -609,10 +680,11 @@ def test_workspace_and_output_guards_untouched(weights, kind):
                         workspace=ws)
     else:
         sp = torch.tensor(starts, dtype=torch.int32, device="cuda")
-        prev = G.set_decode_fusion(kind == "decode_fused")
+        prev = G.set_decode_fusion(kind != "decode_three")
         try:
-            G.decode(d["x"], sp, max(starts), d["wq"], d["wk"], d["wv"], d["wo"], rope, d["cache_k"], d["cache_v"],
-                     out=out, workspace=ws)
+            with attention_split("head" if kind == "decode_fused_head" else "position"):
+                G.decode(d["x"], sp, max(starts), d["wq"], d["wk"], d["wv"], d["wo"], rope, d["cache_k"],
+                         d["cache_v"], out=out, workspace=ws)
         finally:
             G.set_decode_fusion(prev)
     torch.cuda.synchronize()

@@ -42,7 +42,14 @@ MUTANTS = {
     "head_merge_transposed": ("delta = o.reshape(len(rows), n_heads * head_dim) @ wo.T",
                               "delta = o.transpose(0, 2, 1).reshape(len(rows), n_heads * head_dim) @ wo.T"),
     "new_rows_written_at_zero": ("        ck[b, sp[b]:sp[b] + T] = nk", "        ck[b, :T] = nk"),
+    # scaled-RoPE band blends that still meet both edges
+    "band_geometric_blend": ("mid = (1.0 - mu) * f / factor + mu * f", "mid = f / factor * factor ** mu"),
+    "band_linear_in_wavelength": (
+        "mu = (original_context / wavelength - low_freq_factor) / (high_freq_factor - low_freq_factor)",
+        "mu = (long_edge - wavelength) / (long_edge - short_edge)"),
 }
+
+BAND_MUTANTS = ("band_geometric_blend", "band_linear_in_wavelength")
 
 
 def load(src):
@@ -86,6 +93,13 @@ def pin_scaled_frequencies(M):
     np.testing.assert_allclose(f, [brute.frequency(i, 128, 500000.0, True) for i in range(64)], rtol=1e-14)
 
 
+def pin_band_affine(M):
+    """Structural pin of the band (no restated formula): f'/f affine in f."""
+    from tests.test_oracle_pins import band_ratio_affine_residual
+    assert band_ratio_affine_residual(M.rope_frequencies(128, 500000.0, True),
+                                      M.rope_frequencies(128, 500000.0, False)) < 1e-12
+
+
 def pin_gqa_vs_mha(M):
     rng = np.random.default_rng(8)
     H, Hkv, hd = 4, 2, 4
@@ -118,7 +132,7 @@ def pin_layer_residual(M):
     np.testing.assert_array_equal(h, x)
 
 
-PINS = (pin_brute, pin_scaled_frequencies, pin_gqa_vs_mha, pin_rms_norm, pin_layer_residual)
+PINS = (pin_brute, pin_scaled_frequencies, pin_band_affine, pin_gqa_vs_mha, pin_rms_norm, pin_layer_residual)
 
 
 def test_unmutated_oracle_passes_every_pin():
@@ -140,3 +154,13 @@ def test_planted_mistake_is_caught(name):
         except (AssertionError, ValueError, IndexError):
             failures += 1
     assert failures > 0, f"no pin caught the planted mistake {name}"
+
+
+@pytest.mark.parametrize("name", BAND_MUTANTS)
+def test_band_blend_mistake_is_caught_by_the_structural_pin(name):
+    """The affine-ratio pin alone catches a wrong band blend: it does not lean
+    on the scalar restatement of the same formula."""
+    old, new = MUTANTS[name]
+    M = load(SRC.replace(old, new))
+    with pytest.raises(AssertionError):
+        pin_band_affine(M)

@@ -168,6 +168,35 @@ def test_scaled_frequency_bands():
     np.testing.assert_allclose(f, [brute.frequency(i, 128, 500000.0, True) for i in range(64)], rtol=1e-14)
 
 
+def band_ratio_affine_residual(fr_scaled, fr_base, low=1.0, high=4.0, ctx=8192):
+    """Largest distance of the band's points (f, f'/f) from their least-squares
+    line, relative to the spread of f'/f. The reading interpolates linearly in
+    mu, and mu is affine in 1/wavelength, i.e. in f: the points are collinear.
+    A geometric blend (f/8 * 8^mu) or a blend linear in the wavelength puts
+    them on a curve."""
+    wl = 2 * math.pi / fr_base
+    band = (wl >= ctx / high) & (wl <= ctx / low)
+    f, r = fr_base[band], fr_scaled[band] / fr_base[band]
+    assert band.sum() >= 3
+    A = np.stack([f, np.ones_like(f)], axis=1)
+    coef, *_ = np.linalg.lstsq(A, r, rcond=None)
+    return float(np.abs(A @ coef - r).max() / (r.max() - r.min()))
+
+
+def test_scaled_band_ratio_is_affine_in_frequency():
+    base = O.rope_frequencies(128, 500000.0, False)
+    assert band_ratio_affine_residual(O.rope_frequencies(128, 500000.0, True), base) < 1e-12
+    # the pin separates the reading from the two other smooth blends that meet
+    # both edges: geometric in mu, and linear in the wavelength
+    wl = 2 * math.pi / base
+    mu = (8192 / wl - 1) / 3
+    geo = np.where(wl < 2048, base, np.where(wl > 8192, base / 8, base / 8 * 8.0 ** mu))
+    lam = (8192 - wl) / (8192 - 2048)
+    in_wl = np.where(wl < 2048, base, np.where(wl > 8192, base / 8, (1 - lam) * base / 8 + lam * base))
+    assert band_ratio_affine_residual(geo, base) > 1e-3
+    assert band_ratio_affine_residual(in_wl, base) > 1e-3
+
+
 def test_scaled_band_formula_is_continuous_at_both_edges():
     # choose theta so that pair 1's wavelength sits exactly on each edge
     for edge, expect_div in ((8192 / 4, 1.0), (8192 / 1, 8.0)):

@@ -4,10 +4,12 @@ cudaMalloc, a real-time serving loop where a synchronous allocation would
 stall the device). Its scratch is a static array inside the library instead
 of a caller workspace.
 
-Two calls in a row on different inputs, each checked against gqa_decode on
-the same inputs with the parity tolerance of the other tests; the second call
-must not see anything the first one left in the shared array. Collected last
-on purpose, and valid both alone and after the other tests."""
+Calls in a row on different inputs, each checked against gqa_decode on the
+same inputs with the parity tolerance of the other tests and against the CPU
+oracle; a later call must not see anything an earlier one left in the shared
+array. The last case is a batch of 64 ragged sequences, the largest batch the
+header promises fits the array. Collected last on purpose, and valid both
+alone and after the other tests."""
 import numpy as np
 import pytest
 import torch
@@ -38,14 +40,16 @@ def _decode_both_ways(c):
     return ref, got, ref_k, ref_v
 
 
-def test_decode_static_matches_decode_on_two_calls_in_a_row():
+def test_decode_static_matches_decode_and_the_oracle_on_calls_in_a_row():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from grouped_query_attention_gemv_gb300 import build
     build.build()
     weights = I.draw_weights(seed=0)
+    ragged64 = [int(p) for p in np.random.default_rng(64).integers(0, 2048, 64)]
     cases = [H.make_case(6, 1, [1000, 3, 517, 64, 0, 2047], 2048, weights=weights),
-             H.make_case(3, 1, [40, 129, 7], 160, seed=0, weights=weights)]
+             H.make_case(3, 1, [40, 129, 7], 160, seed=0, weights=weights),
+             H.make_case(64, 1, ragged64, 2048, seed=1, weights=weights)]
     for c in cases:
         ref, got, ref_k, ref_v = _decode_both_ways(c)
         a, b = H.f64(got), H.f64(ref)
@@ -56,4 +60,7 @@ def test_decode_static_matches_decode_on_two_calls_in_a_row():
             for name, ref_c in (("cache_k", ref_k), ("cache_v", ref_v)):
                 H.check_rows_within_one_ulp(c.dev[name][bi, sp:sp + 1], H.f64(ref_c[bi, sp:sp + 1]),
                                             f"{name} row of sequence {bi}")
+        # and against the oracle on the same seeded inputs (delta and the written rows)
+        for bi in range(0, c.B, max(1, c.B // 8)):
+            H.compare_sequence(c, got, bi)
         H.check_canaries(c)
