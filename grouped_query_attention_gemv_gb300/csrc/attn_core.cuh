@@ -273,11 +273,12 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
       const uint32_t dst = smem_u32(sh.ring + s * UNIT_BYTES);
       const uint32_t fb = smem_u32(&sh.full[s]);
       const int pos = iss.j * UNIT, h0 = (iss.b % NG) * N_KV, sb = iss.b / NG;
+      const uint64_t pol = l2_evict_first();
       mbar_expect_tx(fb, UNIT_BYTES);
-      tma_load_4d(dst, &mk, fb, 0, pos, h0, sb);
-      tma_load_4d(dst + BOX_BYTES, &mk, fb, 64, pos, h0, sb);
-      tma_load_4d(dst + 2 * BOX_BYTES, &mv, fb, 0, pos, h0, sb);
-      tma_load_4d(dst + 3 * BOX_BYTES, &mv, fb, 64, pos, h0, sb);
+      tma_load_4d_stream(dst, &mk, fb, 0, pos, h0, sb, pol);
+      tma_load_4d_stream(dst + BOX_BYTES, &mk, fb, 64, pos, h0, sb, pol);
+      tma_load_4d_stream(dst + 2 * BOX_BYTES, &mv, fb, 0, pos, h0, sb, pol);
+      tma_load_4d_stream(dst + 3 * BOX_BYTES, &mv, fb, 64, pos, h0, sb, pol);
       advance(iss, pre, B);
     };
     int i = 0;
@@ -446,11 +447,12 @@ __device__ __forceinline__ bool attn_items(const CUtensorMap& mk, const CUtensor
       const uint32_t dst = smem_u32(sh.ring + s * UNIT_BYTES);
       const uint32_t fb = smem_u32(&sh.full[s]);
       const int pos = i * ITEM_POS;
+      const uint64_t pol = l2_evict_first();
       mbar_expect_tx(fb, UNIT_BYTES);
-      tma_load_4d(dst, &mk, fb, 0, g, pos, b);
-      tma_load_4d(dst + BOX_BYTES, &mk, fb, 64, g, pos, b);
-      tma_load_4d(dst + 2 * BOX_BYTES, &mv, fb, 0, g, pos, b);
-      tma_load_4d(dst + 3 * BOX_BYTES, &mv, fb, 64, g, pos, b);
+      tma_load_4d_stream(dst, &mk, fb, 0, g, pos, b, pol);
+      tma_load_4d_stream(dst + BOX_BYTES, &mk, fb, 64, g, pos, b, pol);
+      tma_load_4d_stream(dst + 2 * BOX_BYTES, &mv, fb, 0, g, pos, b, pol);
+      tma_load_4d_stream(dst + 3 * BOX_BYTES, &mv, fb, 64, g, pos, b, pol);
     };
     int i = 0;
     while (i + 1 < n && i < PRE_GATE_UNITS) issue(i++);  // stages before the one holding row P

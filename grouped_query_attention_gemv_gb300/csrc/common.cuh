@@ -258,6 +258,29 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
       :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z) : "memory");
 }
+// L2 cache policy for bytes a kernel streams once (weights, KV rows): their
+// lines are the first L2 evicts, so the small data every step re-reads (the
+// kernel's code, token rows, queries, start positions, the RoPE rows, grid
+// counters) stays resident while each step streams 150 MB and more through L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_load_3d_stream(uint32_t dst, const void* map, uint32_t bar, int x, int y, int z,
+                                                   uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;"
+      :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_stream(uint32_t dst, const void* map, uint32_t bar, int x, int y, int z,
+                                                   int w, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;"
+      :: "r"(dst), "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "l"(pol) : "memory");
+}
 // Ask L2 for the box of a 4-D tensor map at the given coordinates.
 __device__ __forceinline__ void tma_prefetch_4d(const void* map, int x, int y, int z, int w) {
   asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"

@@ -155,7 +155,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
     for (int i = 0; i < 4; ++i) flags_a[i] = flags_b[i] = flags_c[i] = 0;
     fence_barrier_init();
   }
-  if (warp == rowsk::WARPS - 1) attnk::build_prefix<1>(fp.at, pre);
+  // (nothing here may wait on a global load: at the start of the grid a load
+  // that misses L2 queues behind every CTA's first weight stages, ~3 us)
   __syncthreads();
   const int grid = static_cast<int>(gridDim.x);
   int* const cnt = fp.counters;
@@ -167,6 +168,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   fence_proxy_async_smem();  // the ring's generic reads and writes precede phase B's TMA writes into it
   __syncthreads();
   bool aborted = flags_a[0] != 0;
+  if (!fp.head_major) {
+    // the position-major split's unit prefix (the start positions are in L2 by now)
+    if (warp == rowsk::WARPS - 1) attnk::build_prefix<1>(fp.at, pre);
+    __syncthreads();
+  }
 
   // ---------------- phase B: attention units (waits for every CTA's Q|K|V rows)
   const attnk::Shared shb{smem, b_bars, b_bars + attnk::STAGES, flags_b, pre,
@@ -193,6 +199,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
     fence_proxy_async_smem();  // ldmatrix reads of the ring precede phase C's TMA writes into it
   }
   __syncthreads();
+  // Head-major outputs are complete and fenced: publish them before phase C's
+  // weight loads are in flight, because a release on an SM waits for the
+  // bulk loads that SM has in flight (~1.5 us more when W_O's stages are out).
+  const bool early_signal = fp.head_major && !aborted;
+  if (early_signal) {
+    if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
+    __syncthreads();
+  }
 
   // ---------------- phase C: W_O projection. Its weight loads start at once;
   // meanwhile the compute warps meet the grid and merge the attention
@@ -202,7 +216,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
     // this CTA's units gave up: it still meets the grid (no other CTA waits in vain)
     if (warp < attnk::COMPUTE_WARPS) {
       if (!fp.head_major) attnk::attn_merge<N_REP>(fp.at, shb, &cnt[3], false);
-      if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
+      if (threadIdx.x == 0 && !early_signal) signal_counter(&cnt[1], 1);
     }
   } else if (!aborted) {
     rowsk::rows_phase<CfgC<NP>, false>(m.o, fp.po, fp.o_plan, shc,
@@ -211,11 +225,11 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
                                          fence_proxy_async_global();  // o was written by plain stores
                                          return ok;
                                        },
-                                       [&fp, &shb, cnt, units_ok]() {
-                                         // head-major outputs need no merge (attn_items fenced them)
-                                         const bool ok = fp.head_major
-                                                             ? units_ok
-                                                             : attnk::attn_merge<N_REP>(fp.at, shb, &cnt[3], units_ok);
+                                       [&fp, &shb, cnt, units_ok, early_signal]() {
+                                         // head-major outputs need no merge (attn_items fenced them and
+                                         // they are published already)
+                                         if (early_signal) return units_ok;
+                                         const bool ok = attnk::attn_merge<N_REP>(fp.at, shb, &cnt[3], units_ok);
                                          // this CTA's attention outputs (whole sequences, merges) are fenced
                                          if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
                                          return ok;

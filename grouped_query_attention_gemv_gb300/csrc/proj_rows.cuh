@@ -135,7 +135,7 @@ __device__ __forceinline__ void issue_w_stage(const CUtensorMap* wmap, const Sha
   const int s = i % S, ks = (i + rot) % NST;
   const uint32_t fb = smem_u32(&sh.full[s]);
   mbar_expect_tx(fb, KC * mr.h * 128);
-  tma_load_3d(smem_u32(sh.ring + s * wstage), wmap, fb, 0, mr.row0, ks * KC);
+  tma_load_3d_stream(smem_u32(sh.ring + s * wstage), wmap, fb, 0, mr.row0, ks * KC, l2_evict_first());
 }
 // The token rows of stage i into token slot i % XS.
 template <class C_>
@@ -244,11 +244,19 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
   const int ks0 = C_::TOKEN_SPLIT ? 0 : 2 * (warp / KC);
   const int tok0 = C_::TOKEN_SPLIT ? (warp / KC) * (NP / 2) : 0;
   const int mtc = (mr.h + 15) >> 4;  // row tiles holding this CTA's rows
-  float acc[MT_MAX][C_::NT][4];
+  // With few tokens the two k16 halves of a stage accumulate separately
+  // (summed after the stream): an mma.sync result feeds the next product on
+  // the same accumulator only after a long fixed latency, and one chain per
+  // accumulator instead of two halves the stall each stage pays for it.
+  constexpr int KH = C_::NT <= 2 ? 2 : 1;
+  float acc[KH][MT_MAX][C_::NT][4];
 #pragma unroll
-  for (int mt = 0; mt < MT_MAX; ++mt)
+  for (int h = 0; h < KH; ++h)
 #pragma unroll
-    for (int nt = 0; nt < C_::NT; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+    for (int mt = 0; mt < MT_MAX; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < C_::NT; ++nt)
+        acc[h][mt][nt][0] = acc[h][mt][nt][1] = acc[h][mt][nt][2] = acc[h][mt][nt][3] = 0.f;
 
   // Each warp runs through the stages on its own (no per-stage barrier, so
   // that warps drift and cover each other's latencies); a warp whose bounded
@@ -286,30 +294,42 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
   };
   if (norm) load_g(0, gnext);
   // the epilogue's first EPF items of this thread (item = (row pair, token)):
-  // their start positions and RoPE factors are loaded now, so that the
-  // loads' latency is spent under the stream rather than after it
+  // their start positions and RoPE factors are loaded during the stream, in
+  // two steps (the start positions after stage EPF_SP, the factors, whose
+  // address depends on them, after stage EPF_ROPE), so that no compute warp
+  // waits on a load before its first stage: at the start of the grid every
+  // load that misses L2 queues behind the whole grid's first weight stages
   const int fbase = (mr.mat == 0 ? 0 : (mr.mat == 1 ? p.r1 : p.r2)) + mr.row0;  // feature of row 0
   const int items = (mr.h / 2) * p.M;
-  constexpr int EPF = 2;
-  int pos_pf[EPF];
+  constexpr int EPF = 2, EPF_SP = 1, EPF_ROPE = NST / 2;
+  int pos_pf[EPF], sp_pf[EPF];
   float2 cs_pf[EPF];
 #pragma unroll
   for (int k = 0; k < EPF; ++k) {
     pos_pf[k] = -1;
+    sp_pf[k] = -1;
     cs_pf[k] = make_float2(1.f, 0.f);
-    const int idx = threadIdx.x + k * WARPS * 32;
-    if (QKV && idx < items) {
-      const int m = idx % p.M, f = fbase + 2 * (idx / p.M);
-      const int b = m / p.T;
-      const int start = p.sp.get(b);
-      if (p.sp.ok(start)) {
-        pos_pf[k] = start + (m - b * p.T);
+  }
+  auto epf_start_positions = [&]() {
+#pragma unroll
+    for (int k = 0; k < EPF; ++k) {
+      const int idx = threadIdx.x + k * WARPS * 32;
+      if (idx < items) sp_pf[k] = p.sp.get((idx % p.M) / p.T);
+    }
+  };
+  auto epf_rope = [&]() {
+#pragma unroll
+    for (int k = 0; k < EPF; ++k) {
+      const int idx = threadIdx.x + k * WARPS * 32;
+      if (idx < items && p.sp.ok(sp_pf[k])) {
+        const int m = idx % p.M, f = fbase + 2 * (idx / p.M);
+        pos_pf[k] = sp_pf[k] + (m - (m / p.T) * p.T);
         if (f < p.r2)
           cs_pf[k] = *reinterpret_cast<const float2*>(
               p.rope + (static_cast<size_t>(pos_pf[k]) * ROPE_PAIRS + ((f & (HEAD_DIM - 1)) >> 1)) * 2);
       }
     }
-  }
+  };
   for (int i = 0; ok && i < NST; ++i) {
     uint32_t gcur[NG];
 #pragma unroll
@@ -354,7 +374,7 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
             ldsm_x4(wa + sw128(r, 2 * (ks + kk) + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
             for (int nt = 0; nt < C_::NT; ++nt)
-              mma16816(acc[mt][nt], a0, a1, a2, a3, b[nt][2 * kk], b[nt][2 * kk + 1]);
+              mma16816(acc[kk % KH][mt][nt], a0, a1, a2, a3, b[nt][2 * kk], b[nt][2 * kk + 1]);
           }
         }
       }
@@ -363,6 +383,10 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     if (lane == 0) {
       mbar_arrive(smem_u32(&sh.empty[s]));
       mbar_arrive(smem_u32(&sh.xempty[xs]));
+    }
+    if constexpr (QKV) {
+      if (i == EPF_SP) epf_start_positions();
+      if (i == EPF_ROPE) epf_rope();
     }
   }
   if (!ok && lane == 0) atomicExch(&flags[0], 1);
@@ -383,8 +407,13 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
         for (int nt = 0; nt < C_::NT; ++nt) {
           const int row = mt * 16 + gr, tok = tok0 + nt * 8 + 2 * t;
           float* d = red + (warp * ROWS_MAX_H + row) * NP + tok;
-          *reinterpret_cast<float2*>(d) = make_float2(acc[mt][nt][0], acc[mt][nt][1]);
-          *reinterpret_cast<float2*>(d + 8 * NP) = make_float2(acc[mt][nt][2], acc[mt][nt][3]);
+          float v[4] = {acc[0][mt][nt][0], acc[0][mt][nt][1], acc[0][mt][nt][2], acc[0][mt][nt][3]};
+#pragma unroll
+          for (int h = 1; h < KH; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] += acc[h][mt][nt][e];
+          *reinterpret_cast<float2*>(d) = make_float2(v[0], v[1]);
+          *reinterpret_cast<float2*>(d + 8 * NP) = make_float2(v[2], v[3]);
         }
       }
     }
