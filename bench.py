@@ -61,6 +61,8 @@ def args_():
     ap.add_argument("--replicas", type=int, default=4)
     ap.add_argument("--graph-steps", type=int, default=8, help="steps captured per CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="headline only (by default its line also carries every other configuration)")
     ap.add_argument("--oracle-sample", type=float, default=None, help=argparse.SUPPRESS)  # internal: one-core leg
     ap.add_argument("--entry", choices=["block", "layer"], default="block",
                     help="block: delta = attention(x); layer: h = x + attention(RMSNorm(x)) (one more kernel)")
@@ -176,14 +178,11 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        if not self.rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        inside = [r for t, r in self.rows if self.t0 and self.t1 and self.t0 <= t <= self.t1]
-        use = inside or [r for _, r in self.rows]
+    @staticmethod
+    def _stats(rows):
         sm, smax, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for r in use:
+        for r in rows:
             f = [x.strip() for x in r.split(",")]
             try:
                 sm.append(float(f[1]))
@@ -193,8 +192,26 @@ class ClockSampler:
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
+        return (statistics.median(sm) if sm else None, max(smax) if smax else None, sorted(reasons))
+
+    def summary(self, soak_replays=None):
+        """sm_mhz and reasons from the samples inside the timed region, else
+        (a region shorter than the sampling period) from the soak that replays
+        the same graphs right after it; both sets are reported."""
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [r for t, r in self.rows if self.t0 and self.t1 and self.t0 <= t <= self.t1]
+        soak = [r for t, r in self.rows if getattr(self, "s0", None) and self.s0 <= t <= getattr(self, "s1", 0)]
+        use = inside or soak or [r for _, r in self.rows]
+        sm, smax, reasons = self._stats(use)
+        out = {"sm_mhz": sm, "sm_max_mhz": smax, "reasons": reasons, "samples": len(use),
+               "samples_in_timed_region": len(inside),
+               "source": "timed region" if inside else ("soak" if soak else "whole run")}
+        if soak:
+            s_sm, s_max, s_reasons = self._stats(soak)
+            out["soak"] = {"sm_mhz": s_sm, "sm_max_mhz": s_max, "reasons": s_reasons, "samples": len(soak),
+                           "replays": soak_replays}
+        return out
 
 
 def _oracle_inputs(w: I.Workload):
@@ -322,10 +339,12 @@ def run_reference(a, w: I.Workload, rank: int, world: int):
     }))
 
 
-def config_dict(w: I.Workload, a, starts):
+def config_dict(w: I.Workload, a, starts, replicas=None):
+    replicas = a.replicas if replicas is None else replicas
     c = {"workload": w.name, "B": w.B, "T": w.T, "s_max": w.cache_rows(), "d_model": 4096, "n_heads": 32,
          "n_kv_heads": w.n_kv_heads, "head_dim": 128,
-         "l2": f"inputs larger than L2: {a.replicas} rotating replicas of weights+cache+x, one per step",
+         "l2": (f"inputs larger than L2: {replicas} rotating replicas of weights+cache+x, one per step"
+                if replicas > 1 else "inputs larger than L2: the KV cache alone is several GB"),
          "parallelism": "replicas"}
     if w.layers > 1:
         c["layers"] = w.layers
@@ -361,35 +380,31 @@ def _max_over_ranks(v, world, dev):
     return float(t.item())
 
 
-def main():
-    a = args_()
-    rank, world, local = dist_env()
-    w = I.workload(a.workload)
-    if a.oracle_sample is not None:   # the one-core leg of the CPU baseline (a child of cpu_baseline)
-        print(json.dumps(cpu_baseline(w, a.oracle_sample, one_core=False)))
-        return
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("gloo" if a.impl == "reference" else "nccl")
-    if a.impl == "reference":
-        run_reference(a, w, rank, world)
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
+# The other configurations of the benchmark, measured in the same run and
+# attached to the headline line under "workloads": (name, step cap, replicas
+# of weights + cache rotated between steps; one where the cache alone is far
+# above L2)
+SECONDARY = (("decode_b1_p15", 2000, 4), ("batched_decode_b64_p512_32768", 50, 1),
+             ("long_decode_b8_p131071", 50, 1), ("prefill_b1_t2048", 200, 4), ("prefill_b4_t2048", 100, 2))
+NOMINAL_HBM_GBS = 7900.0      # GB300 HBM3e, nominal
+NOMINAL_BF16_TFLOPS = 2250.0  # GB300 dense bf16 tensor, nominal
+SOAK_S = 0.5                  # clock samples taken over graph replays after each timed region
 
-    import grouped_query_attention_gemv_gb300 as G
-    from grouped_query_attention_gemv_gb300 import build
-    build.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+
+def measure(a, G, w, rank, world, local, dev, steps, warmup, replicas, full, shared_weights=None):
+    """Time one workload: `steps` steps replayed from CUDA graphs (device
+    time), a clock soak, per-kernel attribution and, with `full`, the
+    end-to-end timings with host buffers. Returns the fields of its line."""
     decode = w.T == 1
-    G.set_decode_fusion(a.decode_kernels == "fused")
-    G.set_decode_attention_split(a.attention_split)
-
     starts = w.start_positions().tolist()
     s_max = w.cache_rows()
-    gen, wt = I.draw_weights(w.dims, seed=w.seed)
+    if shared_weights is not None:
+        gen = torch.Generator().manual_seed(0)
+        gen.set_state(shared_weights[1])
+        wt_dev = shared_weights[0]
+    else:
+        gen, wt = I.draw_weights(w.dims, seed=w.seed)
+        wt_dev = {k: v.to(dev) for k, v in wt.items()}
     x0 = I.draw_x(gen, w.B, w.T)
     ck0, cv0 = I.draw_cache(w.B, s_max, starts, w.dims, seed=w.seed)
     nkv = w.n_kv_heads
@@ -397,13 +412,15 @@ def main():
     L = w.layers
     # a multi-layer step: one replica per layer (its own weights, cache and
     # workspace), chained; the working set (L x 150 MB) is far above L2
-    R = L if L > 1 else max(1, a.replicas)
+    R = L if L > 1 else max(1, replicas)
     max_start = max(starts)
     reps = []
-    for _ in range(R):
-        reps.append({**{k: v.to(dev) for k, v in wt.items()}, "x": x0.to(dev), "ck": ck0.to(dev), "cv": cv0.to(dev),
+    for r in range(R):
+        wr = wt_dev if r == 0 else {k: v.clone() for k, v in wt_dev.items()}
+        reps.append({**wr, "x": x0.to(dev), "ck": ck0.to(dev), "cv": cv0.to(dev),
                      "out": torch.empty_like(x0, device=dev),
                      "ws": G.make_workspace(w.B, w.T, max_start + w.T, dev)})
+    del ck0, cv0
     sp = torch.tensor(starts, dtype=torch.int32, device=dev)
     rope = G.rope_table(s_max, device=dev)
 
@@ -445,7 +462,7 @@ def main():
             G.prefill(r["x"], starts[0], r["wq"], r["wk"], r["wv"], r["wo"], rope, r["ck"], r["cv"],
                       out=r["out"], workspace=r["ws"])
 
-    for i in range(max(a.warmup, R)):
+    for i in range(max(warmup, R)):
         step(i)
     torch.cuda.synchronize()
     per_step_launches = G.last_launch_count() * L
@@ -474,7 +491,7 @@ def main():
                 step(i)
         return g
     g_full = capture(GS)
-    g_rest = capture(a.steps % GS) if a.steps % GS else None
+    g_rest = capture(steps % GS) if steps % GS else None
     g_full.replay()
     if g_rest is not None:
         g_rest.replay()
@@ -490,7 +507,7 @@ def main():
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks.mark("t0")
     e0.record(stream)
-    for i in range(a.steps // GS):
+    for i in range(steps // GS):
         g_full.replay()
     if g_rest is not None:
         g_rest.replay()
@@ -498,17 +515,28 @@ def main():
     torch.cuda.synchronize()
     clocks.mark("t1")
     _barrier(world)
+    # ---- clock soak: the same graphs replayed for SOAK_S under the sampler
+    # (a short timed region can fall between two samples)
+    clocks.mark("s0")
+    t_end = time.time() + SOAK_S
+    soak_replays = 0
+    while time.time() < t_end:
+        for _ in range(16):
+            g_full.replay()
+        soak_replays += 16
+        torch.cuda.synchronize()
+    clocks.mark("s1")
     time.sleep(0.1)
     clocks.stop()
     ms = _max_over_ranks(e0.elapsed_time(e1), world, dev)
-    ms_step = ms / a.steps
-    launches = per_step_launches * a.steps
+    ms_step = ms / steps
+    launches = per_step_launches * steps
     for r in reps:
         assert G.device_status(r["ws"]) == 0, "device status set during the timed steps"
 
     # ---- per-kernel attribution: events recorded by the library around each
     # kernel, with a device-side backlog so host gaps do not enter the intervals
-    ksteps = min(a.steps, 200)
+    ksteps = min(steps, 200)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)] for _ in range(ksteps)]
     for e4 in evs:          # torch only times events it has recorded once itself
         for e in e4:
@@ -522,10 +550,76 @@ def main():
     torch.cuda.synchronize()
     per_kernel = {k: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs) for j, k in enumerate(kernels)}
 
-    # ---- end to end with host buffers: pinned x in, delta out, copies inside
-    # the timed region. Two timings: serial through the device entry (torch
-    # copy in, step, torch copy out, one stream) and through the host-buffer
-    # entry
+    e2e = None
+    if full:
+        e2e = _end_to_end(a, G, w, step, in_buf, out_buf, x0, reps, R, L, layer, decode, sp, max_start, rope, nkv,
+                          starts, dev, world, stream, steps)
+    for r in reps:
+        assert G.device_status(r["ws"]) == 0, "device status set during the end-to-end steps"
+
+    hbm, tflops, peak_kind = load_peaks()
+    dom = max(per_kernel, key=per_kernel.get)
+    # the dominant kernel's duration: a one-kernel step takes its time per
+    # step inside the replayed graphs (no longer than the step); a step of
+    # several kernels takes the median of the events around the kernel
+    one_kernel = len(kernels) == 1 and L == 1
+    launch_ms = ms_step if one_kernel else per_kernel[dom]
+    if decode:
+        work = step_bytes(w.B, starts, kv_row)
+        if layer:  # the norm's x in and rows out, the residual's x in
+            work["step"] += 3 * w.B * 8192 + 8192
+        work["step"] *= L   # per-kernel figures stay per launch (one layer)
+        value = world * w.B * steps / (ms / 1e3)
+        unit = "seq-steps/s"
+        achieved = work[dom] / (launch_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": kernel_traffic(dom, w.name), "algorithmic_bytes_per_launch": work[dom],
+                "launch_ms": launch_ms, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind}: copy, read + write)",
+                "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS}
+        step_rate = {"step_hbm_gbs": work["step"] / (ms_step / 1e3) / 1e9}
+        step_rate["step_hbm_frac"] = step_rate["step_hbm_gbs"] / hbm
+    else:
+        work = step_flops(w.B, w.T, starts[0], kv_row)
+        value = world * work["step"] * steps / (ms / 1e3) / 1e12
+        unit = "TFLOP/s"
+        achieved = work[dom] / (launch_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+                "frac": achieved / tflops, "traffic": kernel_traffic(dom, w.name), "algorithmic_flops_per_launch": work[dom],
+                "launch_ms": launch_ms, "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({peak_kind}: cuBLAS burst)",
+                "nominal_peak": NOMINAL_BF16_TFLOPS, "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS}
+        step_rate = {"step_tflops": work["step"] / (ms_step / 1e3) / 1e12}
+        step_rate["step_tensor_frac"] = step_rate["step_tflops"] / tflops
+    roof["launch_ms_source"] = ("time per step inside the replayed graphs (one kernel per step)" if one_kernel else
+                                "median of events around the kernel's graph-free launches")
+    if one_kernel:
+        roof["launch_ms_graph_free"] = per_kernel[dom]
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) x and cache, N(0,1/4096) weights)",
+        "config": config_dict(w, a, starts, R), **step_rate, "peak_kind": peak_kind,
+        "roofline": roof,
+        "kernels_ms": per_kernel,
+        "gpu_launches": launches,
+        "timing": f"device region replays CUDA graphs of {GS} consecutive steps (the same C-ABI call captured, "
+                  f"replicas in turn); e2e calls the Python API per step",
+        "clocks": clocks.summary(soak_replays=soak_replays),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if L > 1:
+        line["timing"] += f"; a step chains {L} layer calls (one replica per layer), kernels_ms is one layer's launch"
+    del reps
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
+
+
+def _end_to_end(a, G, w, step, in_buf, out_buf, x0, reps, R, L, layer, decode, sp, max_start, rope, nkv, starts, dev,
+                world, stream, steps):
+    """End to end with host buffers: pinned x in, delta out, copies inside the
+    timed region. Two timings: serial through the device entry (torch copy
+    in, step, torch copy out, one stream) and through the host-buffer entry."""
     xh = x0.pin_memory()
     oh = torch.empty_like(x0).pin_memory()
     for i in range(min(a.warmup, 5)):
@@ -536,7 +630,7 @@ def main():
     torch.cuda.synchronize()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for i in range(a.steps):
+    for i in range(steps):
         in_buf(i).copy_(xh, non_blocking=True)
         step(i)
         oh.copy_(out_buf(i), non_blocking=True)
@@ -566,7 +660,7 @@ def main():
         _barrier(world)
         torch.cuda.synchronize()
         f0.record(stream)
-        for i in range(a.steps):
+        for i in range(steps):
             host_step(i)
         G.host_stage_wait(stage)   # the last read-backs are inside the region
         f1.record(stream)
@@ -574,70 +668,81 @@ def main():
         _barrier(world)
         ems = _max_over_ranks(f0.elapsed_time(f1), world, dev)
         G.release_host_stage(stage)
-    for r in reps:
-        assert G.device_status(r["ws"]) == 0, "device status set during the end-to-end steps"
-    if rank != 0:
+    if decode:
+        per = world * w.B * steps
+        unit = "seq-steps/s"
+        e2e_value, e2e_serial = per / (ems / 1e3), per / (ems_serial / 1e3)
+    else:
+        flops = world * step_flops(w.B, w.T, starts[0], w.n_kv_heads * 128)["step"] * steps
+        unit = "TFLOP/s"
+        e2e_value, e2e_serial = flops / (ems / 1e3) / 1e12, flops / (ems_serial / 1e3) / 1e12
+    return {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": x0.numel() * 2,
+            "d2h_bytes_per_step": x0.numel() * 2,
+            "call": ("the host-buffer C-ABI entry per step (gqa_decode_host / gqa_block_forward_host: "
+                     "uploads and read-backs on the library's copy streams, overlapping the neighbouring "
+                     "steps; joined by gqa_host_stage_wait before the end event)") if host_entry
+                    else "torch copies and the device entry per step, one stream",
+            "serial_value": e2e_serial}
+
+
+def main():
+    a = args_()
+    rank, world, local = dist_env()
+    w = I.workload(a.workload)
+    if a.oracle_sample is not None:   # the one-core leg of the CPU baseline (a child of cpu_baseline)
+        print(json.dumps(cpu_baseline(w, a.oracle_sample, one_core=False)))
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo" if a.impl == "reference" else "nccl")
+    if a.impl == "reference":
+        run_reference(a, w, rank, world)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
         return
 
-    hbm, tflops, peak_kind = load_peaks()
-    dom = max(per_kernel, key=per_kernel.get)
-    if decode:
-        work = step_bytes(w.B, starts, kv_row)
-        if layer:  # the norm's x in and rows out, the residual's x in
-            work["step"] += 3 * w.B * 8192 + 8192
-        work["step"] *= L   # per-kernel figures stay per launch (one layer)
-        value = world * w.B * a.steps / (ms / 1e3)
-        unit = "seq-steps/s"
-        e2e_value = world * w.B * a.steps / (ems / 1e3)
-        e2e_serial = world * w.B * a.steps / (ems_serial / 1e3)
-        achieved = work[dom] / (per_kernel[dom] / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": kernel_traffic(dom, w.name), "algorithmic_bytes_per_launch": work[dom],
-                "launch_ms": per_kernel[dom], "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}
-        step_rate = {"step_hbm_gbs": work["step"] / (ms_step / 1e3) / 1e9}
-        step_rate["step_hbm_frac"] = step_rate["step_hbm_gbs"] / hbm
-    else:
-        work = step_flops(w.B, w.T, starts[0], kv_row)
-        value = world * work["step"] * a.steps / (ms / 1e3) / 1e12
-        unit = "TFLOP/s"
-        e2e_value = world * work["step"] * a.steps / (ems / 1e3) / 1e12
-        e2e_serial = world * work["step"] * a.steps / (ems_serial / 1e3) / 1e12
-        achieved = work[dom] / (per_kernel[dom] / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
-                "frac": achieved / tflops, "traffic": kernel_traffic(dom, w.name), "algorithmic_flops_per_launch": work[dom],
-                "launch_ms": per_kernel[dom], "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({peak_kind})"}
-        step_rate = {"step_tflops": work["step"] / (ms_step / 1e3) / 1e12}
-        step_rate["step_tensor_frac"] = step_rate["step_tflops"] / tflops
-    line = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": a.steps,
-        "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) x and cache, N(0,1/4096) weights)",
-        "config": config_dict(w, a, starts), **step_rate, "peak_kind": peak_kind,
-        "roofline": roof,
-        "kernels_ms": per_kernel,
-        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": x0.numel() * 2,
-                "d2h_bytes_per_step": x0.numel() * 2,
-                "call": ("the host-buffer C-ABI entry per step (gqa_decode_host / gqa_block_forward_host: "
-                         "uploads and read-backs on the library's copy streams, overlapping the neighbouring "
-                         "steps; joined by gqa_host_stage_wait before the end event)") if host_entry
-                        else "torch copies and the device entry per step, one stream",
-                "serial_value": e2e_serial},
-        "gpu_launches": launches,
-        "timing": f"device region replays CUDA graphs of {GS} consecutive steps (the same C-ABI call captured, "
-                  f"replicas in turn); e2e calls the Python API per step",
-        "clocks": clocks.summary(),
-    }
-    if L > 1:
-        line["timing"] += f"; a step chains {L} layer calls (one replica per layer), kernels_ms is one layer's launch"
+    import grouped_query_attention_gemv_gb300 as G
+    from grouped_query_attention_gemv_gb300 import build
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    G.set_decode_fusion(a.decode_kernels == "fused")
+    G.set_decode_attention_split(a.attention_split)
+
+    # the seeded weights, drawn once; workloads of the same model share them
+    gen, wt = I.draw_weights(w.dims, seed=w.seed)
+    shared = ({k: v.to(dev) for k, v in wt.items()}, gen.get_state())
+    del wt
+    line = measure(a, G, w, rank, world, local, dev, a.steps, a.warmup, a.replicas, True, shared)
+    headline = w.name == args_default_workload() and a.entry == "block" and a.decode_kernels == "fused" \
+        and a.attention_split == "auto" and not a.no_workloads
+    if headline:
+        line["workloads"] = {}
+        for name, cap, reps in SECONDARY:
+            ws_ = I.workload(name)
+            n = min(a.steps, cap)
+            sub = measure(a, G, ws_, rank, world, local, dev, n, min(a.warmup, 5), reps, False,
+                          shared if ws_.dims == w.dims and ws_.seed == w.seed else None)
+            keep = ("value", "unit", "ms_per_step", "steps", "warmup", "roofline", "clocks", "config", "gpu_launches",
+                    "kernels_ms", "step_hbm_gbs", "step_hbm_frac", "step_tflops", "step_tensor_frac")
+            line["workloads"][name] = {k: sub[k] for k in keep if k in sub}
+            line["workloads"][name]["step_cap"] = cap
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     if not a.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def args_default_workload() -> str:
+    return "decode_b16_p1000"
 
 
 if __name__ == "__main__":

@@ -27,7 +27,7 @@ __all__ = [
     "GQAError", "D_MODEL", "N_HEADS", "N_KV_HEADS", "HEAD_DIM", "library_path", "lib",
     "exported_symbols", "workspace_bytes", "make_workspace", "rope_table", "block_forward",
     "decode", "prefill", "device_status", "last_launch_count", "set_profile_events",
-    "set_decode_fusion", "set_decode_attention_split", "decode_static", "rms_norm", "layer_forward", "layer_decode", "static_device_status",
+    "set_decode_fusion", "set_decode_attention_split", "set_wait_limit_ns", "decode_static", "rms_norm", "layer_forward", "layer_decode", "static_device_status",
     "STATIC_SCRATCH_BYTES", "make_host_stage", "default_host_stage", "host_stage_wait", "release_host_stage",
     "decode_host",
     "block_forward_host",
@@ -67,6 +67,7 @@ _SIGNATURES = {
     "gqa_last_launch_count": (_i, []),
     "gqa_set_decode_fusion": (_i, [_i]),
     "gqa_set_decode_attention_split": (_i, [_i]),
+    "gqa_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
     "gqa_set_profile_events": (_i, [ctypes.POINTER(_vp), _i]),
     "gqa_decode_static": (_i, [_vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp]),
     "gqa_static_device_status": (_i, [ctypes.POINTER(_i), _i]),
@@ -316,6 +317,14 @@ def set_decode_fusion(enable: bool) -> bool:
     persistent kernel (True, the default) or as three kernels (False).
     Returns the previous setting."""
     return bool(lib().gqa_set_decode_fusion(1 if enable else 0))
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit (ns) of the decode kernels' grid-wide waits on this thread; 0
+    restores the default (2 s). Returns the previous limit."""
+    if ns < 0:
+        raise ValueError("the wait limit is a non-negative number of nanoseconds")
+    return int(lib().gqa_set_wait_limit_ns(int(ns)))
 
 
 _SPLITS = {"auto": 0, "position": 1, "head": 2}

@@ -18,6 +18,7 @@ thread_local void* const* t_prof_events = nullptr;
 thread_local int t_prof_count = 0;
 thread_local int t_fused = 1;
 thread_local int t_attn_split = 0;  // fused decode attention: 0 chosen per call, 1 position-major, 2 head-major
+thread_local unsigned long long t_wait_ns = WAIT_LIMIT_NS;  // grid-wide waits of the decode kernels
 
 thread_local int t_prof_base = 0;  // 1 while a layer call's norm kernel occupies events[0..1]
 void prof_mark(int i, cudaStream_t s) {
@@ -328,6 +329,7 @@ DecodeAttnParams decode_attn_params(const Call& c) {
   a.cache_k = reinterpret_cast<const __nv_bfloat16*>(c.cache_k);
   a.cache_v = reinterpret_cast<const __nv_bfloat16*>(c.cache_v);
   a.s_max = c.s_max;
+  a.wait_ns = t_wait_ns;
   return a;
 }
 
@@ -723,6 +725,12 @@ int gqa_last_launch_count(void) { return t_launches; }
 int gqa_set_decode_fusion(int enable) {
   const int prev = t_fused;
   t_fused = enable ? 1 : 0;
+  return prev;
+}
+
+unsigned long long gqa_set_wait_limit_ns(unsigned long long ns) {
+  const unsigned long long prev = t_wait_ns;
+  t_wait_ns = ns ? ns : WAIT_LIMIT_NS;
   return prev;
 }
 

@@ -581,7 +581,7 @@ __device__ __forceinline__ bool attn_merge(const DecodeAttnParams& a, const Shar
   }
   if (threadIdx.x == 0) {
     atomicAdd(meet, 1);
-    flags[3] = wait_counter(meet, static_cast<int>(C)) ? 1 : 0;
+    flags[3] = wait_counter(meet, static_cast<int>(C), a.wait_ns) ? 1 : 0;
   }
   asm volatile("bar.sync 2, 256;" ::: "memory");
   if (!all_ok || flags[3] == 0) {

@@ -182,6 +182,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// mbar_wait that also gives up (false) as soon as *abort, a shared-memory
+// flag a producer raises when it stops issuing, becomes non-zero: consumers
+// then leave a phase whose loads will not come without waiting out the limit.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, const int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*reinterpret_cast<const volatile int*>(abort) || global_ns() - t0 > WAIT_LIMIT_NS) return false;
+  }
+  return true;
+}
+
 // ----------------------------------------------------------------- grid-level ordering
 // Programmatic dependent launch: wait for the predecessor grid / let the
 // dependent grid start launching.
@@ -216,12 +228,14 @@ __device__ __forceinline__ int wait_flag_cta(const int* flag) {
   return v;
 }
 
-// false after WAIT_LIMIT_NS.
-__device__ __forceinline__ bool wait_counter(const int* counter, int target) {
+// false after limit_ns (the grid-wide waits take the caller's limit, see
+// gqa_set_wait_limit_ns).
+__device__ __forceinline__ bool wait_counter(const int* counter, int target,
+                                             unsigned long long limit_ns = WAIT_LIMIT_NS) {
   if (ld_acquire(counter) >= target) return true;
   const unsigned long long t0 = global_ns();
   while (ld_acquire(counter) < target) {
-    if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
+    if (global_ns() - t0 > limit_ns) return false;
     __nanosleep(32);
   }
   return true;

@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   if (!aborted) {
     // one poller per CTA: the producer lane waits on the grid counter and
     // hands the outcome to the compute warps through shared memory
-    auto gate_lane = [cnt, grid, flags_b]() {
-      const bool ok = wait_counter(&cnt[0], grid);
+    auto gate_lane = [cnt, grid, flags_b, &fp]() {
+      const bool ok = wait_counter(&cnt[0], grid, fp.at.wait_ns);
       fence_proxy_async_global();  // the new K/V rows were written by plain stores
       st_release_cta(&flags_b[1], ok ? 1 : 2);
       return ok;
@@ -220,8 +220,8 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
     }
   } else if (!aborted) {
     rowsk::rows_phase<CfgC<NP>, false>(m.o, fp.po, fp.o_plan, shc,
-                                       [cnt, grid]() {
-                                         const bool ok = wait_counter(&cnt[1], grid);
+                                       [cnt, grid, &fp]() {
+                                         const bool ok = wait_counter(&cnt[1], grid, fp.at.wait_ns);
                                          fence_proxy_async_global();  // o was written by plain stores
                                          return ok;
                                        },

@@ -159,6 +159,7 @@ struct DecodeAttnParams {
   const __nv_bfloat16* cache_k;  // [B][s_max][n_kv][128], for L2 prefetches only
   const __nv_bfloat16* cache_v;
   int s_max;
+  unsigned long long wait_ns;    // limit of the grid-wide waits (the meeting; the fused grid's gates)
 };
 int attn_decode_ctas(int num_sms);
 int attn_decode_slots(int ctas);   // (CTA, first or last stretch, KV head) partial slots

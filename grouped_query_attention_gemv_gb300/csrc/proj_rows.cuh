@@ -200,13 +200,13 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     if (started == 0) tma_prefetch_desc(wmap);
     int i = started;
     for (; i < NST; ++i) {
-      if (i >= S && !mbar_wait(smem_u32(&sh.empty[i % S]), ((i / S) & 1) ^ 1)) {
+      if (i >= S && !mbar_wait_or_abort(smem_u32(&sh.empty[i % S]), ((i / S) & 1) ^ 1, &flags[0])) {
         atomicExch(&flags[0], 1);
         break;
       }
       // at most INFL stages in flight: stage i - INFL must have landed
       if (i >= C_::INFL && C_::INFL < S &&
-          !mbar_wait(smem_u32(&sh.full[(i - C_::INFL) % S]), ((i - C_::INFL) / S) & 1)) {
+          !mbar_wait_or_abort(smem_u32(&sh.full[(i - C_::INFL) % S]), ((i - C_::INFL) / S) & 1, &flags[0])) {
         atomicExch(&flags[0], 1);
         break;
       }
@@ -225,7 +225,7 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     bool ok = gate();
     int i = started;
     for (; ok && i < NST; ++i) {
-      if (i >= XS && !mbar_wait(smem_u32(&sh.xempty[i % XS]), ((i / XS) & 1) ^ 1)) {
+      if (i >= XS && !mbar_wait_or_abort(smem_u32(&sh.xempty[i % XS]), ((i / XS) & 1) ^ 1, &flags[0])) {
         ok = false;
         break;
       }
@@ -336,8 +336,8 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     for (int j = 0; j < NG; ++j) gcur[j] = gnext[j];
     if (norm && i + 1 < NST) load_g(i + 1, gnext);
     const int s = i % S, xs = i % XS;
-    bool landed = mbar_wait(smem_u32(&sh.full[s]), (i / S) & 1);
-    landed = landed && mbar_wait(smem_u32(&sh.xfull[xs]), (i / XS) & 1);
+    bool landed = mbar_wait_or_abort(smem_u32(&sh.full[s]), (i / S) & 1, &flags[0]);
+    landed = landed && mbar_wait_or_abort(smem_u32(&sh.xfull[xs]), (i / XS) & 1, &flags[0]);
     if (!__all_sync(0xffffffffu, landed)) {
       if (lane == 0) atomicExch(&flags[0], 1);
       ok = false;

@@ -240,6 +240,18 @@ int gqa_set_decode_fusion(int enable);
  * the previous setting, or -1 (nothing changed) for another value. */
 int gqa_set_decode_attention_split(int mode);
 
+/* Limit, for calls made on the calling thread, of the grid-wide waits of the
+ * decode kernels: the one-kernel step's two gates (every CTA's Q|K|V rows
+ * published; every attention output published) and the attention's meeting
+ * before its merges. A wait that runs out records GQA_DEV_WAIT_TIMEOUT in the
+ * workspace status word; the kernel then skips the work that needed the
+ * wait, lets its own loads land, leaves the grid counters reset and exits
+ * (the call's output is unspecified). ns = 0 restores the default of 2 s
+ * (2,000,000,000 ns). Returns the previous limit. Meant for tests and for
+ * callers that prefer a fast error over a long stall; the waits on the
+ * kernels' own data loads keep their 2 s limit. */
+unsigned long long gqa_set_wait_limit_ns(unsigned long long ns);
+
 /* Measurement hook; it changes nothing the block computes. While set, every
  * block call on the calling thread records events[0] on its stream before its
  * first kernel and events[i] right after its i-th kernel (for i < count), so

@@ -50,3 +50,27 @@ def test_workloads_match_their_descriptions():
     assert w.B == 64 and int(p.min()) >= 512 and int(p.max()) <= 32768
     assert I.workload("mha_decode_b16_p1000").dims.n_kv_heads == 32
     assert I.workload("decode32_b16_p1000").layers == 32
+
+
+def test_headline_line_carries_every_other_configuration():
+    """The headline (B=16 at 1,001 keys) and the five secondary workloads are
+    the benchmark's six configurations: B=1 at 16 keys, the batched decode,
+    the two prefills and the long-context decode."""
+    names = [n for n, _, _ in bench.SECONDARY]
+    assert bench.args_default_workload() == "decode_b16_p1000"
+    assert sorted(names) == sorted(["decode_b1_p15", "batched_decode_b64_p512_32768", "long_decode_b8_p131071",
+                                    "prefill_b1_t2048", "prefill_b4_t2048"])
+    assert all(cap > 0 and reps >= 1 for _, cap, reps in bench.SECONDARY)
+
+
+def test_clock_summary_falls_back_to_the_soak():
+    c = bench.ClockSampler(0)
+    row = "0, {mhz}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, {cap}"
+    c.rows = [(1.0, row.format(mhz=1500, cap="Not Active")), (5.0, row.format(mhz=2070, cap="Active")),
+              (5.5, row.format(mhz=2060, cap="Not Active"))]
+    c.t0, c.t1, c.s0, c.s1 = 2.0, 2.001, 4.9, 6.0     # no sample inside a 1 ms timed region
+    s = c.summary(soak_replays=64)
+    assert s["samples_in_timed_region"] == 0 and s["source"] == "soak"
+    assert s["sm_mhz"] == 2065 and s["soak"]["samples"] == 2 and s["reasons"] == ["sw_power_cap"]
+    c.t0, c.t1 = 0.5, 1.5
+    assert c.summary()["source"] == "timed region" and c.summary()["sm_mhz"] == 1500

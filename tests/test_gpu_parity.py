@@ -235,6 +235,71 @@ def test_decode_split_setting_is_validated():
         G.set_decode_attention_split("rows")
 
 
+class wait_limit:
+    """Limit of the decode kernels' grid-wide waits inside the with-block."""
+
+    def __init__(self, ns):
+        self.ns = ns
+
+    def __enter__(self):
+        self.prev = G.set_wait_limit_ns(self.ns)
+
+    def __exit__(self, *exc):
+        G.set_wait_limit_ns(self.prev)
+
+
+COUNTERS = 16   # byte offset of the grid counters in the workspace's status region
+
+
+@pytest.mark.parametrize("path,split,counter", [
+    ("fused", "head", 0),        # the Q|K|V gate of the one-kernel step
+    ("fused", "head", 1),        # the W_O gate
+    ("fused", "position", 0),
+    ("fused", "position", 3),    # the attention's meeting before its merges
+    ("three", "auto", 0),        # the standalone attention kernel's meeting
+])
+def test_grid_wait_timeout_is_reported_and_recovered(weights, path, split, counter):
+    """Failure injected on the host: a grid counter in the workspace is set so
+    far below its target that the wait on it cannot finish. With a 1 ms limit
+    the call must end, record GQA_DEV_WAIT_TIMEOUT, leave every grid counter
+    reset and every cache row outside the new ones untouched; the next call
+    on the same workspace must pass parity."""
+    c = H.make_case(3, 1, [1000, 517, 64], 1100, weights=weights)   # sequences split between CTAs
+    d = c.dev
+    sp = torch.tensor(c.start, dtype=torch.int32, device="cuda")
+    ws = G.make_workspace(3, 1, 1001)
+    counters = ws[COUNTERS:COUNTERS + 16].view(torch.int32)
+    counters[counter] = -(1 << 30)
+    prev = G.set_decode_fusion(path == "fused")
+    try:
+        with attention_split(split), wait_limit(1_000_000):
+            G.decode(d["x"], sp, 1000, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"],
+                     workspace=ws)
+            torch.cuda.synchronize()
+        assert G.device_status(ws, clear=True) == 2      # GQA_DEV_WAIT_TIMEOUT
+        assert int(counters.abs().sum()) == 0, f"grid counters left {counters.tolist()}"
+        H.check_canaries(c)
+        # the same step again on the untouched cache, default limit: parity
+        d["cache_k"].copy_(d["cache_k0"])
+        d["cache_v"].copy_(d["cache_v0"])
+        with attention_split(split):
+            out, _ = run_decode(c, ws=ws)
+    finally:
+        G.set_decode_fusion(prev)
+    for b in range(3):
+        H.compare_sequence(c, out, b)
+    H.check_canaries(c)
+
+
+def test_wait_limit_setting_round_trips():
+    prev = G.set_wait_limit_ns(5_000_000)
+    try:
+        assert G.set_wait_limit_ns(0) == 5_000_000
+        assert G.set_wait_limit_ns(prev) == 2_000_000_000   # 0 restored the default
+    finally:
+        G.set_wait_limit_ns(prev)
+
+
 def test_block_forward_decode_matches_oracle(weights):
     c = H.make_case(4, 1, [37, 37, 37, 37], 40, weights=weights)
     d = c.dev
