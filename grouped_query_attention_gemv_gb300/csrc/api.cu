@@ -405,12 +405,13 @@ int run_attention(const Call& c) {
 // Tensor maps of a row-owner projection: per matrix, boxes of its two row
 // counts; the token rows x (M of them), boxes of np rows.
 bool row_maps(const gqa_bf16* const* w, const RowPlan& plan, const void* x, int M, int np, RowMaps* m) {
+  const int kc = rows_kc(np);
   for (int i = 0; i < 3; ++i) {
     const int mi = i < plan.nmat ? i : 0;
     for (int hi = 0; hi < 2; ++hi)
-      if (!map_rows_kblocks(&m->w[i][hi], w[mi], plan.rows[mi], plan.h_lo[mi] + 2 * hi, 4)) return false;
+      if (!map_rows_kblocks(&m->w[i][hi], w[mi], plan.rows[mi], plan.h_lo[mi] + 2 * hi, kc)) return false;
   }
-  return np > 0 && map_rows_kblocks(&m->x, x, M, np, 4);
+  return np > 0 && map_rows_kblocks(&m->x, x, M, np, kc);
 }
 
 // Work split of the fused grid's attention for one call. Head-major (one

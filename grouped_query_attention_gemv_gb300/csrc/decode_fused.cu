@@ -87,12 +87,12 @@ struct FusedParams {
 // become ready at the gate: a deep token ring (128 KB at 16 tokens).
 // (Asking L2 for the rest of W_O at the same time measured 1.5 us slower per
 // step at B = 16: the requests queue ahead of the merge and the gate.)
-// Both keep 4 weight stages in flight per SM (about 13 MB over the grid,
-// 2 us of HBM time).
+// Both keep about 85 KB of weight stages in flight per SM (13 MB over the
+// grid, 2 us of HBM time).
 template <int NP>
 using CfgA = rowsk::Cfg<NP>;
 template <int NP>
-using CfgC = rowsk::Cfg<NP, NP <= 16 ? 16 : (NP == 32 ? 8 : 3)>;
+using CfgC = rowsk::Cfg<NP, NP <= 16 ? 8 : (NP == 32 ? 4 : 3)>;
 
 template <int NP>
 struct Layout {

@@ -199,10 +199,14 @@ struct RowPlan {
   int h_lo[3];
 };
 constexpr int ROWS_MAX_H = 48;   // rows one CTA can own (3 row tiles of 16)
+// k blocks of 64 per stage of the row-owner projections for np padded tokens
+// (8; 4 at 64 tokens, where the warps split the tokens): the weight and token
+// boxes of the fused grid's tensor maps hold this many k blocks.
+__host__ __device__ constexpr int rows_kc(int np) { return np <= 32 ? 8 : 4; }
 // Tensor maps over (64 k, row, k block) views of the weight matrices:
 // w[i][0] / w[i][1] are matrix i with boxes of 64 x h_lo[i] (or h_lo[i] + 2)
-// rows x 4 k blocks; x is the same view of the M token rows with boxes of 64 x
-// NP tokens x 4 k blocks (NP = decode_fused_np(M)).
+// rows x rows_kc(NP) k blocks; x is the same view of the M token rows with
+// boxes of 64 x NP tokens x rows_kc(NP) k blocks (NP = decode_fused_np(M)).
 struct RowMaps {
   CUtensorMap w[3][2];
   CUtensorMap x;

@@ -51,31 +51,36 @@ namespace rowsk {
 
 constexpr int KBLK = 64;
 constexpr int NKB = D_MODEL / KBLK;      // 64 k blocks
-constexpr int KC = 4;                    // k blocks per stage (= k-block groups of warps)
-constexpr int NST = NKB / KC;            // 16 stages per CTA
 constexpr int MT_MAX = ROWS_MAX_H / 16;  // row tiles of 16
 constexpr int WARPS = 8;                 // compute warps 0-7; warp 8 lane 0 loads W, warp 9 lane 0 loads x
 constexpr int MAX_STAGES = 12;           // weight stages (barrier pairs)
 constexpr int RING_BYTES = 216 * 1024;   // weight ring + token ring
 constexpr int OVERREAD = 1024;           // the last row tile may read up to 15 rows past a stage
 
-constexpr int XS_MAX = NST;              // token stages at most (all of a phase's tokens)
+constexpr int XS_MAX = 16;               // token stages at most (all of a phase's tokens)
 
-// NP padded tokens; XS token stages in flight. A phase whose weights come
-// from HBM wants most of shared memory for them (few token stages); one whose
-// weights are already in L2 but whose tokens only become ready when it starts
-// wants the tokens in flight instead. INFL: weight stages requested but not
-// yet landed, at most (the ring may hold more landed ones): with every SM
-// streaming, 4 stages keep HBM busy, and each SM's reads and counter polls
-// queue behind what it has in flight, so more only adds latency.
-template <int NP_, int XS_ = (NP_ <= 16 ? 4 : (NP_ == 32 ? 3 : 2)), int INFL_ = 4>
+// NP padded tokens; KC k blocks per stage (rows_kc: 8, or 4 at 64 tokens,
+// whose warps split the tokens); XS token stages in flight (0: the default,
+// 2). A phase whose weights come from HBM wants most of shared memory for
+// them (few token stages); one whose weights are already in L2 but whose
+// tokens only become ready when it starts wants the tokens in flight
+// instead. INFL: weight stages requested but not yet landed, at most (the
+// ring may hold more landed ones): with every SM streaming, ~85 KB a SM keep
+// HBM busy, and each SM's reads and counter polls queue behind what it has
+// in flight, so more only adds latency. Stages of 8 k blocks halve the
+// per-stage cost every warp pays (a barrier wait and an arrive for the
+// weights and for the tokens, ~0.25 us a stage).
+template <int NP_, int XS_ = 0, int INFL_ = 0>
 struct Cfg {
   static constexpr int NP = NP_;
-  static constexpr int INFL = INFL_;
+  static constexpr int KC = rows_kc(NP_);
+  static constexpr int NST = NKB / KC;              // stages per CTA
+  static constexpr int INFL = INFL_ ? INFL_ : 4 * KBLK * 4 / (KC * KBLK);  // ~4 stages of 4 k blocks
   static constexpr int B_BYTES = NP * KBLK * 2;      // one k block of the token tile
   static constexpr int X_STAGE = KC * B_BYTES;       // the token rows of one weight stage
-  static constexpr int XS = XS_;                     // token stages
-  static_assert(XS >= 1 && XS <= XS_MAX, "token stages");
+  static constexpr int XS = XS_ ? XS_ : 2;           // token stages
+  static_assert(XS >= 1 && XS <= XS_MAX && XS <= NST, "token stages");
+  static_assert(KC * (WARPS / KC) == WARPS || KC == WARPS, "warps per k block");
   static constexpr int X_RING = XS * X_STAGE;
   static constexpr int W_RING = RING_BYTES - X_RING;
   static constexpr bool TOKEN_SPLIT = NP > 32;      // warps split the tokens (else the k of a block)
@@ -84,12 +89,12 @@ struct Cfg {
   static_assert(RED_BYTES <= W_RING, "the reduction fits in the weight ring");
 };
 
-// Weight stage: 4 k blocks of the phase's largest row count, rounded up to
+// Weight stage: kc k blocks of the phase's largest row count, rounded up to
 // whole 1 KB swizzle atoms (so that every stage starts 1024-byte aligned).
-__device__ __forceinline__ int wstage_bytes(const RowPlan& plan) {
+__device__ __forceinline__ int wstage_bytes(const RowPlan& plan, int kc) {
   int hmax = 0;
   for (int i = 0; i < plan.nmat; ++i) hmax = max(hmax, plan.h_lo[i] + 2);
-  return ((KC * hmax * 128 + 1023) / 1024) * 1024;
+  return ((kc * hmax * 128 + 1023) / 1024) * 1024;
 }
 
 // This CTA's rows: matrix `mat`, rows [row0, row0 + h), map index hi (0: h_lo, 1: h_lo + 2).
@@ -130,23 +135,25 @@ struct Shared {
 };
 
 // One weight stage (i-th of this CTA's walk) into ring slot i % S.
+template <class C_>
 __device__ __forceinline__ void issue_w_stage(const CUtensorMap* wmap, const Shared& sh, int i, int S, int wstage,
                                               const MyRows& mr, int rot) {
-  const int s = i % S, ks = (i + rot) % NST;
+  const int s = i % S, ks = (i + rot) % C_::NST;
   const uint32_t fb = smem_u32(&sh.full[s]);
-  mbar_expect_tx(fb, KC * mr.h * 128);
-  tma_load_3d_stream(smem_u32(sh.ring + s * wstage), wmap, fb, 0, mr.row0, ks * KC, l2_evict_first());
+  mbar_expect_tx(fb, C_::KC * mr.h * 128);
+  tma_load_3d_stream(smem_u32(sh.ring + s * wstage), wmap, fb, 0, mr.row0, ks * C_::KC, l2_evict_first());
 }
 // The token rows of stage i into token slot i % XS.
 template <class C_>
 __device__ __forceinline__ void issue_x_stage(const CUtensorMap* xmap, const Shared& sh, int i, int rot) {
-  const int s = i % C_::XS, ks = (i + rot) % NST;
+  const int s = i % C_::XS, ks = (i + rot) % C_::NST;
   const uint32_t fb = smem_u32(&sh.xfull[s]);
   mbar_expect_tx(fb, C_::X_STAGE);
-  tma_load_3d(smem_u32(sh.ring + C_::W_RING + s * C_::X_STAGE), xmap, fb, 0, 0, ks * KC);
+  tma_load_3d(smem_u32(sh.ring + C_::W_RING + s * C_::X_STAGE), xmap, fb, 0, 0, ks * C_::KC);
 }
-__device__ __forceinline__ int ring_stages(int w_ring, const RowPlan& plan) {
-  return min(MAX_STAGES, (w_ring - OVERREAD) / wstage_bytes(plan));
+template <class C_>
+__device__ __forceinline__ int ring_stages(const RowPlan& plan) {
+  return min(MAX_STAGES, (C_::W_RING - OVERREAD) / wstage_bytes(plan, C_::KC));
 }
 
 // Starts a phase's streams before the rest of the CTA is ready, for a phase
@@ -157,11 +164,12 @@ __device__ __forceinline__ int ring_stages(int w_ring, const RowPlan& plan) {
 template <class C_>
 __device__ __forceinline__ int rows_start(const RowMaps& maps, const RowPlan& plan, const Shared& sh) {
   const MyRows mr = my_rows(plan, blockIdx.x);
-  const int rot = (blockIdx.x * 7) % NST;
+  const int rot = (blockIdx.x * 7) % C_::NST;
   if ((threadIdx.x >> 5) == WARPS) {
-    const int S = ring_stages(C_::W_RING, plan);
+    const int S = ring_stages<C_>(plan);
     const int D = min(S, C_::INFL);
-    for (int i = 0; i < D; ++i) issue_w_stage(&maps.w[mr.mat][mr.hi], sh, i, S, wstage_bytes(plan), mr, rot);
+    for (int i = 0; i < D; ++i)
+      issue_w_stage<C_>(&maps.w[mr.mat][mr.hi], sh, i, S, wstage_bytes(plan, C_::KC), mr, rot);
     return D;
   }
   for (int i = 0; i < C_::XS; ++i) issue_x_stage<C_>(&maps.x, sh, i, rot);
@@ -186,10 +194,11 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
   constexpr int NP = C_::NP;
   constexpr int XS = C_::XS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int NST = C_::NST, KC = C_::KC;
   const MyRows mr = my_rows(plan, blockIdx.x);
   const int rot = (blockIdx.x * 7) % NST;  // this CTA's first k stage
-  const int wstage = wstage_bytes(plan);
-  const int S = ring_stages(C_::W_RING, plan);
+  const int wstage = wstage_bytes(plan, KC);
+  const int S = ring_stages<C_>(plan);
   uint8_t* const xring = sh.ring + C_::W_RING;
   int* flags = sh.flags;
 
@@ -210,7 +219,7 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
         atomicExch(&flags[0], 1);
         break;
       }
-      issue_w_stage(wmap, sh, i, S, wstage, mr, rot);
+      issue_w_stage<C_>(wmap, sh, i, S, wstage, mr, rot);
     }
     flags[2] = i;
     if (i == NST) w_issued();
@@ -240,8 +249,8 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
   // ---------------- compute warps: k block kb of every stage; k16 steps [ks0, ks0 + KS) of it and
   // tokens [tok0, tok0 + 8 NT)
   const int kb = warp & (KC - 1);
-  constexpr int KS = C_::TOKEN_SPLIT ? 4 : 2;
-  const int ks0 = C_::TOKEN_SPLIT ? 0 : 2 * (warp / KC);
+  constexpr int KS = C_::TOKEN_SPLIT ? 4 : 4 * KC / WARPS;
+  const int ks0 = C_::TOKEN_SPLIT ? 0 : KS * (warp / KC);
   const int tok0 = C_::TOKEN_SPLIT ? (warp / KC) * (NP / 2) : 0;
   const int mtc = (mr.h + 15) >> 4;  // row tiles holding this CTA's rows
   // With few tokens the two k16 halves of a stage accumulate separately
@@ -493,7 +502,7 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
 template <class C_>
 __device__ __forceinline__ void rows_drain(const Shared& sh, const RowPlan& plan) {
   constexpr int XS = C_::XS;
-  const int S = ring_stages(C_::W_RING, plan);
+  const int S = ring_stages<C_>(plan);
   for (int i = max(0, sh.flags[2] - S); i < sh.flags[2]; ++i) mbar_wait(smem_u32(&sh.full[i % S]), (i / S) & 1);
   for (int i = max(0, sh.flags[3] - XS); i < sh.flags[3]; ++i) mbar_wait(smem_u32(&sh.xfull[i % XS]), (i / XS) & 1);
 }
