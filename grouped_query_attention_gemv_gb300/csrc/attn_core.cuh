@@ -544,9 +544,10 @@ __device__ __forceinline__ bool attn_items(const CUtensorMap& mk, const CUtensor
     *reinterpret_cast<uint32_t*>(a.o + static_cast<size_t>(b) * D_MODEL + static_cast<size_t>(g * N_REP + hh) * HEAD_DIM +
                                  d2) = pack_bf16(o0 * inv, o1 * inv);
   }
-  // its output is out (a later phase of the same grid reads o by TMA)
+  // its output is out: a later phase of the same grid reads o by TMA, after
+  // the caller's release on one thread behind a CTA barrier (it covers every
+  // thread's stores; see the caller)
   fence_proxy_async_global();
-  __threadfence();
   return ok;
 }
 

@@ -240,8 +240,10 @@ __device__ __forceinline__ bool wait_counter(const int* counter, int target,
   }
   return true;
 }
-// Publish: writes before this call (by the calling thread) are visible to a
-// thread that observes the increment with ld_acquire.
+// Publish: writes that happen before this call (the calling thread's, and
+// those of other threads of the CTA ordered before it by a CTA barrier: the
+// release is cumulative) are visible to a thread that observes the increment
+// with ld_acquire.
 __device__ __forceinline__ void signal_counter(int* counter, int add) {
   __threadfence();
   atomicAdd(counter, add);

@@ -199,9 +199,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
     fence_proxy_async_smem();  // ldmatrix reads of the ring precede phase C's TMA writes into it
   }
   __syncthreads();
-  // Head-major outputs are complete and fenced: publish them before phase C's
-  // weight loads are in flight, because a release on an SM waits for the
-  // bulk loads that SM has in flight (~1.5 us more when W_O's stages are out).
+  // Head-major outputs are complete: publish them (thread 0's release after
+  // the barrier covers every thread's stores) before phase C's weight loads
+  // are in flight, because a release on an SM waits for the bulk loads that
+  // SM has in flight (~1.5 us more when W_O's stages are out).
   const bool early_signal = fp.head_major && !aborted;
   if (early_signal) {
     if (threadIdx.x == 0) signal_counter(&cnt[1], 1);

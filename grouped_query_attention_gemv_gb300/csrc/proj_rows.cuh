@@ -487,12 +487,12 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     }
     item(idx, pos, cs);
   }
-  if constexpr (QKV) {
-    // later phases of the grid read these rows by TMA; the W_O phase is the
-    // grid's last, and its rows are only read after the kernel boundary
-    fence_proxy_async_global();
-    __threadfence();
-  }
+  // later phases of the grid read the Q|K|V rows by TMA (the W_O phase is
+  // the grid's last: its rows are only read after the kernel boundary). The
+  // rows reach other CTAs through rows_done's release on thread 0 after the
+  // barrier, which covers every thread's stores before it; a full fence per
+  // thread would wait for each thread's own stores (~0.5 us) for nothing
+  if constexpr (QKV) fence_proxy_async_global();
   asm volatile("bar.sync 4, 256;" ::: "memory");
   if (threadIdx.x == 0) rows_done();
 }
