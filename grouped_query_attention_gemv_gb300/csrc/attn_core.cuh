@@ -422,6 +422,55 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
 // `gate_lane`. Roles, gates and the return value as in attn_units; the
 // standalone kernel does not use this phase (its queries are ready at launch
 // and its batches are larger).
+// Stage i occupies ring slot (i + ITEM_ROT) % STAGES: the first stages then
+// lie past the ring's first slot, which a preceding projection phase still
+// uses for its cross-warp sums after its last weight stage is consumed, so
+// attn_items_early can request them during that phase's epilogue. One stage
+// (64 KB) lands within the epilogue; a second is still in flight when the
+// epilogue publishes its rows, and that release waits for the SM's loads
+// (B = 16 at 500-2,000 keys: 0.9 us saved with one, 0.5 us with two).
+constexpr int ITEM_ROT = 1;
+constexpr int EARLY_ITEMS = 1;
+static_assert(EARLY_ITEMS + ITEM_ROT <= STAGES, "early stages fit past the first slot");
+__device__ __forceinline__ int item_slot(int i) { return (i + ITEM_ROT) % STAGES; }
+
+// One head-major stage: positions i*ITEM_POS .. +127 of KV head g of sequence
+// b, K and V, into its ring slot (producer lane).
+__device__ __forceinline__ void item_issue(const CUtensorMap& mk, const CUtensorMap& mv, const Shared& sh, int b,
+                                           int g, int i) {
+  const int s = item_slot(i);
+  const uint32_t dst = smem_u32(sh.ring + s * UNIT_BYTES);
+  const uint32_t fb = smem_u32(&sh.full[s]);
+  const int pos = i * ITEM_POS;
+  const uint64_t pol = l2_evict_first();
+  mbar_expect_tx(fb, UNIT_BYTES);
+  tma_load_4d_stream(dst, &mk, fb, 0, g, pos, b, pol);
+  tma_load_4d_stream(dst + BOX_BYTES, &mk, fb, 64, g, pos, b, pol);
+  tma_load_4d_stream(dst + 2 * BOX_BYTES, &mv, fb, 0, g, pos, b, pol);
+  tma_load_4d_stream(dst + 3 * BOX_BYTES, &mv, fb, 64, g, pos, b, pol);
+}
+
+// Requests this CTA's first head-major stages (at most EARLY_ITEMS, none
+// holding position P_b) before phase B: called by the producer lane once the
+// ring's slots past the first are free (every stage of the preceding phase
+// consumed, no load of it in flight). Records the count in sh.flags[2], where
+// attn_items (same lane) continues and attn_drain looks. Returns the count.
+__device__ __forceinline__ int attn_items_early(const CUtensorMap& mk, const CUtensorMap& mv,
+                                                const DecodeAttnParams& a, const Shared& sh) {
+  const int item = blockIdx.x;
+  if (item >= a.B * N_KV) return 0;
+  const int b = item / N_KV, g = item % N_KV;
+  const int P = a.sp.get(b);
+  if (!a.sp.ok(P)) return 0;
+  const int n = (P + 1 + ITEM_POS - 1) / ITEM_POS;
+  tma_prefetch_desc(&mk);
+  tma_prefetch_desc(&mv);
+  int i = 0;
+  while (i + 1 < n && i < EARLY_ITEMS) item_issue(mk, mv, sh, b, g, i++);
+  sh.flags[2] = i;
+  return i;
+}
+
 template <class GateLane, class GateWarp>
 __device__ __forceinline__ bool attn_items(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeAttnParams& a,
                                            const Shared& sh, GateLane gate_lane, GateWarp gate_warp) {
@@ -442,23 +491,12 @@ __device__ __forceinline__ bool attn_items(const CUtensorMap& mk, const CUtensor
     if (lane != 0) return true;
     tma_prefetch_desc(&mk);
     tma_prefetch_desc(&mv);
-    auto issue = [&](int i) {
-      const int s = i % STAGES;
-      const uint32_t dst = smem_u32(sh.ring + s * UNIT_BYTES);
-      const uint32_t fb = smem_u32(&sh.full[s]);
-      const int pos = i * ITEM_POS;
-      const uint64_t pol = l2_evict_first();
-      mbar_expect_tx(fb, UNIT_BYTES);
-      tma_load_4d_stream(dst, &mk, fb, 0, g, pos, b, pol);
-      tma_load_4d_stream(dst + BOX_BYTES, &mk, fb, 64, g, pos, b, pol);
-      tma_load_4d_stream(dst + 2 * BOX_BYTES, &mv, fb, 0, g, pos, b, pol);
-      tma_load_4d_stream(dst + 3 * BOX_BYTES, &mv, fb, 64, g, pos, b, pol);
-    };
-    int i = 0;
+    auto issue = [&](int i) { item_issue(mk, mv, sh, b, g, i); };
+    int i = flags[2];  // stages attn_items_early requested (0 if none)
     while (i + 1 < n && i < PRE_GATE_UNITS) issue(i++);  // stages before the one holding row P
     bool ok = gate_lane();
     for (; ok && i < n; ++i) {
-      if (i >= STAGES && !mbar_wait(smem_u32(&sh.empty[i % STAGES]), ((i / STAGES) & 1) ^ 1)) {
+      if (i >= STAGES && !mbar_wait(smem_u32(&sh.empty[item_slot(i)]), ((i / STAGES) & 1) ^ 1)) {
         ok = false;
         break;
       }
@@ -487,7 +525,7 @@ __device__ __forceinline__ bool attn_items(const CUtensorMap& mk, const CUtensor
       qb[s][1] = gr < N_REP ? q32[s * 8 + 4 + t] : 0u;
     }
     for (int i = 0; i < n; ++i) {
-      const int s = i % STAGES;
+      const int s = item_slot(i);
       const bool landed = mbar_wait(smem_u32(&sh.full[s]), (i / STAGES) & 1);
       if (!__all_sync(0xffffffffu, landed)) {
         if (lane == 0) atomicExch(&flags[0], 1);
@@ -641,10 +679,12 @@ __device__ __forceinline__ bool attn_merge(const DecodeAttnParams& a, const Shar
 }
 
 // After an aborted phase: let loads that were issued but never consumed land
-// (bounded). One thread.
-__device__ __forceinline__ void attn_drain(const Shared& sh) {
+// (bounded). One thread. `rot`: the split's slot rotation (ITEM_ROT for the
+// head-major stages, 0 for position-major units).
+__device__ __forceinline__ void attn_drain(const Shared& sh, int rot = 0) {
   const int issued = sh.flags[2];
-  for (int i = max(0, issued - STAGES); i < issued; ++i) mbar_wait(smem_u32(&sh.full[i % STAGES]), (i / STAGES) & 1);
+  for (int i = max(0, issued - STAGES); i < issued; ++i)
+    mbar_wait(smem_u32(&sh.full[(i + rot) % STAGES]), (i / STAGES) & 1);
 }
 
 }  // namespace attnk

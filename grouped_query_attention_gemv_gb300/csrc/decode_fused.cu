@@ -25,6 +25,14 @@
 // Each phase keeps at most a few weight stages in flight per SM: deeper
 // queues do not raise the stream's rate, and every counter poll and grid
 // hand-over waits behind the bytes an SM has in flight.
+// The grid is launched with programmatic stream serialization: a step that
+// follows another kernel of the stream is set up by the hardware while that
+// kernel finishes (~0.4 us per step), and every thread executes
+// griddepcontrol.wait before its first global access, so the step sees all
+// that the previous kernel wrote and overwrites nothing it still reads, as
+// in plain stream order. (Its CTAs, one per SM, start only when the previous
+// grid has left the SMs: a request of weights before the wait gained nothing
+// measurable and is not made.)
 // Waits are bounded (DEV_WAIT_TIMEOUT in the status word, then a clean exit).
 // The last CTA out resets the counters, so the workspace is ready for the
 // next call.
@@ -121,6 +129,10 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   float* rs = reinterpret_cast<float*>(ints + 16);  // [FUSED_MAX_B] attention_norm scales (layer calls)
   int* pre = ints + 16 + FUSED_MAX_B;
 
+  // everything below may touch what the previous kernel of the stream wrote;
+  // a dependent step may be set up as soon as every CTA of this one runs
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5;
   const rowsk::Shared sha{smem, a_bars, a_bars + MS, a_bars + 2 * MS, a_bars + 2 * MS + XS, flags_a, rs};
   // phase A needs nothing from the grid: its two producers set up their own
@@ -161,9 +173,21 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   const int grid = static_cast<int>(gridDim.x);
   int* const cnt = fp.counters;
 
-  // ---------------- phase A: Q|K|V projection, RoPE, cache append
+  const attnk::Shared shb{smem, b_bars, b_bars + attnk::STAGES, flags_b, pre,
+                          reinterpret_cast<float*>(smem + attnk::RING)};
+
+  // ---------------- phase A: Q|K|V projection, RoPE, cache append. With the
+  // head-major split, its weight producer requests the first KV stage (into
+  // a ring slot past the first, which holds the epilogue's sums) once the
+  // phase's last stage is consumed: HBM keeps streaming through the
+  // epilogue, and the stage has landed before the gate's poll.
   rowsk::rows_phase<CfgA<NP>, true>(
-      m.qkv, fp.pq, fp.qkv_plan, sha, []() { return true; }, []() { return true; }, []() {},
+      m.qkv, fp.pq, fp.qkv_plan, sha, []() { return true; }, []() { return true; },
+      [&fp, &m, &shb](auto drained) {
+        if constexpr (CfgA<NP>::RED_BYTES <= attnk::UNIT_BYTES) {
+          if (fp.head_major && drained()) attnk::attn_items_early(m.cache_hm.k, m.cache_hm.v, fp.at, shb);
+        }
+      },
       [cnt]() { signal_counter(&cnt[0], 1); }, a_started);
   fence_proxy_async_smem();  // the ring's generic reads and writes precede phase B's TMA writes into it
   __syncthreads();
@@ -175,8 +199,6 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   }
 
   // ---------------- phase B: attention units (waits for every CTA's Q|K|V rows)
-  const attnk::Shared shb{smem, b_bars, b_bars + attnk::STAGES, flags_b, pre,
-                          reinterpret_cast<float*>(smem + attnk::RING)};
   bool units_ok = true;
   if (!aborted) {
     // one poller per CTA: the producer lane waits on the grid counter and
@@ -235,14 +257,15 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
                                          if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
                                          return ok;
                                        },
-                                       []() {}, []() {}, 0);
+                                       [](auto) {}, []() {}, 0);
   }
   aborted = aborted || flags_b[0] != 0;
   __syncthreads();
   if (threadIdx.x == 0 && (aborted || flags_c[0])) {
     report(fp.pq.status, DEV_WAIT_TIMEOUT);
     if (flags_a[0]) rowsk::rows_drain<CfgA<NP>>(sha, fp.qkv_plan);
-    if (flags_b[0]) attnk::attn_drain(shb);
+    // (phase A's producer may have requested head-major stages before phase A gave up)
+    if (flags_a[0] || flags_b[0]) attnk::attn_drain(shb, fp.head_major ? attnk::ITEM_ROT : 0);
     if (flags_c[0]) rowsk::rows_drain<CfgC<NP>>(shc, fp.o_plan);
   }
   if (threadIdx.x == 0) {
@@ -295,11 +318,13 @@ cudaError_t launch_fused_np(const DecodeFusedArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = Layout<NP>::FIXED + (a.at.B + 1) * 4;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, m, fp);
 }
 

@@ -183,9 +183,11 @@ __device__ __forceinline__ int rows_start(const RowMaps& maps, const RowPlan& pl
 // token producer's TMA reads);
 // prologue() runs on the 256 compute threads before they consume anything
 // (other work of the grid that may overlap the first weight loads; false =
-// give up); w_issued() runs on the weight producer once all its loads are
-// requested; rows_done() runs on thread 0 once this CTA's rows are written
-// and fenced. `started`: the stages the calling producer thread already
+// give up); w_issued(drained) runs on the weight producer once all its loads
+// are requested, `drained` a callable that waits until the phase no longer
+// uses the ring past the cross-warp sums (the first RED_BYTES, which the
+// epilogue reads); rows_done() runs on thread 0 once this CTA's rows are
+// written and fenced. `started`: the stages the calling producer thread already
 // requested in rows_start (0 if none).
 template <class C_, bool QKV, class Gate, class Prologue, class WIssued, class RowsDone>
 __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams& p, const RowPlan& plan,
@@ -222,7 +224,16 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
       issue_w_stage<C_>(wmap, sh, i, S, wstage, mr, rot);
     }
     flags[2] = i;
-    if (i == NST) w_issued();
+    if (i == NST) {
+      // drained(): waits (bounded) until the compute warps have released the
+      // last stage's weights and tokens; every stage is then consumed and no
+      // load of the phase is in flight. False if the phase gave up.
+      const int l = NST - 1;
+      w_issued([&]() {
+        return mbar_wait_or_abort(smem_u32(&sh.empty[l % S]), (l / S) & 1, &flags[0]) &&
+               mbar_wait_or_abort(smem_u32(&sh.xempty[l % XS]), (l / XS) & 1, &flags[0]);
+      });
+    }
     return;
   }
   if (warp == WARPS + 1) {

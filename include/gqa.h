@@ -219,7 +219,10 @@ int gqa_last_launch_count(void);
 /* Selects, for the calling thread, how a decode step (T = 1) of at most 64
  * sequences is launched: enable != 0 (the default) runs it as one persistent
  * cooperative kernel (projection, attention and output projection ordered by
- * counters in the workspace's status region); enable = 0 as three kernels.
+ * counters in the workspace's status region; launched with programmatic
+ * stream serialization, it touches no memory before the previous kernel of
+ * the stream has completed, so stream order holds as usual); enable = 0 as
+ * three kernels.
  * Both compute the same function. Returns the previous setting. */
 int gqa_set_decode_fusion(int enable);
 
