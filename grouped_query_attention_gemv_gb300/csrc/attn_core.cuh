@@ -417,9 +417,13 @@ __device__ __forceinline__ bool attn_units(const CUtensorMap& mk, const CUtensor
 // all against the pair's 4 query heads (the same 16-row tile shape as a
 // position-major unit, so block16 serves both). At the end the 8 warps'
 // (max, sum, o) states are combined in shared memory by the log-sum-exp rule
-// in warp order and o[b, heads 4g..4g+3] written as bf16. The stages that do
-// not hold position P_b (the row the projection writes) are requested before
-// `gate_lane`. Roles, gates and the return value as in attn_units; the
+// in warp order and o[b, heads 4g..4g+3] written as bf16. The first stages
+// (up to the ring's depth) are requested before `gate_lane`, the one holding
+// position P_b too, although the projection writes that row concurrently:
+// after the gate, the warp whose keys include P_b loads the new K and V rows
+// (plain loads, published like the queries) and writes them over the stale
+// copy once the stage has landed. Roles, gates and the return value as in
+// attn_units; the
 // standalone kernel does not use this phase (its queries are ready at launch
 // and its batches are larger).
 // Stage i occupies ring slot (i + ITEM_ROT) % STAGES: the first stages then
@@ -450,8 +454,8 @@ __device__ __forceinline__ void item_issue(const CUtensorMap& mk, const CUtensor
   tma_load_4d_stream(dst + 3 * BOX_BYTES, &mv, fb, 64, g, pos, b, pol);
 }
 
-// Requests this CTA's first head-major stages (at most EARLY_ITEMS, none
-// holding position P_b) before phase B: called by the producer lane once the
+// Requests this CTA's first head-major stages (at most EARLY_ITEMS) before
+// phase B: called by the producer lane once the
 // ring's slots past the first are free (every stage of the preceding phase
 // consumed, no load of it in flight). Records the count in sh.flags[2], where
 // attn_items (same lane) continues and attn_drain looks. Returns the count.
@@ -466,7 +470,7 @@ __device__ __forceinline__ int attn_items_early(const CUtensorMap& mk, const CUt
   tma_prefetch_desc(&mk);
   tma_prefetch_desc(&mv);
   int i = 0;
-  while (i + 1 < n && i < EARLY_ITEMS) item_issue(mk, mv, sh, b, g, i++);
+  while (i < n && i < EARLY_ITEMS) item_issue(mk, mv, sh, b, g, i++);
   sh.flags[2] = i;
   return i;
 }
@@ -493,7 +497,7 @@ __device__ __forceinline__ bool attn_items(const CUtensorMap& mk, const CUtensor
     tma_prefetch_desc(&mv);
     auto issue = [&](int i) { item_issue(mk, mv, sh, b, g, i); };
     int i = flags[2];  // stages attn_items_early requested (0 if none)
-    while (i + 1 < n && i < PRE_GATE_UNITS) issue(i++);  // stages before the one holding row P
+    while (i < n && i < PRE_GATE_UNITS) issue(i++);  // row P is put in place after the gate
     bool ok = gate_lane();
     for (; ok && i < n; ++i) {
       if (i >= STAGES && !mbar_wait(smem_u32(&sh.empty[item_slot(i)]), ((i / STAGES) & 1) ^ 1)) {
@@ -524,6 +528,19 @@ __device__ __forceinline__ bool attn_items(const CUtensorMap& mk, const CUtensor
       qb[s][0] = gr < N_REP ? q32[s * 8 + t] : 0u;
       qb[s][1] = gr < N_REP ? q32[s * 8 + 4 + t] : 0u;
     }
+    // the new row P: lane l holds 16 bytes of box l / 8 (K lo, K hi, V lo,
+    // V hi), chunk l % 8; the warp whose keys include P writes it into stage
+    // P / ITEM_POS, which may have been read before the projection wrote it
+    const int iP = P / ITEM_POS, rP = P % ITEM_POS;
+    const bool ownP = rP / UNIT == warp;
+    const int bx = lane >> 3, ch = lane & 7;
+    uint4 rowP = make_uint4(0u, 0u, 0u, 0u);
+    if (ownP) {
+      const __nv_bfloat16* src = (bx < 2 ? a.cache_k : a.cache_v) +
+                                 (static_cast<size_t>(b) * a.s_max + P) * (N_KV * HEAD_DIM) + g * HEAD_DIM +
+                                 (bx & 1) * 64 + ch * 8;
+      rowP = *reinterpret_cast<const uint4*>(src);
+    }
     for (int i = 0; i < n; ++i) {
       const int s = item_slot(i);
       const bool landed = mbar_wait(smem_u32(&sh.full[s]), (i / STAGES) & 1);
@@ -531,6 +548,11 @@ __device__ __forceinline__ bool attn_items(const CUtensorMap& mk, const CUtensor
         if (lane == 0) atomicExch(&flags[0], 1);
         ok = false;
         break;
+      }
+      if (i == iP && ownP) {  // warp-uniform
+        st_shared_v4(smem_u32(sh.ring + s * UNIT_BYTES + bx * BOX_BYTES) + sw128(rP, ch), rowP);
+        fence_proxy_async_smem();  // before any later TMA write into this slot
+        __syncwarp();
       }
       const int key0 = i * ITEM_POS + warp * UNIT;
       if (key0 < L) {  // warp-uniform: a warp whose keys all lie past the sequence skips the stage

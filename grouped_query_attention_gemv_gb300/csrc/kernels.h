@@ -156,7 +156,7 @@ struct DecodeAttnParams {
   int* counters;           // [2] grid counters (meeting, exit), zero-filled, left zero-filled
   __nv_bfloat16* o;        // [B][4096]
   int* status;
-  const __nv_bfloat16* cache_k;  // [B][s_max][n_kv][128], for L2 prefetches only
+  const __nv_bfloat16* cache_k;  // [B][s_max][n_kv][128]: L2 prefetches; the head-major split's new row
   const __nv_bfloat16* cache_v;
   int s_max;
   unsigned long long wait_ns;    // limit of the grid-wide waits (the meeting; the fused grid's gates)

@@ -366,35 +366,85 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     const uint32_t wa = smem_u32(sh.ring + s * wstage);
     const int rb = kb * mr.h;  // this warp's k block starts at row rb of the stage
     const uint32_t xb = smem_u32(xring + xs * C_::X_STAGE + kb * C_::B_BYTES);
+    if constexpr (C_::NT <= 2) {
+      // with few tokens, every fragment of the stage first, then the
+      // products: the loads are in flight together instead of one load's
+      // latency before each product (more tokens: the registers are not there)
+      constexpr int NKS = KS / 2;  // k16 pairs of this warp in the stage
+      uint32_t bf[NKS][C_::NT][4];
+      uint32_t af[NKS][2][MT_MAX][4];
 #pragma unroll
-    for (int ks = ks0; ks < ks0 + KS; ks += 2) {
-      // token fragments of two k16 steps: matrices (tokens, 16-byte chunks 2ks .. 2ks+3)
-      uint32_t b[C_::NT][4];
+      for (int j = 0; j < NKS; ++j) {
+        const int ks = ks0 + 2 * j;
+        // token fragments of two k16 steps: matrices (tokens, 16-byte chunks 2ks .. 2ks+3)
 #pragma unroll
-      for (int nt = 0; nt < C_::NT; ++nt) {
-        const int tr = tok0 + nt * 8 + (lane & 7);
-        ldsm_x4(xb + sw128(tr, 2 * ks + (lane >> 3)), b[nt][0], b[nt][1], b[nt][2], b[nt][3]);
+        for (int nt = 0; nt < C_::NT; ++nt) {
+          const int tr = tok0 + nt * 8 + (lane & 7);
+          ldsm_x4(xb + sw128(tr, 2 * ks + (lane >> 3)), bf[j][nt][0], bf[j][nt][1], bf[j][nt][2], bf[j][nt][3]);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+          for (int mt = 0; mt < MT_MAX; ++mt)
+            if (mt < mtc) {
+              const int r = rb + mt * 16 + (lane & 15);
+              ldsm_x4(wa + sw128(r, 2 * (ks + kk) + (lane >> 4)), af[j][kk][mt][0], af[j][kk][mt][1], af[j][kk][mt][2],
+                      af[j][kk][mt][3]);
+            }
       }
       if (norm) {
         // fragment q holds token tok0 + nt*8 + lane/4, features k, k+1 of chunk 2ks + q
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t g2 = gcur[((ks - ks0) >> 1) * 4 + q];
+        for (int j = 0; j < NKS; ++j)
 #pragma unroll
-          for (int nt = 0; nt < C_::NT; ++nt) b[nt][q] = norm_pair(b[nt][q], rn[nt], g2);
-        }
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t g2 = gcur[j * 4 + q];
+#pragma unroll
+            for (int nt = 0; nt < C_::NT; ++nt) bf[j][nt][q] = norm_pair(bf[j][nt][q], rn[nt], g2);
+          }
       }
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
+      for (int j = 0; j < NKS; ++j)
 #pragma unroll
-        for (int mt = 0; mt < MT_MAX; ++mt) {
-          if (mt < mtc) {
-            uint32_t a0, a1, a2, a3;
-            const int r = rb + mt * 16 + (lane & 15);
-            ldsm_x4(wa + sw128(r, 2 * (ks + kk) + (lane >> 4)), a0, a1, a2, a3);
+        for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
-            for (int nt = 0; nt < C_::NT; ++nt)
-              mma16816(acc[kk % KH][mt][nt], a0, a1, a2, a3, b[nt][2 * kk], b[nt][2 * kk + 1]);
+          for (int mt = 0; mt < MT_MAX; ++mt)
+            if (mt < mtc)
+#pragma unroll
+              for (int nt = 0; nt < C_::NT; ++nt)
+                mma16816(acc[kk % KH][mt][nt], af[j][kk][mt][0], af[j][kk][mt][1], af[j][kk][mt][2], af[j][kk][mt][3],
+                         bf[j][nt][2 * kk], bf[j][nt][2 * kk + 1]);
+    } else {
+#pragma unroll
+      for (int ks = ks0; ks < ks0 + KS; ks += 2) {
+        // token fragments of two k16 steps: matrices (tokens, 16-byte chunks 2ks .. 2ks+3)
+        uint32_t b[C_::NT][4];
+#pragma unroll
+        for (int nt = 0; nt < C_::NT; ++nt) {
+          const int tr = tok0 + nt * 8 + (lane & 7);
+          ldsm_x4(xb + sw128(tr, 2 * ks + (lane >> 3)), b[nt][0], b[nt][1], b[nt][2], b[nt][3]);
+        }
+        if (norm) {
+          // fragment q holds token tok0 + nt*8 + lane/4, features k, k+1 of chunk 2ks + q
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t g2 = gcur[((ks - ks0) >> 1) * 4 + q];
+#pragma unroll
+            for (int nt = 0; nt < C_::NT; ++nt) b[nt][q] = norm_pair(b[nt][q], rn[nt], g2);
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+          for (int mt = 0; mt < MT_MAX; ++mt) {
+            if (mt < mtc) {
+              uint32_t a0, a1, a2, a3;
+              const int r = rb + mt * 16 + (lane & 15);
+              ldsm_x4(wa + sw128(r, 2 * (ks + kk) + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+              for (int nt = 0; nt < C_::NT; ++nt)
+                mma16816(acc[kk % KH][mt][nt], a0, a1, a2, a3, b[nt][2 * kk], b[nt][2 * kk + 1]);
+            }
           }
         }
       }

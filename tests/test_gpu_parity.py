@@ -216,6 +216,26 @@ def test_decode_head_major_edges(weights, B, starts, s_max):
     H.check_canaries(c)
 
 
+@pytest.mark.parametrize("split", SPLITS)
+def test_decode_stale_new_row_never_reaches_the_scores(weights, split):
+    """Row P of the cache holds NaN before the call. The head-major split
+    requests the stage holding P before the projection has written that row
+    (the warp holding key P then writes the new row over the stale copy); the
+    position-major split reads it only after the gate. Either way the NaN
+    must not reach the output, at one stage (P < 128) and at several."""
+    starts = [0, 15, 127, 200, 383]
+    c = H.make_case(len(starts), 1, starts, 400, weights=weights)
+    for b, p in enumerate(starts):
+        c.dev["cache_k"][b, p] = float("nan")
+        c.dev["cache_v"][b, p] = float("nan")
+    with attention_split(split):
+        out, _ = run_decode(c)
+    assert torch.isfinite(out.float()).all()
+    for b in range(c.B):
+        H.compare_sequence(c, out, b)
+    H.check_canaries(c)
+
+
 def test_decode_splits_alternate_on_one_workspace(weights):
     """Calls switching between the two attention splits share one workspace:
     each leaves the grid counters ready for the other."""
