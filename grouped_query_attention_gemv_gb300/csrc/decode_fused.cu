@@ -90,17 +90,20 @@ struct FusedParams {
 };
 
 // Phase A streams its weights from HBM as soon as the grid starts: the
-// default (short) token ring. Phase C requests its first weight stages while
-// the grid finishes the attention; its tokens, the attention output, only
-// become ready at the gate: a deep token ring (128 KB at 16 tokens).
+// default (short) token ring, about 85 KB of weight stages in flight per SM
+// (13 MB over the grid, 2 us of HBM time). Phase C requests its first weight
+// stages while the grid finishes the attention; its tokens, the attention
+// output, only become ready at the gate. Once past the gate its consumer
+// waits on weight stages that take ~1.2 us to land, so the period per stage
+// is that latency over the stages in flight: up to 16 tokens, 4 token stages
+// (half the output) leave 5-6 weight slots, 3 of them in flight (B = 16:
+// -0.3 us per step, B = 1: -0.6 us against 8 token stages and 2 in flight).
 // (Asking L2 for the rest of W_O at the same time measured 1.5 us slower per
 // step at B = 16: the requests queue ahead of the merge and the gate.)
-// Both keep about 85 KB of weight stages in flight per SM (13 MB over the
-// grid, 2 us of HBM time).
 template <int NP>
 using CfgA = rowsk::Cfg<NP>;
 template <int NP>
-using CfgC = rowsk::Cfg<NP, NP <= 16 ? 8 : (NP == 32 ? 4 : 3)>;
+using CfgC = rowsk::Cfg<NP, NP <= 16 ? 4 : (NP == 32 ? 4 : 3), NP <= 16 ? 3 : 0>;
 
 template <int NP>
 struct Layout {
