@@ -350,14 +350,22 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
       }
     }
   };
+  // stage i's slots in the two rings and their barrier phases, advanced by
+  // one each stage: the ring size S is only known at run time, and a
+  // division by it costs the consumer ~150 cycles a stage
+  int s = 0, xs = 0;
+  uint32_t ph = 0, xph = 0;
   for (int i = 0; ok && i < NST; ++i) {
     uint32_t gcur[NG];
 #pragma unroll
     for (int j = 0; j < NG; ++j) gcur[j] = gnext[j];
     if (norm && i + 1 < NST) load_g(i + 1, gnext);
-    const int s = i % S, xs = i % XS;
-    bool landed = mbar_wait_or_abort(smem_u32(&sh.full[s]), (i / S) & 1, &flags[0]);
-    landed = landed && mbar_wait_or_abort(smem_u32(&sh.xfull[xs]), (i / XS) & 1, &flags[0]);
+    if (i > 0) {
+      if (++s == S) { s = 0; ph ^= 1u; }
+      if (++xs == XS) { xs = 0; xph ^= 1u; }
+    }
+    bool landed = mbar_wait_or_abort(smem_u32(&sh.full[s]), ph, &flags[0]);
+    landed = landed && mbar_wait_or_abort(smem_u32(&sh.xfull[xs]), xph, &flags[0]);
     if (!__all_sync(0xffffffffu, landed)) {
       if (lane == 0) atomicExch(&flags[0], 1);
       ok = false;
@@ -391,6 +399,14 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
               ldsm_x4(wa + sw128(r, 2 * (ks + kk) + (lane >> 4)), af[j][kk][mt][0], af[j][kk][mt][1], af[j][kk][mt][2],
                       af[j][kk][mt][3]);
             }
+      }
+      // the stage's slots are no longer read: release them before the
+      // products (the arrive orders the warp's loads, which __syncwarp
+      // orders before lane 0's arrive)
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sh.empty[s]));
+        mbar_arrive(smem_u32(&sh.xempty[xs]));
       }
       if (norm) {
         // fragment q holds token tok0 + nt*8 + lane/4, features k, k+1 of chunk 2ks + q
@@ -449,10 +465,12 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(smem_u32(&sh.empty[s]));
-      mbar_arrive(smem_u32(&sh.xempty[xs]));
+    if constexpr (C_::NT > 2) {  // the interleaved form reads the ring up to its last product
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sh.empty[s]));
+        mbar_arrive(smem_u32(&sh.xempty[xs]));
+      }
     }
     if constexpr (QKV) {
       if (i == EPF_SP) epf_start_positions();
