@@ -414,6 +414,17 @@ bool row_maps(const gqa_bf16* const* w, const RowPlan& plan, const void* x, int 
   return np > 0 && map_rows_kblocks(&m->x, x, M, np, kc);
 }
 
+// Tensor maps of the multi-head Q|K|V phase: Wq, Wk and Wv (4,096 rows
+// each) walked in three passes of one plan, so every matrix gets that plan's
+// boxes.
+bool row_maps_passes(const gqa_bf16* const* w, const RowPlan& plan, const void* x, int M, int np, RowMaps* m) {
+  const int kc = rows_kc(np);
+  for (int i = 0; i < 3; ++i)
+    for (int hi = 0; hi < 2; ++hi)
+      if (!map_rows_kblocks(&m->w[i][hi], w[i], plan.rows[0], plan.h_lo[0] + 2 * hi, kc)) return false;
+  return np > 0 && map_rows_kblocks(&m->x, x, M, np, kc);
+}
+
 // Work split of the fused grid's attention for one call. Head-major (one
 // (sequence, KV head) pair per CTA) streams each head of a sequence on one
 // SM, at about 50 GB/s per SM (measured with 128 SMs streaming at B = 16,
@@ -433,22 +444,30 @@ bool head_major_pays(int B, int max_keys, int ctas) {
 // GQA_EINVAL without launching anything when this GPU cannot run it (too few
 // SMs for the row split); the caller then takes the three-kernel path.
 int run_decode_fused(const Call& c) {
-  if (c.n_kv != N_KV) return GQA_EINVAL;  // phase A's row split is sized for 8 KV heads
+  // 8 KV heads: one Q|K|V pass over 6,144 rows. 32 KV heads (12,288 rows):
+  // three passes of 4,096, up to 16 sequences (the attention's unit prefix
+  // covers 4 head groups per sequence), block entries only.
+  const bool mha = c.n_kv == N_HEADS;
+  if (c.n_kv != N_KV && !(mha && c.B * N_REP <= FUSED_MAX_B && !c.norm_w)) return GQA_EINVAL;
   DecodeFusedArgs a;
   a.ctas = launch_sms();
   const int qkv_rows[3] = {D_MODEL, KV_ROW, KV_ROW};
   const int o_rows[1] = {D_MODEL};
-  if (!make_row_plan(3, qkv_rows, a.ctas, &a.qkv_plan) || !make_row_plan(1, o_rows, a.ctas, &a.o_plan))
+  a.qkv_passes = mha ? 3 : 1;
+  if (!(mha ? make_row_plan(1, o_rows, a.ctas, &a.qkv_plan) : make_row_plan(3, qkv_rows, a.ctas, &a.qkv_plan)) ||
+      !make_row_plan(1, o_rows, a.ctas, &a.o_plan))
     return GQA_EINVAL;
   a.pq = proj_params(c, true, /*fold_norm=*/true);
   a.po = proj_params(c, false);
   const gqa_bf16* wqkv[3] = {c.wq, c.wk, c.wv};
   const gqa_bf16* wo[1] = {c.wo};
   const int np = decode_fused_np(a.pq.M);
-  a.head_major = t_attn_split == 2 ? (c.B * N_KV <= a.ctas)
+  a.head_major = mha                 ? 0
+                 : t_attn_split == 2 ? (c.B * N_KV <= a.ctas)
                  : t_attn_split == 1 ? 0
                                      : head_major_pays(c.B, c.max_keys, a.ctas);
-  if (!row_maps(wqkv, a.qkv_plan, a.pq.x, a.pq.M, np, &a.qkv_maps) ||
+  if (!(mha ? row_maps_passes(wqkv, a.qkv_plan, a.pq.x, a.pq.M, np, &a.qkv_maps)
+            : row_maps(wqkv, a.qkv_plan, a.pq.x, a.pq.M, np, &a.qkv_maps)) ||
       !row_maps(wo, a.o_plan, a.po.x, a.po.M, np, &a.o_maps) ||
       !decode_cache_maps(c, &a.cache))
     return fail_cuda(cudaErrorInvalidValue);

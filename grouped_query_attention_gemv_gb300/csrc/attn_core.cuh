@@ -586,19 +586,25 @@ __device__ __forceinline__ bool attn_items(const CUtensorMap& mk, const CUtensor
       }
     }
     asm volatile("bar.sync 3, 256;" ::: "memory");
-    // thread -> query head hh, dims d2, d2 + 1; warp 0 always holds key 0, so M is finite
+    // thread -> query head hh, dims d2, d2 + 1; warp 0 always holds key 0, so M is finite.
+    // Warps past the first nw hold no key (max -inf, sum 0, o 0): their
+    // terms are exact zeros and are skipped
     const int hh = threadIdx.x >> 6, d2 = (threadIdx.x & 63) * 2;
+    const int nw = min(COMPUTE_WARPS, (L + UNIT - 1) / UNIT);
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < COMPUTE_WARPS; ++w) M = fmaxf(M, ml[(w * N_REP + hh) * 2]);
+    for (int w = 0; w < COMPUTE_WARPS; ++w)
+      if (w < nw) M = fmaxf(M, ml[(w * N_REP + hh) * 2]);
     float den = 0.f, o0 = 0.f, o1 = 0.f;
 #pragma unroll
     for (int w = 0; w < COMPUTE_WARPS; ++w) {
-      const float f = exp2f(ml[(w * N_REP + hh) * 2] - M);  // 0 for a warp without keys (max -inf)
-      den += f * ml[(w * N_REP + hh) * 2 + 1];
-      const float2 v = *reinterpret_cast<const float2*>(sh.stage_out + (w * N_REP + hh) * HEAD_DIM + d2);
-      o0 += f * v.x;
-      o1 += f * v.y;
+      if (w < nw) {
+        const float f = exp2f(ml[(w * N_REP + hh) * 2] - M);
+        den += f * ml[(w * N_REP + hh) * 2 + 1];
+        const float2 v = *reinterpret_cast<const float2*>(sh.stage_out + (w * N_REP + hh) * HEAD_DIM + d2);
+        o0 += f * v.x;
+        o1 += f * v.y;
+      }
     }
     const float inv = 1.f / den;
     *reinterpret_cast<uint32_t*>(a.o + static_cast<size_t>(b) * D_MODEL + static_cast<size_t>(g * N_REP + hh) * HEAD_DIM +

@@ -115,9 +115,14 @@ struct Layout {
   static_assert(attnk::RING + attnk::STAGE_OUT_BYTES <= RING, "attention staging fits");
 };
 
-template <int NP>
+// NREP: query heads per KV head, 4 (8 KV heads) or 1 (the multi-head variant:
+// 32 KV heads, Wk and Wv of 4,096 rows each; phase A walks Wq, Wk and Wv in
+// three passes over the grid, the attention runs each sequence as 4 groups
+// of 8 KV heads, position-major).
+template <int NP, int NREP>
 __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_constant__ FusedMaps m, FusedParams fp) {
   using L = Layout<NP>;
+  constexpr int NG = N_REP / NREP;  // head groups of 8 KV heads per sequence
   constexpr int MS = rowsk::MAX_STAGES, XS = rowsk::XS_MAX;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -184,20 +189,61 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   // a ring slot past the first, which holds the epilogue's sums) once the
   // phase's last stage is consumed: HBM keeps streaming through the
   // epilogue, and the stage has landed before the gate's poll.
-  rowsk::rows_phase<CfgA<NP>, true>(
-      m.qkv, fp.pq, fp.qkv_plan, sha, []() { return true; }, []() { return true; },
-      [&fp, &m, &shb](auto drained) {
-        if constexpr (CfgA<NP>::RED_BYTES <= attnk::UNIT_BYTES) {
-          if (fp.head_major && drained()) attnk::attn_items_early(m.cache_hm.k, m.cache_hm.v, fp.at, shb);
+  if constexpr (NREP == N_REP) {
+    rowsk::rows_phase<CfgA<NP>, true>(
+        m.qkv, fp.pq, fp.qkv_plan, sha, []() { return true; }, []() { return true; },
+        [&fp, &m, &shb](auto drained) {
+          if constexpr (CfgA<NP>::RED_BYTES <= attnk::UNIT_BYTES) {
+            if (fp.head_major && drained()) attnk::attn_items_early(m.cache_hm.k, m.cache_hm.v, fp.at, shb);
+          }
+        },
+        [cnt]() { signal_counter(&cnt[0], 1); }, a_started);
+  } else {
+    // 32 KV heads: Wq, Wk and Wv in turn, each of its 4,096 rows split over
+    // the grid as W_O's are; the CTA publishes its rows once, after the last
+    // pass (thread 0's release after the epilogue's barrier covers all three)
+    for (int pass = 0; pass < 3; ++pass) {
+      if (pass > 0) {
+        // the ring's generic reads and writes precede the next pass's TMA
+        // writes; every load of the pass has landed and been consumed, so
+        // its barriers start again from phase 0
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (flags_a[0]) break;
+        if (threadIdx.x == 0) {
+          for (int s = 0; s < MS; ++s) {
+            mbar_inval(smem_u32(&sha.full[s]));
+            mbar_inval(smem_u32(&sha.empty[s]));
+            mbar_init(smem_u32(&sha.full[s]), 1);
+            mbar_init(smem_u32(&sha.empty[s]), rowsk::WARPS);
+          }
+          for (int s = 0; s < XS; ++s) {
+            mbar_inval(smem_u32(&sha.xfull[s]));
+            mbar_inval(smem_u32(&sha.xempty[s]));
+            mbar_init(smem_u32(&sha.xfull[s]), 1);
+            mbar_init(smem_u32(&sha.xempty[s]), rowsk::WARPS);
+          }
+          flags_a[2] = 0;
+          fence_barrier_init();
         }
-      },
-      [cnt]() { signal_counter(&cnt[0], 1); }, a_started);
+        __syncthreads();
+      }
+      RowPlan pp = fp.qkv_plan;
+      pp.mat0 = pass;
+      rowsk::rows_phase<CfgA<NP>, true>(
+          m.qkv, fp.pq, pp, sha, []() { return true; }, []() { return true; }, [](auto) {},
+          [cnt, pass]() {
+            if (pass == 2) signal_counter(&cnt[0], 1);
+          },
+          pass == 0 ? a_started : 0);
+    }
+  }
   fence_proxy_async_smem();  // the ring's generic reads and writes precede phase B's TMA writes into it
   __syncthreads();
   bool aborted = flags_a[0] != 0;
   if (!fp.head_major) {
     // the position-major split's unit prefix (the start positions are in L2 by now)
-    if (warp == rowsk::WARPS - 1) attnk::build_prefix<1>(fp.at, pre);
+    if (warp == rowsk::WARPS - 1) attnk::build_prefix<NG>(fp.at, pre);
     __syncthreads();
   }
 
@@ -205,7 +251,9 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   bool units_ok = true;
   if (!aborted) {
     // one poller per CTA: the producer lane waits on the grid counter and
-    // hands the outcome to the compute warps through shared memory
+    // hands the outcome to the compute warps through shared memory (lane 0
+    // of every compute warp polling the counter as well measured 0.4 us
+    // slower at B = 16)
     auto gate_lane = [cnt, grid, flags_b, &fp]() {
       const bool ok = wait_counter(&cnt[0], grid, fp.at.wait_ns);
       fence_proxy_async_global();  // the new K/V rows were written by plain stores
@@ -217,10 +265,14 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
       if ((threadIdx.x & 31) == 0) v = wait_flag_cta(&flags_b[1]);
       return __shfl_sync(0xffffffffu, v, 0) == 1;
     };
-    if (fp.head_major)
-      units_ok = attnk::attn_items(m.cache_hm.k, m.cache_hm.v, fp.at, shb, gate_lane, gate_warp);
-    else
-      units_ok = attnk::attn_units<N_REP>(m.cache.k, m.cache.v, fp.at, shb, gate_lane, gate_warp, []() {});
+    if constexpr (NREP == N_REP) {
+      if (fp.head_major)
+        units_ok = attnk::attn_items(m.cache_hm.k, m.cache_hm.v, fp.at, shb, gate_lane, gate_warp);
+      else
+        units_ok = attnk::attn_units<NREP>(m.cache.k, m.cache.v, fp.at, shb, gate_lane, gate_warp, []() {});
+    } else {
+      units_ok = attnk::attn_units<NREP>(m.cache.k, m.cache.v, fp.at, shb, gate_lane, gate_warp, []() {});
+    }
     fence_proxy_async_smem();  // ldmatrix reads of the ring precede phase C's TMA writes into it
   }
   __syncthreads();
@@ -241,7 +293,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   if (!aborted && flags_b[0]) {
     // this CTA's units gave up: it still meets the grid (no other CTA waits in vain)
     if (warp < attnk::COMPUTE_WARPS) {
-      if (!fp.head_major) attnk::attn_merge<N_REP>(fp.at, shb, &cnt[3], false);
+      if (!fp.head_major) attnk::attn_merge<NREP>(fp.at, shb, &cnt[3], false);
       if (threadIdx.x == 0 && !early_signal) signal_counter(&cnt[1], 1);
     }
   } else if (!aborted) {
@@ -255,7 +307,7 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
                                          // head-major outputs need no merge (attn_items fenced them and
                                          // they are published already)
                                          if (early_signal) return units_ok;
-                                         const bool ok = attnk::attn_merge<N_REP>(fp.at, shb, &cnt[3], units_ok);
+                                         const bool ok = attnk::attn_merge<NREP>(fp.at, shb, &cnt[3], units_ok);
                                          // this CTA's attention outputs (whole sequences, merges) are fenced
                                          if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
                                          return ok;
@@ -284,21 +336,24 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   }
 }
 
-template <int NP>
+template <int NP, int NREP>
 cudaError_t launch_fused_np(const DecodeFusedArgs& a, cudaStream_t s) {
   static bool attr_set[64] = {};
+  constexpr int NG = N_REP / NREP;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  auto kern = decode_fused_kernel<NP>;
+  auto kern = decode_fused_kernel<NP, NREP>;
   const int max_smem = Layout<NP>::FIXED + (FUSED_MAX_B + 1) * 4;
   if (!attr_set[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  if (a.at.B <= 0 || a.at.B > FUSED_MAX_B) return cudaErrorInvalidValue;
+  // the unit prefix over B * NG virtual sequences lives in shared memory
+  if (a.at.B <= 0 || a.at.B * NG > FUSED_MAX_B) return cudaErrorInvalidValue;
+  if (a.qkv_passes != (NREP == N_REP ? 1 : 3) || (NREP != N_REP && a.qkv_plan.nmat != 1)) return cudaErrorInvalidValue;
   int planned = 0;
   for (int i = 0; i < a.qkv_plan.nmat; ++i) planned += a.qkv_plan.ctas[i];
   if (planned != a.ctas || a.o_plan.nmat != 1 || a.o_plan.ctas[0] != a.ctas) return cudaErrorInvalidValue;
@@ -315,11 +370,11 @@ cudaError_t launch_fused_np(const DecodeFusedArgs& a, cudaStream_t s) {
   fp.at = a.at;
   fp.counters = a.counters;
   fp.head_major = a.head_major;
-  if (a.head_major && a.at.B * N_KV > a.ctas) return cudaErrorInvalidValue;
+  if (a.head_major && (NREP != N_REP || a.at.B * N_KV > a.ctas)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ctas);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = Layout<NP>::FIXED + (a.at.B + 1) * 4;
+  cfg.dynamicSmemBytes = Layout<NP>::FIXED + (a.at.B * NG + 1) * 4;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -338,14 +393,23 @@ int decode_fused_np(int M) {
 }
 
 cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
-  if (a.at.n_kv != N_KV) return cudaErrorInvalidValue;  // 8 KV heads (the row split of phase A)
-  switch (decode_fused_np(a.pq.M)) {
-    case 8: return launch_fused_np<8>(a, s);
-    case 16: return launch_fused_np<16>(a, s);
-    case 32: return launch_fused_np<32>(a, s);
-    case 64: return launch_fused_np<64>(a, s);
-    default: return cudaErrorInvalidValue;
+  if (a.at.n_kv == N_KV) {
+    switch (decode_fused_np(a.pq.M)) {
+      case 8: return launch_fused_np<8, N_REP>(a, s);
+      case 16: return launch_fused_np<16, N_REP>(a, s);
+      case 32: return launch_fused_np<32, N_REP>(a, s);
+      case 64: return launch_fused_np<64, N_REP>(a, s);
+      default: return cudaErrorInvalidValue;
+    }
   }
+  if (a.at.n_kv == N_HEADS) {  // the multi-head variant, up to 16 sequences
+    switch (decode_fused_np(a.pq.M)) {
+      case 8: return launch_fused_np<8, 1>(a, s);
+      case 16: return launch_fused_np<16, 1>(a, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace gqa

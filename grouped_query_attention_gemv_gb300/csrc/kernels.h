@@ -197,6 +197,7 @@ struct RowPlan {
   int rows[3];
   int ctas[3];
   int h_lo[3];
+  int mat0;  // RowMaps index of matrix 0 (0; a pass over one matrix of three sets it to that matrix)
 };
 constexpr int ROWS_MAX_H = 48;   // rows one CTA can own (3 row tiles of 16)
 // k blocks of 64 per stage of the row-owner projections for np padded tokens
@@ -230,6 +231,8 @@ struct DecodeFusedArgs {
   DecodeAttnParams at;
   int* counters;           // [3] grid progress counters, zero-filled, left zero-filled
   int ctas;                // one CTA per SM
+  int qkv_passes;          // 1 (8 KV heads: qkv_plan splits all 6,144 rows) or 3 (32 KV heads: qkv_plan
+                           // splits one 4,096-row matrix, walked for Wq, Wk, Wv in turn)
 };
 cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s);
 int decode_fused_np(int M);   // padded tokens of the fused grid's projections (0 if M > 64)

@@ -108,7 +108,7 @@ __device__ __forceinline__ MyRows my_rows(const RowPlan& plan, int c) {
   const int p0 = static_cast<int>(static_cast<long long>(pairs) * c / n);
   const int p1 = static_cast<int>(static_cast<long long>(pairs) * (c + 1) / n);
   MyRows r;
-  r.mat = mat;
+  r.mat = plan.mat0 + mat;  // the RowMaps (and feature range) index
   r.row0 = 2 * p0;
   r.h = 2 * (p1 - p0);
   r.hi = r.h == plan.h_lo[mat] ? 0 : 1;

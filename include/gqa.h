@@ -152,8 +152,10 @@ int gqa_decode(const gqa_bf16* x, int B, const int32_t* start_pos, int max_start
  * Any other value is GQA_EINVAL. Every other argument, the workspace size
  * (gqa_workspace_bytes covers both), the cache update and the error
  * behaviour as in gqa_block_forward / gqa_decode; gqa_decode_nkv with 32 KV
- * heads also requires B <= 512. The multi-head decode step runs as three
- * kernels (the fused decode grid is sized for 8 KV heads). */
+ * heads also requires B <= 512. The multi-head decode step of up to 16
+ * sequences runs as one grid like the grouped one (its Q|K|V projection in
+ * three passes over Wq, Wk and Wv; see gqa_set_decode_fusion), larger batches
+ * as three kernels. */
 int gqa_block_forward_nkv(const gqa_bf16* x, int B, int T, int start_pos, int n_kv_heads,
                           const gqa_bf16* wq, const gqa_bf16* wk, const gqa_bf16* wv,
                           const gqa_bf16* wo, const float* rope, int rope_rows,
@@ -217,7 +219,7 @@ const char* gqa_strerror(int status);
 int gqa_last_launch_count(void);
 
 /* Selects, for the calling thread, how a decode step (T = 1) of at most 64
- * sequences is launched: enable != 0 (the default) runs it as one persistent
+ * sequences (16 with 32 KV heads) is launched: enable != 0 (the default) runs it as one persistent
  * cooperative kernel (projection, attention and output projection ordered by
  * counters in the workspace's status region; launched with programmatic
  * stream serialization, it touches no memory before the previous kernel of

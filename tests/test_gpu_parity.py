@@ -311,6 +311,42 @@ def test_grid_wait_timeout_is_reported_and_recovered(weights, path, split, count
     H.check_canaries(c)
 
 
+@pytest.mark.parametrize("counter", [0, 3])   # the Q|K|V gate after the three passes; the merges' meeting
+def test_mha_fused_wait_timeout_is_reported_and_recovered(mha_weights, counter):
+    """The multi-head one-grid step: a grid counter that cannot reach its
+    target ends the call under a 1 ms limit with GQA_DEV_WAIT_TIMEOUT, every
+    counter reset and no cache row outside the new ones changed; the next
+    call on the same workspace passes parity."""
+    starts = [1000, 517, 64]
+    c = H.make_case(3, 1, starts, 1100, seed=3, weights=mha_weights, dims=I.LLAMA31_8B_MHA)
+    d = c.dev
+    sp = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    ws = G.make_workspace(3, 1, 1001)
+    counters = ws[COUNTERS:COUNTERS + 16].view(torch.int32)
+    counters[counter] = -(1 << 30)
+    prev = G.set_decode_fusion(True)
+    try:
+        with wait_limit(1_000_000):
+            G.decode(d["x"], sp, 1000, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"],
+                     d["cache_v"], workspace=ws, n_kv_heads=32)
+            torch.cuda.synchronize()
+        assert G.last_launch_count() == 1
+        assert G.device_status(ws, clear=True) == 2      # GQA_DEV_WAIT_TIMEOUT
+        assert int(counters.abs().sum()) == 0, f"grid counters left {counters.tolist()}"
+        H.check_canaries(c)
+        d["cache_k"].copy_(d["cache_k0"])
+        d["cache_v"].copy_(d["cache_v0"])
+        out = G.decode(d["x"], sp, 1000, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"],
+                       d["cache_v"], workspace=ws, n_kv_heads=32)
+        torch.cuda.synchronize()
+        assert G.device_status(ws) == 0
+    finally:
+        G.set_decode_fusion(prev)
+    for b in range(3):
+        H.compare_sequence(c, out, b)
+    H.check_canaries(c)
+
+
 def test_wait_limit_setting_round_trips():
     prev = G.set_wait_limit_ns(5_000_000)
     try:
@@ -568,21 +604,31 @@ def mha_weights():
     return I.draw_weights(I.LLAMA31_8B_MHA, seed=3)
 
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("B,starts,s_max", [
-    (1, [15], 16),                                    # few tokens: stream-K projections, one sequence
+    (1, [15], 16),                                    # one sequence, one unit
     (4, [0, 17, 128, 300], 320),                      # ragged positions, split sequences
+    (9, [int(v) for v in np.random.default_rng(9).integers(0, 700, 9)], 704),  # 16 padded tokens, 36 head groups
     (80, [int(v) for v in np.random.default_rng(5).integers(0, 90, 80)], 96),  # tcgen05 GEMM projections
 ])
-def test_mha_decode_matches_oracle(mha_weights, B, starts, s_max):
+def test_mha_decode_matches_oracle(mha_weights, B, starts, s_max, fused):
     """32 KV heads (query head h with KV head h): the decode path over head
-    groups, against the oracle with n_kv_heads = 32."""
+    groups, against the oracle with n_kv_heads = 32. Up to 16 sequences the
+    step runs as one grid (Q|K|V in three passes over Wq, Wk, Wv) or as
+    three kernels; above, as three kernels either way."""
     c = H.make_case(B, 1, starts, s_max, seed=3, weights=mha_weights, dims=I.LLAMA31_8B_MHA)
     d = c.dev
     sp = torch.tensor(starts, dtype=torch.int32, device="cuda")
     ws = G.make_workspace(B, 1, max(starts) + 1)
-    out = G.decode(d["x"], sp, max(starts), d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"],
-                   d["cache_v"], workspace=ws, n_kv_heads=32)
-    torch.cuda.synchronize()
+    prev = G.set_decode_fusion(fused)
+    try:
+        out = G.decode(d["x"], sp, max(starts), d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"],
+                       d["cache_v"], workspace=ws, n_kv_heads=32)
+        torch.cuda.synchronize()
+        launches = G.last_launch_count()
+    finally:
+        G.set_decode_fusion(prev)
+    assert launches == (1 if fused and B <= 16 else 3), launches
     assert G.device_status(ws) == 0
     for b in range(0, B, max(1, B // 6)):
         H.compare_sequence(c, out, b)
@@ -636,8 +682,9 @@ def test_mha_with_duplicated_kv_heads_equals_gqa(weights):
     assert r2 <= 5e-3, r2
     for b in range(B):
         for cm, cg in ((ck4, d["cache_k"]), (cv4, d["cache_v"])):
-            # each of the four copies of a KV head (summed in different k
-            # splits of the stream-K projection) within an ulp of the grouped row
+            # each of the four copies of a KV head (rows of different CTAs of
+            # the Wk / Wv pass, whose sums over k start at different stages)
+            # within an ulp of the grouped row
             new = cm[b, starts[b]].view(8, 4, 128)
             for r in range(4):
                 H.check_rows_within_one_ulp(new[:, r], H.f64(cg[b, starts[b]]), f"new row {r} of sequence {b}")
