@@ -229,6 +229,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      // every token tile is read by the CTAs of its group at about the same
+      // time and never again; every weight tile by each token tile in turn:
+      // L2 keeps the weights before the token rows
+      const uint64_t pol_x = l2_evict_first(), pol_w = l2_evict_last();
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < tiles; t += G) {
@@ -249,8 +253,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t fb = smem_u32(&bs.full[s]);
           const uint32_t sa = sbase + s * STAGE_BYTES;
           mbar_expect_tx(fb, STAGE_BYTES);
-          tma_load_2d(sa, &map_a, fb, kb * BK, m0);
-          tma_load_2d(sa + A_BYTES, mb, fb, kb * BK, brow);
+          tma_load_2d_hint(sa, &map_a, fb, kb * BK, m0, pol_x);
+          tma_load_2d_hint(sa + A_BYTES, mb, fb, kb * BK, brow, pol_w);
         }
       }
       if (!ok) atomicExch(&bs.abort, 1);
