@@ -228,12 +228,14 @@ __device__ __forceinline__ int ld_acquire_cta(const int* flag) {
   return v;
 }
 // Wait until a shared-memory flag is non-zero; returns it (0 after WAIT_LIMIT_NS).
+// The clock is read every 64 polls: read on every poll it slowed the loop
+// enough to add ~0.1 us to the hand-off it serves.
 __device__ __forceinline__ int wait_flag_cta(const int* flag) {
   int v = ld_acquire_cta(flag);
   if (v) return v;
   const unsigned long long t0 = global_ns();
-  while (!(v = ld_acquire_cta(flag))) {
-    if (global_ns() - t0 > WAIT_LIMIT_NS) return 0;
+  for (int k = 1; !(v = ld_acquire_cta(flag)); ++k) {
+    if ((k & 63) == 0 && global_ns() - t0 > WAIT_LIMIT_NS) return 0;
   }
   return v;
 }
