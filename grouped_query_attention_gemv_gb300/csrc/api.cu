@@ -395,6 +395,7 @@ int run_attention(const Call& c) {
     a.sp = c.sp;
     a.o = reinterpret_cast<__nv_bfloat16*>(c.ws + c.L.o);
     a.status = reinterpret_cast<int*>(c.ws + c.L.status);
+    a.num_sms = sm_count();
     e = launch_attn_prefill(maps, a, c.stream);
   }
   if (e != cudaSuccess) return fail_cuda(e);

@@ -4,14 +4,23 @@
 // Transformer.forward is -inf above the diagonal, left-padded with start_pos
 // visible columns; softmax in fp32; output heads merged h*128 + d).
 //
-// One CTA owns 64 query positions of one sequence and the 4 query heads of
+// A work item is 64 query positions of one sequence and the 4 query heads of
 // one KV group, as two 128-row Q tiles (32 positions x 4 heads each; row
 // r = position r/4, head r%4), so every 64-key K/V tile is staged once for
 // 8 x 32 query rows. In the multi-head variant (32 KV heads, one query head
-// each) a Q tile is 128 positions of one head and a CTA owns 256 positions:
+// each) a Q tile is 128 positions of one head and an item 256 positions:
 // the kernel is templated on the query heads per KV head, NREP.
-//   warp 8 (one lane)  TMA producer: both Q tiles once, then K_j / V_j
-//                      (128B swizzle, 4-stage rings on mbarriers)
+// The grid is persistent: one CTA per SM (its shared memory and TMEM admit
+// no second) walks a fixed list of items, longest key range first, so that
+// the next item's Q tiles, K/V tiles and first score products overlap the
+// current item's last P.V products and epilogue. One CTA per item measured
+// ~4 us of set-up, first loads and epilogue per item with nothing else on
+// the SM, a third of the kernel at 4 x 2048 tokens.
+//   warp 8 (one lane)  TMA producer: per item K_0..K_3 (after the first item:
+//                      their slots free up during the previous one), both Q
+//                      tiles once the previous item's last score products
+//                      are done, then V_j / K_j (128B swizzle, 4-stage rings
+//                      on mbarriers shared by all items)
 //   warps 9, 10        MMA issuers, one lane each, one per Q tile t: for key
 //                      tile j, S_{t,j} = Q_t K_j^T (M=128, N=64) into TMEM
 //                      slot j%2 of the tile, then O_t += P_{t,j-1} V_{j-1}
@@ -23,13 +32,17 @@
 //                      loads S from TMEM, masks keys past the row's position,
 //                      keeps a running max / sum in fp32, writes
 //                      P = 2^(S*scale - max) as bf16 over S, and at the end
-//                      reads O, divides by the sum and stores bf16.
+//                      of the item reads O, divides by the sum, stores bf16
+//                      and frees O for the next item's products.
 // TMEM (512 columns): Q tile t owns [256t, 256t+256): S slots at +0 and +64,
 // O at +128. While one warpgroup works on its scores the tensor core runs
 // the other tile's products and the next key tile's scores. The K/V rings
-// hold 4 tiles each: a 16 KB K tile takes ~1.4 us from request to arrival
-// under load, and two stages made that latency the period of the whole
-// kernel.
+// hold 4 tiles each. Cycle stamps of one CTA in steady state: a key tile
+// every ~1500 cycles, with the issuers' loop (S_j, then O_{j-1} once P_{j-1}
+// is stored) and the softmax chain (~800 cycles from S to P) in step; a K
+// tile lands ~4700 cycles after its copy is issued with 128 KB of tiles in
+// flight per SM. A fifth stage made that ~6200 cycles and left the period
+// as it was; two stages made the copy latency the period.
 // O is rescaled only when a row's running max grows by more than 2^8 over the
 // max its P values were taken against (the result is the same: every P and
 // the sum use that reference).
@@ -71,44 +84,86 @@ struct Bars {
   uint64_t o_done[NQ], mma_done[NQ];
   uint32_t tmem_slot;
   int abort;
-  int k_issued, v_issued;
+  int q_issued, k_issued, v_issued;
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ bool aborted(const Bars& bs) { return *reinterpret_cast<const volatile int*>(&bs.abort) != 0; }
 
+// One work item: 2 Q tiles (NQ x QP query positions) of one KV head g of
+// sequence b, and the key tiles they see.
+struct Item {
+  int g, b, q0, start, n;  // n: key tiles of the item (the longer of its Q tiles)
+  int nt[NQ];              // key tiles of each Q tile (0: the tile is past T)
+  bool valid;              // start position in range
+  bool report;             // the item that reports an invalid start of sequence b
+};
+
+// Items are numbered longest key range first: item idx is KV head idx % NKV of
+// sequence (idx / NKV) % B, pair npairs - 1 - idx / (NKV * B).
+template <int NREP>
+__device__ __forceinline__ Item item_at(int idx, const PrefillAttnParams& a) {
+  constexpr int QP = ROWS / NREP, NKV = N_HEADS / NREP;
+  const int npairs = ((a.T + QP - 1) / QP + NQ - 1) / NQ;
+  Item it;
+  it.g = idx % NKV;
+  const int rest = idx / NKV;
+  it.b = rest % a.B;
+  const int pair = npairs - 1 - rest / a.B;
+  it.start = a.sp.get(it.b);
+  it.valid = a.sp.ok(it.start);
+  it.report = pair == npairs - 1 && it.g == 0;
+  it.q0 = pair * NQ * QP;
+  it.n = 0;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    const int qt = it.q0 + t * QP;
+    it.nt[t] = it.valid && qt < a.T ? (it.start + min(qt + QP, a.T) + KT - 1) / KT : 0;
+    it.n = max(it.n, it.nt[t]);
+  }
+  return it;
+}
+
+// The items of this CTA in order: round k takes item k * G + c on even rounds
+// and k * G + G - 1 - c on odd ones (G CTAs, c = blockIdx.x), so that the CTA
+// with the longest item of one round gets the shortest of the next. Every
+// role of the CTA walks the same sequence; items with an invalid start are
+// skipped by all of them.
+template <int NREP>
+struct ItemWalk {
+  int k, nitems;
+  __device__ __forceinline__ explicit ItemWalk(const PrefillAttnParams& a) : k(0) {
+    constexpr int QP = ROWS / NREP, NKV = N_HEADS / NREP;
+    nitems = ((a.T + QP - 1) / QP + NQ - 1) / NQ * NKV * a.B;
+  }
+  // the next valid item, or false at the end of the list
+  __device__ __forceinline__ bool next(const PrefillAttnParams& a, Item& it) {
+    const int G = gridDim.x, c = blockIdx.x;
+    for (; k * G < nitems; ++k) {
+      const int idx = k * G + ((k & 1) ? G - 1 - c : c);
+      if (idx >= nitems) continue;
+      it = item_at<NREP>(idx, a);
+      if (!it.valid) {
+        if (it.report && threadIdx.x == 0) report(a.status, DEV_BAD_POSITION);
+        continue;
+      }
+      ++k;
+      return true;
+    }
+    return false;
+  }
+};
+
 template <int NREP>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                         const __grid_constant__ CUtensorMap mv, PrefillAttnParams a) {
   constexpr int QP = ROWS / NREP;         // query positions per Q tile
-  constexpr int NKV = N_HEADS / NREP;     // KV heads
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars& bs = *reinterpret_cast<Bars*>(smem + BAR_OFF);
-
-  // longest key ranges first: the pair of query tiles falls with blockIdx.x
-  const int nqt = (a.T + QP - 1) / QP;
-  const int npairs = (nqt + NQ - 1) / NQ;
-  const int g = blockIdx.x % NKV;
-  const int rest = blockIdx.x / NKV;
-  const int b = rest % a.B;
-  const int pair = npairs - 1 - rest / a.B;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int start = a.sp.get(b);
-  if (!a.sp.ok(start)) {
-    if (pair == npairs - 1 && g == 0 && threadIdx.x == 0) report(a.status, DEV_BAD_POSITION);
-    return;
-  }
-  const int q0 = pair * NQ * QP;  // first position (index t) of Q tile 0
-  int nt[NQ];                     // key tiles of each Q tile (0: the tile is past T)
-#pragma unroll
-  for (int t = 0; t < NQ; ++t) {
-    const int qt = q0 + t * QP;
-    nt[t] = qt < a.T ? (start + min(qt + QP, a.T) + KT - 1) / KT : 0;
-  }
-  const int n = nt[NQ - 1] > nt[0] ? nt[NQ - 1] : nt[0];
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bs.q_full), 1);
@@ -127,6 +182,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&bs.mma_done[t]), 1);
     }
     bs.abort = 0;
+    bs.q_issued = 0;
     bs.k_issued = 0;
     bs.v_issued = 0;
     fence_barrier_init();
@@ -146,40 +202,74 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&mq);
       tma_prefetch_desc(&mk);
       tma_prefetch_desc(&mv);
-      const uint32_t qb = smem_u32(&bs.q_full);
-      mbar_expect_tx(qb, NQ * Q_TILE);
-      // a tile past T reads as zeros (its rows are never stored)
-      for (int t = 0; t < NQ; ++t) {
-        tma_load_4d(sbase + t * Q_TILE, &mq, qb, 0, g * NREP, q0 + t * QP, b);
-        tma_load_4d(sbase + t * Q_TILE + Q_HALF, &mq, qb, 64, g * NREP, q0 + t * QP, b);
-      }
-      int kn = 0, vn = 0;
-      bool ok = true;
-      for (int j = 0; j <= n && ok; ++j) {
-        if (j < n) {
-          const int s = j % STAGES;
-          if (j >= STAGES) ok = mbar_wait(smem_u32(&bs.k_empty[s]), ((j / STAGES) - 1) & 1);
-          if (!ok || aborted(bs)) break;
-          const uint32_t fb = smem_u32(&bs.k_full[s]);
-          const uint32_t dst = sbase + K_OFF + s * KV_TILE;
-          mbar_expect_tx(fb, KV_TILE);
-          tma_load_4d(dst, &mk, fb, 0, g, j * KT, b);
-          tma_load_4d(dst + KV_HALF, &mk, fb, 64, g, j * KT, b);
-          kn = j + 1;
+      // K_j / V_j of every item through one pair of rings: u counts tiles over
+      // the CTA's items, stage u % STAGES
+      int u0 = 0, kn = 0, vn = 0, qn = 0;
+      int cs[NQ] = {};  // score tiles of each Q tile so far (as its issuer counts them)
+      bool ok = true, stop = false;
+      ItemWalk<NREP> walk(a);
+      Item it;
+      // copy of K_j (ring index u0 + j) / V_j; false when a wait gave up or
+      // the kernel is aborting
+      auto load_k = [&](const Item& it, int j) -> bool {
+        const int u = u0 + j, s = u % STAGES;
+        if (u >= STAGES) ok = mbar_wait(smem_u32(&bs.k_empty[s]), ((u / STAGES) - 1) & 1);
+        if (!ok || aborted(bs)) return false;
+        const uint32_t fb = smem_u32(&bs.k_full[s]);
+        const uint32_t dst = sbase + K_OFF + s * KV_TILE;
+        mbar_expect_tx(fb, KV_TILE);
+        tma_load_4d(dst, &mk, fb, 0, it.g, j * KT, it.b);
+        tma_load_4d(dst + KV_HALF, &mk, fb, 64, it.g, j * KT, it.b);
+        kn = u + 1;
+        return true;
+      };
+      auto load_v = [&](const Item& it, int j) -> bool {
+        const int u = u0 + j, s = u % STAGES;
+        if (u >= STAGES) ok = mbar_wait(smem_u32(&bs.v_empty[s]), ((u / STAGES) - 1) & 1);
+        if (!ok || aborted(bs)) return false;
+        const uint32_t fb = smem_u32(&bs.v_full[s]);
+        const uint32_t dst = sbase + V_OFF + s * KV_TILE;
+        mbar_expect_tx(fb, KV_TILE);
+        tma_load_4d(dst, &mv, fb, 0, it.g, j * KT, it.b);
+        tma_load_4d(dst + KV_HALF, &mv, fb, 64, it.g, j * KT, it.b);
+        vn = u + 1;
+        return true;
+      };
+      for (int ii = 0; !stop && walk.next(a, it); ++ii) {
+        // after the first item, the item's first K tiles go out before its
+        // Q tiles: their ring slots free up while the previous item's last
+        // score products run, the Q tiles only after those have completed
+        const int la = ii > 0 ? min(STAGES, it.n) : 0;
+        for (int j = 0; j < la && !stop; ++j) stop = !load_k(it, j);
+        if (stop) break;
+        // Q tile t is free once the last score product of the previous item
+        // that read it has completed (its s_full phase; the next product on
+        // that slot needs the new Q, so the phase cannot have moved on)
+#pragma unroll
+        for (int t = 0; t < NQ; ++t)
+          if (ok && cs[t] > 0) ok = mbar_wait(smem_u32(&bs.s_full[t][(cs[t] - 1) & 1]), ((cs[t] - 1) >> 1) & 1);
+        if (!ok || aborted(bs)) break;
+        const uint32_t qb = smem_u32(&bs.q_full);
+        mbar_expect_tx(qb, NQ * Q_TILE);
+        // a tile past T reads as zeros (its rows are never stored)
+        for (int t = 0; t < NQ; ++t) {
+          tma_load_4d(sbase + t * Q_TILE, &mq, qb, 0, it.g * NREP, it.q0 + t * QP, it.b);
+          tma_load_4d(sbase + t * Q_TILE + Q_HALF, &mq, qb, 64, it.g * NREP, it.q0 + t * QP, it.b);
         }
-        if (j >= 1) {
-          const int i = j - 1, s = i % STAGES;
-          if (i >= STAGES) ok = mbar_wait(smem_u32(&bs.v_empty[s]), ((i / STAGES) - 1) & 1);
-          if (!ok || aborted(bs)) break;
-          const uint32_t fb = smem_u32(&bs.v_full[s]);
-          const uint32_t dst = sbase + V_OFF + s * KV_TILE;
-          mbar_expect_tx(fb, KV_TILE);
-          tma_load_4d(dst, &mv, fb, 0, g, i * KT, b);
-          tma_load_4d(dst + KV_HALF, &mv, fb, 64, g, i * KT, b);
-          vn = i + 1;
+        qn = ii + 1;
+        // then V_j behind K_{j+1}, as the issuers consume them
+        for (int j = 0; j < la - 1 && !stop; ++j) stop = !load_v(it, j);
+        for (int j = la; j <= it.n && !stop; ++j) {
+          if (j < it.n) stop = !load_k(it, j);
+          if (!stop && j >= 1) stop = !load_v(it, j - 1);
         }
+        if (stop) break;
+        u0 += it.n;
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) cs[t] += it.nt[t];
       }
       if (!ok) atomicExch(&bs.abort, 1);
+      bs.q_issued = qn;
       bs.k_issued = kn;
       bs.v_issued = vn;
     }
@@ -187,59 +277,76 @@ __global__ void __launch_bounds__(THREADS, 1)
     // issuer of Q tile t (the whole warp runs the loop; one elected lane
     // issues): waits on every K/V stage so that its arrivals on the empty
     // barriers stay in step with the other issuer's; a stage past this
-    // tile's causal range gets a plain arrival
+    // tile's causal range gets a plain arrival. cs counts this tile's score
+    // tiles over the items (S slot cs % 2, one O product group each).
     const int t = warp - MMA_WARP;
-    const int n_t = t ? nt[1] : nt[0];
     const uint32_t idesc_s = umma_idesc_bf16(ROWS, KT);
     const uint32_t idesc_o = umma_idesc_bf16(ROWS, HEAD_DIM) | (1u << 16);  // B (V) MN-major
     const uint32_t qt = sbase + t * Q_TILE;
     const uint32_t base = tmem + t * TILE_COLS;
-    bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.q_full), 0));
-    for (int j = 0; ok && j <= n; ++j) {
-      if (j < n) {
-        const int s = j % STAGES;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.k_full[s]), (j / STAGES) & 1));
-        if (!ok) break;
-        if (j < n_t) {
-          tc_fence_after();
-          const uint32_t kt = sbase + K_OFF + s * KV_TILE;
-          if (elect_one()) {
-#pragma unroll
-            for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
-              const uint32_t off = (ks & 3) * 32;
-              umma_bf16(base + (j & 1) * KT, umma_desc_sw128(qt + (ks >> 2) * Q_HALF + off),
-                        umma_desc_sw128(kt + (ks >> 2) * KV_HALF + off), idesc_s, ks > 0 ? 1u : 0u);
-            }
-            umma_commit(smem_u32(&bs.s_full[t][j & 1]));
-            umma_commit(smem_u32(&bs.k_empty[s]));
-          }
-        } else if (elect_one()) {
-          mbar_arrive(smem_u32(&bs.k_empty[s]));
-        }
-        __syncwarp();
-      }
-      if (j >= 1) {
-        const int i = j - 1, s = i % STAGES;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.v_full[s]), (i / STAGES) & 1));
-        if (!ok) break;
-        if (i < n_t) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.p_full[t][i & 1]), (i >> 1) & 1));
+    unsigned u0 = 0, cs = 0;
+    bool ok = true;
+    ItemWalk<NREP> walk(a);
+    Item it;
+    for (int ii = 0; ok && walk.next(a, it); ++ii) {
+      const int n_t = t ? it.nt[1] : it.nt[0];
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.q_full), ii & 1));
+      if (!ok) break;
+      for (int j = 0; ok && j <= it.n; ++j) {
+        if (j < it.n) {
+          const unsigned u = u0 + j, s = u % STAGES;
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.k_full[s]), (u / STAGES) & 1));
           if (!ok) break;
-          tc_fence_after();
-          const uint32_t vt = sbase + V_OFF + s * KV_TILE;
-          if (elect_one()) {
+          if (j < n_t) {
+            tc_fence_after();
+            const uint32_t kt = sbase + K_OFF + s * KV_TILE;
+            const unsigned slot = (cs + j) & 1u;
+            if (elect_one()) {
 #pragma unroll
-            for (int ks = 0; ks < KT / 16; ++ks)
-              umma_bf16_ts(base + O_COL, base + (i & 1) * KT + ks * 8,
-                           umma_desc_sw128_mn(vt + ks * 16 * 128, KV_HALF), idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
-            umma_commit(smem_u32(&bs.o_done[t]));
-            umma_commit(smem_u32(&bs.v_empty[s]));
+              for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
+                const uint32_t off = (ks & 3) * 32;
+                umma_bf16(base + slot * KT, umma_desc_sw128(qt + (ks >> 2) * Q_HALF + off),
+                          umma_desc_sw128(kt + (ks >> 2) * KV_HALF + off), idesc_s, ks > 0 ? 1u : 0u);
+              }
+              umma_commit(smem_u32(&bs.s_full[t][slot]));
+              umma_commit(smem_u32(&bs.k_empty[s]));
+            }
+          } else if (elect_one()) {
+            mbar_arrive(smem_u32(&bs.k_empty[s]));
           }
-        } else if (elect_one()) {
-          mbar_arrive(smem_u32(&bs.v_empty[s]));
+          __syncwarp();
         }
-        __syncwarp();
+        if (j >= 1) {
+          const int i = j - 1;
+          const unsigned u = u0 + i, s = u % STAGES;
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.v_full[s]), (u / STAGES) & 1));
+          if (!ok) break;
+          if (i < n_t) {
+            // P of the item's first key tile also tells that the softmax
+            // warps have read the previous item's O (their epilogue comes
+            // first), so that the first product may overwrite it
+            const unsigned c = cs + i;
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.p_full[t][c & 1]), (c >> 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t vt = sbase + V_OFF + s * KV_TILE;
+            if (elect_one()) {
+#pragma unroll
+              for (int ks = 0; ks < KT / 16; ++ks)
+                umma_bf16_ts(base + O_COL, base + (c & 1) * KT + ks * 8,
+                             umma_desc_sw128_mn(vt + ks * 16 * 128, KV_HALF), idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+              umma_commit(smem_u32(&bs.o_done[t]));
+              umma_commit(smem_u32(&bs.v_empty[s]));
+            }
+          } else if (elect_one()) {
+            mbar_arrive(smem_u32(&bs.v_empty[s]));
+          }
+          __syncwarp();
+        }
       }
+      if (!ok) break;
+      u0 += it.n;
+      cs += n_t;
     }
     if (!ok && lane == 0) atomicExch(&bs.abort, 1);
     if (elect_one()) umma_commit(smem_u32(&bs.mma_done[t]));
@@ -249,108 +356,117 @@ __global__ void __launch_bounds__(THREADS, 1)
     // softmax / epilogue: warpgroup t, thread r owns row r = TMEM lane r of Q tile t
     const int t = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
-    const int n_t = t ? nt[1] : nt[0];
-    const int pos = q0 + t * QP + r / NREP;  // query index within the sequence
     const int hh = r % NREP;
-    const int kv_end = start + min(q0 + t * QP + QP, a.T);
-    const int lim = min(start + pos, kv_end - 1);  // last key this row sees
     const uint32_t lane_addr = tmem + t * TILE_COLS + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    float m_ref = -INFINITY;  // max the current P values and O are taken against (raw score units)
-    float l = 0.f;
+    unsigned cs = 0;  // score tiles of this Q tile over the items (as the issuer counts them)
     bool ok = true;
-    for (int j = 0; j < n_t; ++j) {
-      const int s = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.s_full[t][s]), (j >> 1) & 1))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[KT];
-      tmem_ld32(lane_addr + s * KT, sr);
-      tmem_ld32(lane_addr + s * KT + 32, sr + 32);
-      tmem_ld_wait();
-      const int vis = lim - j * KT;  // columns 0..vis are visible to this row
-      if (vis < KT - 1) {
-#pragma unroll
-        for (int c = 0; c < KT; ++c)
-          if (c > vis) sr[c] = __float_as_uint(-INFINITY);
-      }
-      float mx = fmaxf(__uint_as_float(sr[0]), __uint_as_float(sr[1]));
-#pragma unroll
-      for (int c = 2; c < KT; c += 2) mx = max3(mx, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-      float alpha = 1.f;
-      const bool grow = mx > m_ref && (m_ref == -INFINITY || (mx - m_ref) * SCALE_LOG2 > RESCALE_LOG2);
-      if (grow) {
-        alpha = m_ref == -INFINITY ? 0.f : ex2_approx((m_ref - mx) * SCALE_LOG2);
-        m_ref = mx;
-      }
-      const float neg = m_ref == -INFINITY ? 0.f : -m_ref * SCALE_LOG2;
-      // exponent arguments and the row sum two columns per instruction
-      const float2 sc2 = make_float2(SCALE_LOG2, SCALE_LOG2), ng2 = make_float2(neg, neg);
-      float2 sum2 = make_float2(0.f, 0.f);
-      uint32_t pk[KT / 2];
-#pragma unroll
-      for (int c = 0; c < KT; c += 2) {
-        const float2 e = fma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, ng2);
-        const float2 p = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-        sum2 = add2(sum2, p);
-        pk[c >> 1] = pack_bf16(p.x, p.y);
-      }
-      const float sum = sum2.x + sum2.y;
-      l = l * alpha + sum;
-      if (j > 0) {
-        // O must hold P_{j-1} V_{j-1} before it is rescaled (and this keeps
-        // the o_done phases in step with j)
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.o_done[t]), (j - 1) & 1))) {
+    ItemWalk<NREP> walk(a);
+    Item it;
+    while (ok && walk.next(a, it)) {
+      const int n_t = t ? it.nt[1] : it.nt[0];
+      const int pos = it.q0 + t * QP + r / NREP;  // query index within the sequence
+      const int kv_end = it.start + min(it.q0 + t * QP + QP, a.T);
+      const int lim = min(it.start + pos, kv_end - 1);  // last key this row sees
+      float m_ref = -INFINITY;  // max the current P values and O are taken against (raw score units)
+      float l = 0.f;
+      for (int j = 0; j < n_t; ++j) {
+        const unsigned c = cs + j;
+        const unsigned s = c & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.s_full[t][s]), (c >> 1) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, grow)) {
-#pragma unroll 1
-          for (int c = 0; c < HEAD_DIM; c += 32) {
-            uint32_t o[32];
-            tmem_ld32(lane_addr + O_COL + c, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(lane_addr + O_COL + c, o);
-          }
-        }
-      }
-      tmem_st32(lane_addr + s * KT, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bs.p_full[t][s]));
-    }
-    if (ok && n_t > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.o_done[t]), (n_t - 1) & 1))) ok = false;
-    if (ok && n_t > 0) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = a.o + (static_cast<size_t>(b) * a.T + pos) * D_MODEL +
-                           static_cast<size_t>(g * NREP + hh) * HEAD_DIM;
-#pragma unroll 1
-      for (int c = 0; c < HEAD_DIM; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(lane_addr + O_COL + c, o);
+        uint32_t sr[KT];
+        tmem_ld32(lane_addr + s * KT, sr);
+        tmem_ld32(lane_addr + s * KT + 32, sr + 32);
         tmem_ld_wait();
-        if (pos < a.T) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+        const int vis = lim - j * KT;  // columns 0..vis are visible to this row
+        if (vis < KT - 1) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
-            d4[e] = w;
+          for (int cc = 0; cc < KT; ++cc)
+            if (cc > vis) sr[cc] = __float_as_uint(-INFINITY);
+        }
+        float mx = fmaxf(__uint_as_float(sr[0]), __uint_as_float(sr[1]));
+#pragma unroll
+        for (int cc = 2; cc < KT; cc += 2) mx = max3(mx, __uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1]));
+        float alpha = 1.f;
+        const bool grow = mx > m_ref && (m_ref == -INFINITY || (mx - m_ref) * SCALE_LOG2 > RESCALE_LOG2);
+        if (grow) {
+          alpha = m_ref == -INFINITY ? 0.f : ex2_approx((m_ref - mx) * SCALE_LOG2);
+          m_ref = mx;
+        }
+        const float neg = m_ref == -INFINITY ? 0.f : -m_ref * SCALE_LOG2;
+        // exponent arguments and the row sum two columns per instruction
+        const float2 sc2 = make_float2(SCALE_LOG2, SCALE_LOG2), ng2 = make_float2(neg, neg);
+        float2 sum2 = make_float2(0.f, 0.f);
+        uint32_t pk[KT / 2];
+#pragma unroll
+        for (int cc = 0; cc < KT; cc += 2) {
+          const float2 e = fma2(make_float2(__uint_as_float(sr[cc]), __uint_as_float(sr[cc + 1])), sc2, ng2);
+          const float2 p = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+          sum2 = add2(sum2, p);
+          pk[cc >> 1] = pack_bf16(p.x, p.y);
+        }
+        l = l * alpha + (sum2.x + sum2.y);
+        if (j > 0) {
+          // O must hold P_{j-1} V_{j-1} before it is rescaled (and this keeps
+          // the o_done phases in step with the score tiles)
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.o_done[t]), (c - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+            for (int cc = 0; cc < HEAD_DIM; cc += 32) {
+              uint32_t o[32];
+              tmem_ld32(lane_addr + O_COL + cc, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(lane_addr + O_COL + cc, o);
+            }
+          }
+        }
+        tmem_st32(lane_addr + s * KT, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bs.p_full[t][s]));
+      }
+      if (!ok) break;
+      if (n_t > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.o_done[t]), (cs + n_t - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* dst = a.o + (static_cast<size_t>(it.b) * a.T + pos) * D_MODEL +
+                             static_cast<size_t>(it.g * NREP + hh) * HEAD_DIM;
+#pragma unroll 1
+        for (int cc = 0; cc < HEAD_DIM; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + O_COL + cc, o);
+          tmem_ld_wait();
+          if (pos < a.T) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+              w.y = pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+              w.z = pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+              w.w = pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+              d4[e] = w;
+            }
           }
         }
       }
-    } else if (!ok && lane == 0) {
-      atomicExch(&bs.abort, 1);
+      cs += n_t;
     }
+    if (!ok && lane == 0) atomicExch(&bs.abort, 1);
   }
 
   tc_fence_before();
@@ -358,8 +474,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (aborted(bs)) {
     if (threadIdx.x == 0) report(a.status, DEV_WAIT_TIMEOUT);
     if (warp == PRODUCER_WARP && lane == 0) {
-      // the last copy into each stage may still be in flight
-      mbar_wait(smem_u32(&bs.q_full), 0);
+      // the last copy into each buffer may still be in flight
+      if (bs.q_issued > 0) mbar_wait(smem_u32(&bs.q_full), (bs.q_issued - 1) & 1);
       for (int u = max(0, bs.k_issued - STAGES); u < bs.k_issued; ++u)
         mbar_wait(smem_u32(&bs.k_full[u % STAGES]), (u / STAGES) & 1);
       for (int u = max(0, bs.v_issued - STAGES); u < bs.v_issued; ++u)
@@ -387,10 +503,12 @@ cudaError_t launch_nrep(const PrefillMaps& maps, const PrefillAttnParams& a, cud
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  if (a.B <= 0 || a.T <= 0) return cudaErrorInvalidValue;
-  const long long ctas = static_cast<long long>(((a.T + QP - 1) / QP + NQ - 1) / NQ) * NKV * a.B;
-  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(ctas), THREADS, SMEM_BYTES, s>>>(maps.q, maps.k, maps.v, a);
+  if (a.B <= 0 || a.T <= 0 || a.num_sms <= 0) return cudaErrorInvalidValue;
+  // one CTA per SM (shared memory and TMEM admit no second), each walking its items
+  const long long items = static_cast<long long>(((a.T + QP - 1) / QP + NQ - 1) / NQ) * NKV * a.B;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const unsigned ctas = static_cast<unsigned>(items < a.num_sms ? items : a.num_sms);
+  kern<<<ctas, THREADS, SMEM_BYTES, s>>>(maps.q, maps.k, maps.v, a);
   return cudaGetLastError();
 }
 

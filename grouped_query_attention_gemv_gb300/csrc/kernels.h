@@ -179,6 +179,7 @@ struct PrefillAttnParams {
   StartPos sp;             // common start position (chunked prefill when > 0)
   __nv_bfloat16* o;        // [B*T][4096]
   int* status;
+  int num_sms;             // CTAs of the persistent grid at most
 };
 // Tensor maps of the prefill attention: q over (dim, head, token, sequence)
 // with boxes of 64 dims x n_rep heads x 128 / n_rep tokens; k / v over (dim, KV head,
