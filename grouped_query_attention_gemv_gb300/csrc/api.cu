@@ -455,18 +455,24 @@ int run_decode_fused(const Call& c) {
   const int qkv_rows[3] = {D_MODEL, KV_ROW, KV_ROW};
   const int o_rows[1] = {D_MODEL};
   a.qkv_passes = mha ? 3 : 1;
+  a.head_major = mha                 ? 0
+                 : t_attn_split == 2 ? (c.B * N_KV <= a.ctas)
+                 : t_attn_split == 1 ? 0
+                                     : head_major_pays(c.B, c.max_keys, a.ctas);
+  // One sequence with head-major attention: its 8 attention CTAs finish
+  // phase B last and would only then request their W_O stages (their ring
+  // held the attention's), so W_O's rows go to the other CTAs, whose stages
+  // are in shared memory before the W_O gate opens.
+  const int o_cta0 = a.head_major && c.B == 1 ? N_KV : 0;
   if (!(mha ? make_row_plan(1, o_rows, a.ctas, &a.qkv_plan) : make_row_plan(3, qkv_rows, a.ctas, &a.qkv_plan)) ||
-      !make_row_plan(1, o_rows, a.ctas, &a.o_plan))
+      !make_row_plan(1, o_rows, a.ctas - o_cta0, &a.o_plan))
     return GQA_EINVAL;
+  a.o_plan.cta0 = o_cta0;
   a.pq = proj_params(c, true, /*fold_norm=*/true);
   a.po = proj_params(c, false);
   const gqa_bf16* wqkv[3] = {c.wq, c.wk, c.wv};
   const gqa_bf16* wo[1] = {c.wo};
   const int np = decode_fused_np(a.pq.M);
-  a.head_major = mha                 ? 0
-                 : t_attn_split == 2 ? (c.B * N_KV <= a.ctas)
-                 : t_attn_split == 1 ? 0
-                                     : head_major_pays(c.B, c.max_keys, a.ctas);
   if (!(mha ? row_maps_passes(wqkv, a.qkv_plan, a.pq.x, a.pq.M, np, &a.qkv_maps)
             : row_maps(wqkv, a.qkv_plan, a.pq.x, a.pq.M, np, &a.qkv_maps)) ||
       !row_maps(wo, a.o_plan, a.po.x, a.po.M, np, &a.o_maps) ||

@@ -104,6 +104,10 @@ template <int NP>
 using CfgA = rowsk::Cfg<NP>;
 template <int NP>
 using CfgC = rowsk::Cfg<NP, NP <= 16 ? 4 : (NP == 32 ? 4 : 3), NP <= 16 ? 3 : 0>;
+// One sequence (one token): its attention output row is loaded once after
+// the gate and the W_O ring keeps the four token stages' 24 KB, 7 of a CTA's
+// 8 weight stages instead of 6, all requested before the gate.
+using CfgC1 = rowsk::Cfg<8, 1, 3, true>;
 
 template <int NP>
 struct Layout {
@@ -290,29 +294,41 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
   // meanwhile the compute warps meet the grid and merge the attention
   // outputs of split sequences; its token loads wait for every CTA's outputs.
   const rowsk::Shared shc{smem, c_bars, c_bars + MS, c_bars + 2 * MS, c_bars + 2 * MS + XS, flags_c, nullptr};
+  // one sequence, and W_O rows of at most two row tiles per CTA
+  const bool one_token_c = NP == 8 && fp.po.M == 1 && fp.o_plan.h_lo[0] + 2 <= 32;
   if (!aborted && flags_b[0]) {
     // this CTA's units gave up: it still meets the grid (no other CTA waits in vain)
     if (warp < attnk::COMPUTE_WARPS) {
       if (!fp.head_major) attnk::attn_merge<NREP>(fp.at, shb, &cnt[3], false);
       if (threadIdx.x == 0 && !early_signal) signal_counter(&cnt[1], 1);
     }
+  } else if (!aborted && static_cast<int>(blockIdx.x) < fp.o_plan.cta0) {
+    // no W_O rows here (a head-major attention CTA of a small batch: its
+    // outputs are published already, it has nothing to merge)
   } else if (!aborted) {
-    rowsk::rows_phase<CfgC<NP>, false>(m.o, fp.po, fp.o_plan, shc,
-                                       [cnt, grid, &fp]() {
-                                         const bool ok = wait_counter(&cnt[1], grid, fp.at.wait_ns);
-                                         fence_proxy_async_global();  // o was written by plain stores
-                                         return ok;
-                                       },
-                                       [&fp, &shb, cnt, units_ok, early_signal]() {
-                                         // head-major outputs need no merge (attn_items fenced them and
-                                         // they are published already)
-                                         if (early_signal) return units_ok;
-                                         const bool ok = attnk::attn_merge<NREP>(fp.at, shb, &cnt[3], units_ok);
-                                         // this CTA's attention outputs (whole sequences, merges) are fenced
-                                         if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
-                                         return ok;
-                                       },
-                                       [](auto) {}, []() {}, 0);
+    auto phase_c = [&](auto cfg) {
+      rowsk::rows_phase<decltype(cfg), false>(m.o, fp.po, fp.o_plan, shc,
+                                              [cnt, grid, &fp]() {
+                                                const bool ok = wait_counter(&cnt[1], grid, fp.at.wait_ns);
+                                                fence_proxy_async_global();  // o was written by plain stores
+                                                return ok;
+                                              },
+                                              [&fp, &shb, cnt, units_ok, early_signal]() {
+                                                // head-major outputs need no merge (attn_items fenced them
+                                                // and they are published already)
+                                                if (early_signal) return units_ok;
+                                                const bool ok = attnk::attn_merge<NREP>(fp.at, shb, &cnt[3], units_ok);
+                                                // this CTA's attention outputs (whole sequences, merges)
+                                                // are fenced
+                                                if (threadIdx.x == 0) signal_counter(&cnt[1], 1);
+                                                return ok;
+                                              },
+                                              [](auto) {}, []() {}, 0);
+    };
+    if (one_token_c)
+      phase_c(CfgC1{});
+    else
+      phase_c(CfgC<NP>{});
   }
   aborted = aborted || flags_b[0] != 0;
   __syncthreads();
@@ -321,7 +337,12 @@ __global__ void __launch_bounds__(THREADS, 1) decode_fused_kernel(const __grid_c
     if (flags_a[0]) rowsk::rows_drain<CfgA<NP>>(sha, fp.qkv_plan);
     // (phase A's producer may have requested head-major stages before phase A gave up)
     if (flags_a[0] || flags_b[0]) attnk::attn_drain(shb, fp.head_major ? attnk::ITEM_ROT : 0);
-    if (flags_c[0]) rowsk::rows_drain<CfgC<NP>>(shc, fp.o_plan);
+    if (flags_c[0]) {
+      if (one_token_c)
+        rowsk::rows_drain<CfgC1>(shc, fp.o_plan);
+      else
+        rowsk::rows_drain<CfgC<NP>>(shc, fp.o_plan);
+    }
   }
   if (threadIdx.x == 0) {
     // the last CTA out resets the grid counters for the next call (every
@@ -356,7 +377,9 @@ cudaError_t launch_fused_np(const DecodeFusedArgs& a, cudaStream_t s) {
   if (a.qkv_passes != (NREP == N_REP ? 1 : 3) || (NREP != N_REP && a.qkv_plan.nmat != 1)) return cudaErrorInvalidValue;
   int planned = 0;
   for (int i = 0; i < a.qkv_plan.nmat; ++i) planned += a.qkv_plan.ctas[i];
-  if (planned != a.ctas || a.o_plan.nmat != 1 || a.o_plan.ctas[0] != a.ctas) return cudaErrorInvalidValue;
+  if (planned != a.ctas || a.qkv_plan.cta0 != 0 || a.o_plan.nmat != 1 || a.o_plan.cta0 < 0 ||
+      a.o_plan.cta0 + a.o_plan.ctas[0] != a.ctas || (a.o_plan.cta0 > 0 && !a.head_major))
+    return cudaErrorInvalidValue;
   FusedMaps m;
   m.qkv = a.qkv_maps;
   m.o = a.o_maps;

@@ -199,6 +199,7 @@ struct RowPlan {
   int ctas[3];
   int h_lo[3];
   int mat0;  // RowMaps index of matrix 0 (0; a pass over one matrix of three sets it to that matrix)
+  int cta0;  // first CTA of the split: CTAs [0, cta0) own no rows (0 unless set after make_row_plan)
 };
 constexpr int ROWS_MAX_H = 48;   // rows one CTA can own (3 row tiles of 16)
 // k blocks of 64 per stage of the row-owner projections for np padded tokens

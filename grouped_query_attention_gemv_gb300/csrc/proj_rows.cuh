@@ -70,9 +70,15 @@ constexpr int XS_MAX = 16;               // token stages at most (all of a phase
 // in flight, so more only adds latency. Stages of 8 k blocks halve the
 // per-stage cost every warp pays (a barrier wait and an arrive for the
 // weights and for the tokens, ~0.25 us a stage).
-template <int NP_, int XS_ = 0, int INFL_ = 0>
+// ONE: a single token (M = 1): its whole row is the one token slot, loaded
+// once after the gate, and each warp builds the n8 tile's token fragments
+// from it in registers (lanes 0-3 hold the token's column, the others the
+// zero padding) instead of streaming 8-row token stages: the weight ring
+// keeps the rest of shared memory.
+template <int NP_, int XS_ = 0, int INFL_ = 0, bool ONE_ = false>
 struct Cfg {
   static constexpr int NP = NP_;
+  static constexpr bool ONE = ONE_;
   static constexpr int KC = rows_kc(NP_);
   static constexpr int NST = NKB / KC;              // stages per CTA
   static constexpr int INFL = INFL_ ? INFL_ : 4 * KBLK * 4 / (KC * KBLK);  // ~4 stages of 4 k blocks
@@ -87,6 +93,7 @@ struct Cfg {
   static constexpr int NT = TOKEN_SPLIT ? NP / 16 : NP / 8;  // n8 token tiles per warp
   static constexpr int RED_BYTES = WARPS * ROWS_MAX_H * NP * 4;  // per-warp partials, reuse the weight ring
   static_assert(RED_BYTES <= W_RING, "the reduction fits in the weight ring");
+  static_assert(!ONE || (NT == 1 && XS == 1 && X_STAGE == D_MODEL * 2), "one token row fills the one token slot");
 };
 
 // Weight stage: kc k blocks of the phase's largest row count, rounded up to
@@ -98,10 +105,12 @@ __device__ __forceinline__ int wstage_bytes(const RowPlan& plan, int kc) {
 }
 
 // This CTA's rows: matrix `mat`, rows [row0, row0 + h), map index hi (0: h_lo, 1: h_lo + 2).
+// CTA c >= plan.cta0 (the others own no rows and run no phase of the plan).
 struct MyRows {
   int mat, row0, h, hi;
 };
 __device__ __forceinline__ MyRows my_rows(const RowPlan& plan, int c) {
+  c -= plan.cta0;
   int mat = 0;
   while (mat + 1 < plan.nmat && c >= plan.ctas[mat]) c -= plan.ctas[mat++];
   const int pairs = plan.rows[mat] / 2, n = plan.ctas[mat];
@@ -231,7 +240,7 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
       const int l = NST - 1;
       w_issued([&]() {
         return mbar_wait_or_abort(smem_u32(&sh.empty[l % S]), (l / S) & 1, &flags[0]) &&
-               mbar_wait_or_abort(smem_u32(&sh.xempty[l % XS]), (l / XS) & 1, &flags[0]);
+               (C_::ONE || mbar_wait_or_abort(smem_u32(&sh.xempty[l % XS]), (l / XS) & 1, &flags[0]));
       });
     }
     return;
@@ -241,6 +250,19 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
     // ---------------- token producer: the token rows may come from an earlier
     // phase (gate() waits for them). Rows past M read as zero (the map's rows
     // end at M).
+    if constexpr (C_::ONE) {
+      // the token's row, once
+      const bool ok = gate();
+      if (ok) {
+        const uint32_t fb = smem_u32(&sh.xfull[0]);
+        mbar_expect_tx(fb, C_::X_STAGE);
+        bulk_load(smem_u32(xring), p.x, C_::X_STAGE, fb);
+      } else {
+        atomicExch(&flags[0], 1);
+      }
+      flags[3] = ok ? 1 : 0;
+      return;
+    }
     if (started == 0) tma_prefetch_desc(&maps.x);
     bool ok = gate();
     int i = started;
@@ -355,7 +377,75 @@ __device__ __forceinline__ void rows_phase(const RowMaps& maps, const ProjParams
   // division by it costs the consumer ~150 cycles a stage
   int s = 0, xs = 0;
   uint32_t ph = 0, xph = 0;
-  for (int i = 0; ok && i < NST; ++i) {
+  if constexpr (C_::ONE) {
+    // the token's row first
+    if (ok && !__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&sh.xfull[0]), 0, &flags[0]))) {
+      if (lane == 0) atomicExch(&flags[0], 1);
+      ok = false;
+    }
+    // One token, every stage but the last already in the ring: the stages
+    // are walked two deep, the fragments of stage i + 1 loaded while stage
+    // i's products issue (one stage at a time measured ~0.33 us a stage, the
+    // loads' and products' latencies in series). At most two row tiles
+    // (the grid checks rows <= 32 before it picks this path).
+    constexpr int NKS = KS / 2;
+    constexpr int MT1 = 2;
+    uint32_t af[2][NKS][2][MT1][4];
+    uint32_t bf[2][NKS][4];
+    auto load = [&](int i, int slot, uint32_t(&a)[NKS][2][MT1][4], uint32_t(&b)[NKS][4]) {
+      const uint32_t wa = smem_u32(sh.ring + slot * wstage);
+      const int rb = kb * mr.h;
+      // fragment q of lane l < 4: features 16 ks + 8 q + 2 l, +1 of the token's row
+      const uint32_t* xr = reinterpret_cast<const uint32_t*>(xring) + ((((i + rot) % NST) * KC + kb) * KBLK + 2 * lane) / 2;
+#pragma unroll
+      for (int j = 0; j < NKS; ++j) {
+        const int ks = ks0 + 2 * j;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) b[j][q] = lane < 4 ? xr[8 * ks + 4 * q] : 0u;
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+          for (int mt = 0; mt < MT1; ++mt)
+            if (mt < mtc) {
+              const int r = rb + mt * 16 + (lane & 15);
+              ldsm_x4(wa + sw128(r, 2 * (ks + kk) + (lane >> 4)), a[j][kk][mt][0], a[j][kk][mt][1], a[j][kk][mt][2],
+                      a[j][kk][mt][3]);
+            }
+      }
+    };
+    auto products = [&](const uint32_t(&a)[NKS][2][MT1][4], const uint32_t(&b)[NKS][4]) {
+#pragma unroll
+      for (int j = 0; j < NKS; ++j)
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+          for (int mt = 0; mt < MT1; ++mt)
+            if (mt < mtc) mma16816(acc[kk % KH][mt][0], a[j][kk][mt][0], a[j][kk][mt][1], a[j][kk][mt][2], a[j][kk][mt][3],
+                                   b[j][2 * kk], b[j][2 * kk + 1]);
+    };
+    // stage i: wait for its weights, load its fragments, release its slot
+    auto take = [&](int i, int slot, uint32_t phase, uint32_t(&a)[NKS][2][MT1][4], uint32_t(&b)[NKS][4]) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(smem_u32(&sh.full[slot]), phase, &flags[0]))) {
+        if (lane == 0) atomicExch(&flags[0], 1);
+        return false;
+      }
+      load(i, slot, a, b);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.empty[slot]));
+      return true;
+    };
+    if (ok) ok = take(0, 0, 0u, af[0], bf[0]);
+#pragma unroll
+    for (int i = 0; i < NST; ++i) {
+      if (!ok) break;
+      if (i + 1 < NST) {
+        if (++s == S) { s = 0; ph ^= 1u; }
+        ok = take(i + 1, s, ph, af[(i + 1) & 1], bf[(i + 1) & 1]);
+      }
+      products(af[i & 1], bf[i & 1]);
+    }
+  }
+  for (int i = 0; !C_::ONE && ok && i < NST; ++i) {
     uint32_t gcur[NG];
 #pragma unroll
     for (int j = 0; j < NG; ++j) gcur[j] = gnext[j];
