@@ -117,6 +117,7 @@ struct Layout {
   static constexpr int FIXED = RING + BARS * 8 + 16 * 4 + FUSED_MAX_B * 4 + 1024;  // ..., flags, norm scales
   // the attention's output staging lies past its ring, inside the projections' ring
   static_assert(attnk::RING + attnk::STAGE_OUT_BYTES <= RING, "attention staging fits");
+  static_assert(FIXED + (FUSED_MAX_B + 1) * 4 <= 227 * 1024, "shared memory of one CTA");
 };
 
 // NREP: query heads per KV head, 4 (8 KV heads) or 1 (the multi-head variant:

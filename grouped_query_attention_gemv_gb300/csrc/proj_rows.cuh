@@ -54,7 +54,7 @@ constexpr int NKB = D_MODEL / KBLK;      // 64 k blocks
 constexpr int MT_MAX = ROWS_MAX_H / 16;  // row tiles of 16
 constexpr int WARPS = 8;                 // compute warps 0-7; warp 8 lane 0 loads W, warp 9 lane 0 loads x
 constexpr int MAX_STAGES = 12;           // weight stages (barrier pairs)
-constexpr int RING_BYTES = 216 * 1024;   // weight ring + token ring
+constexpr int RING_BYTES = 224 * 1024;   // weight ring + token ring
 constexpr int OVERREAD = 1024;           // the last row tile may read up to 15 rows past a stage
 
 constexpr int XS_MAX = 16;               // token stages at most (all of a phase's tokens)
