@@ -16,11 +16,13 @@
 // current item's last P.V products and epilogue. One CTA per item measured
 // ~4 us of set-up, first loads and epilogue per item with nothing else on
 // the SM, a third of the kernel at 4 x 2048 tokens.
-//   warp 8 (one lane)  TMA producer: per item K_0..K_3 (after the first item:
-//                      their slots free up during the previous one), both Q
-//                      tiles once the previous item's last score products
-//                      are done, then V_j / K_j (128B swizzle, 4-stage rings
-//                      on mbarriers shared by all items)
+//   warp 8 (one lane)  TMA producer: per item its K/V stages (stage j: K_j
+//                      and V_{j-1}, the tiles the issuers' iteration j
+//                      reads, on one full and one empty barrier), after the
+//                      first item stages 0..3 first (their slots free up
+//                      during the previous item), both Q tiles once the
+//                      previous item's last score products are done (128B
+//                      swizzle, 4-stage rings shared by all items)
 //   warps 9, 10        MMA issuers, one lane each, one per Q tile t: for key
 //                      tile j, S_{t,j} = Q_t K_j^T (M=128, N=64) into TMEM
 //                      slot j%2 of the tile, then O_t += P_{t,j-1} V_{j-1}
@@ -79,12 +81,12 @@ constexpr float RESCALE_LOG2 = 8.f;
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[STAGES], k_empty[STAGES], v_full[STAGES], v_empty[STAGES];
+  uint64_t kv_full[STAGES], kv_empty[STAGES];  // stage j of an item: K_j and V_{j-1}
   uint64_t s_full[NQ][2], p_full[NQ][2];
   uint64_t o_done[NQ], mma_done[NQ];
   uint32_t tmem_slot;
   int abort;
-  int q_issued, k_issued, v_issued;
+  int q_issued, kv_issued;
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -168,10 +170,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bs.q_full), 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&bs.k_full[s]), 1);
-      mbar_init(smem_u32(&bs.k_empty[s]), NQ);  // one arrival per MMA issuer
-      mbar_init(smem_u32(&bs.v_full[s]), 1);
-      mbar_init(smem_u32(&bs.v_empty[s]), NQ);
+      mbar_init(smem_u32(&bs.kv_full[s]), 1);
+      mbar_init(smem_u32(&bs.kv_empty[s]), NQ);  // one arrival per MMA issuer
     }
     for (int t = 0; t < NQ; ++t) {
       for (int s = 0; s < 2; ++s) {
@@ -183,8 +183,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     bs.abort = 0;
     bs.q_issued = 0;
-    bs.k_issued = 0;
-    bs.v_issued = 0;
+    bs.kv_issued = 0;
     fence_barrier_init();
   }
   if (warp == MMA_WARP) {
@@ -202,45 +201,41 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&mq);
       tma_prefetch_desc(&mk);
       tma_prefetch_desc(&mv);
-      // K_j / V_j of every item through one pair of rings: u counts tiles over
-      // the CTA's items, stage u % STAGES
-      int u0 = 0, kn = 0, vn = 0, qn = 0;
+      // stage j of an item holds K_j (j < n) and V_{j-1} (j >= 1), the tiles
+      // its two issuers' iteration j reads: one full and one empty barrier a
+      // stage. u counts stages over the CTA's items, ring slot u % STAGES.
+      int u0 = 0, kvn = 0, qn = 0;
       int cs[NQ] = {};  // score tiles of each Q tile so far (as its issuer counts them)
       bool ok = true, stop = false;
       ItemWalk<NREP> walk(a);
       Item it;
-      // copy of K_j (ring index u0 + j) / V_j; false when a wait gave up or
-      // the kernel is aborting
-      auto load_k = [&](const Item& it, int j) -> bool {
+      // copies of stage j; false when a wait gave up or the kernel is aborting
+      auto load_stage = [&](const Item& it, int j) -> bool {
         const int u = u0 + j, s = u % STAGES;
-        if (u >= STAGES) ok = mbar_wait(smem_u32(&bs.k_empty[s]), ((u / STAGES) - 1) & 1);
+        if (u >= STAGES) ok = mbar_wait(smem_u32(&bs.kv_empty[s]), ((u / STAGES) - 1) & 1);
         if (!ok || aborted(bs)) return false;
-        const uint32_t fb = smem_u32(&bs.k_full[s]);
-        const uint32_t dst = sbase + K_OFF + s * KV_TILE;
-        mbar_expect_tx(fb, KV_TILE);
-        tma_load_4d(dst, &mk, fb, 0, it.g, j * KT, it.b);
-        tma_load_4d(dst + KV_HALF, &mk, fb, 64, it.g, j * KT, it.b);
-        kn = u + 1;
-        return true;
-      };
-      auto load_v = [&](const Item& it, int j) -> bool {
-        const int u = u0 + j, s = u % STAGES;
-        if (u >= STAGES) ok = mbar_wait(smem_u32(&bs.v_empty[s]), ((u / STAGES) - 1) & 1);
-        if (!ok || aborted(bs)) return false;
-        const uint32_t fb = smem_u32(&bs.v_full[s]);
-        const uint32_t dst = sbase + V_OFF + s * KV_TILE;
-        mbar_expect_tx(fb, KV_TILE);
-        tma_load_4d(dst, &mv, fb, 0, it.g, j * KT, it.b);
-        tma_load_4d(dst + KV_HALF, &mv, fb, 64, it.g, j * KT, it.b);
-        vn = u + 1;
+        const uint32_t fb = smem_u32(&bs.kv_full[s]);
+        mbar_expect_tx(fb, (j < it.n ? KV_TILE : 0) + (j >= 1 ? KV_TILE : 0));
+        if (j < it.n) {
+          const uint32_t dst = sbase + K_OFF + s * KV_TILE;
+          tma_load_4d(dst, &mk, fb, 0, it.g, j * KT, it.b);
+          tma_load_4d(dst + KV_HALF, &mk, fb, 64, it.g, j * KT, it.b);
+        }
+        if (j >= 1) {
+          const uint32_t dst = sbase + V_OFF + s * KV_TILE;
+          tma_load_4d(dst, &mv, fb, 0, it.g, (j - 1) * KT, it.b);
+          tma_load_4d(dst + KV_HALF, &mv, fb, 64, it.g, (j - 1) * KT, it.b);
+        }
+        kvn = u + 1;
         return true;
       };
       for (int ii = 0; !stop && walk.next(a, it); ++ii) {
-        // after the first item, the item's first K tiles go out before its
-        // Q tiles: their ring slots free up while the previous item's last
-        // score products run, the Q tiles only after those have completed
-        const int la = ii > 0 ? min(STAGES, it.n) : 0;
-        for (int j = 0; j < la && !stop; ++j) stop = !load_k(it, j);
+        // after the first item, the item's first stages go out before its Q
+        // tiles: their ring slots free up while the previous item's last
+        // products run, the Q tiles only after its last score products have
+        // completed
+        const int la = ii > 0 ? min(STAGES, it.n + 1) : 0;
+        for (int j = 0; j < la && !stop; ++j) stop = !load_stage(it, j);
         if (stop) break;
         // Q tile t is free once the last score product of the previous item
         // that read it has completed (its s_full phase; the next product on
@@ -257,21 +252,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_4d(sbase + t * Q_TILE + Q_HALF, &mq, qb, 64, it.g * NREP, it.q0 + t * QP, it.b);
         }
         qn = ii + 1;
-        // then V_j behind K_{j+1}, as the issuers consume them
-        for (int j = 0; j < la - 1 && !stop; ++j) stop = !load_v(it, j);
-        for (int j = la; j <= it.n && !stop; ++j) {
-          if (j < it.n) stop = !load_k(it, j);
-          if (!stop && j >= 1) stop = !load_v(it, j - 1);
-        }
+        for (int j = la; j <= it.n && !stop; ++j) stop = !load_stage(it, j);
         if (stop) break;
-        u0 += it.n;
+        u0 += it.n + 1;
 #pragma unroll
         for (int t = 0; t < NQ; ++t) cs[t] += it.nt[t];
       }
       if (!ok) atomicExch(&bs.abort, 1);
       bs.q_issued = qn;
-      bs.k_issued = kn;
-      bs.v_issued = vn;
+      bs.kv_issued = kvn;
     }
   } else if (warp >= MMA_WARP) {
     // issuer of Q tile t (the whole warp runs the loop; one elected lane
@@ -293,59 +282,58 @@ __global__ void __launch_bounds__(THREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.q_full), ii & 1));
       if (!ok) break;
       for (int j = 0; ok && j <= it.n; ++j) {
-        if (j < it.n) {
-          const unsigned u = u0 + j, s = u % STAGES;
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.k_full[s]), (u / STAGES) & 1));
-          if (!ok) break;
-          if (j < n_t) {
-            tc_fence_after();
-            const uint32_t kt = sbase + K_OFF + s * KV_TILE;
-            const unsigned slot = (cs + j) & 1u;
-            if (elect_one()) {
+        const unsigned u = u0 + j, s = u % STAGES;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.kv_full[s]), (u / STAGES) & 1));
+        if (!ok) break;
+        bool used = false;
+        if (j < n_t) {
+          tc_fence_after();
+          const uint32_t kt = sbase + K_OFF + s * KV_TILE;
+          const unsigned slot = (cs + j) & 1u;
+          if (elect_one()) {
 #pragma unroll
-              for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
-                const uint32_t off = (ks & 3) * 32;
-                umma_bf16(base + slot * KT, umma_desc_sw128(qt + (ks >> 2) * Q_HALF + off),
-                          umma_desc_sw128(kt + (ks >> 2) * KV_HALF + off), idesc_s, ks > 0 ? 1u : 0u);
-              }
-              umma_commit(smem_u32(&bs.s_full[t][slot]));
-              umma_commit(smem_u32(&bs.k_empty[s]));
+            for (int ks = 0; ks < HEAD_DIM / 16; ++ks) {
+              const uint32_t off = (ks & 3) * 32;
+              umma_bf16(base + slot * KT, umma_desc_sw128(qt + (ks >> 2) * Q_HALF + off),
+                        umma_desc_sw128(kt + (ks >> 2) * KV_HALF + off), idesc_s, ks > 0 ? 1u : 0u);
             }
-          } else if (elect_one()) {
-            mbar_arrive(smem_u32(&bs.k_empty[s]));
+            umma_commit(smem_u32(&bs.s_full[t][slot]));
           }
           __syncwarp();
+          used = true;
         }
-        if (j >= 1) {
+        if (j >= 1 && j - 1 < n_t) {
           const int i = j - 1;
-          const unsigned u = u0 + i, s = u % STAGES;
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.v_full[s]), (u / STAGES) & 1));
+          // P of the item's first key tile also tells that the softmax
+          // warps have read the previous item's O (their epilogue comes
+          // first), so that the first product may overwrite it
+          const unsigned c = cs + i;
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.p_full[t][c & 1]), (c >> 1) & 1));
           if (!ok) break;
-          if (i < n_t) {
-            // P of the item's first key tile also tells that the softmax
-            // warps have read the previous item's O (their epilogue comes
-            // first), so that the first product may overwrite it
-            const unsigned c = cs + i;
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bs.p_full[t][c & 1]), (c >> 1) & 1));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t vt = sbase + V_OFF + s * KV_TILE;
-            if (elect_one()) {
+          tc_fence_after();
+          const uint32_t vt = sbase + V_OFF + s * KV_TILE;
+          if (elect_one()) {
 #pragma unroll
-              for (int ks = 0; ks < KT / 16; ++ks)
-                umma_bf16_ts(base + O_COL, base + (c & 1) * KT + ks * 8,
-                             umma_desc_sw128_mn(vt + ks * 16 * 128, KV_HALF), idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
-              umma_commit(smem_u32(&bs.o_done[t]));
-              umma_commit(smem_u32(&bs.v_empty[s]));
-            }
-          } else if (elect_one()) {
-            mbar_arrive(smem_u32(&bs.v_empty[s]));
+            for (int ks = 0; ks < KT / 16; ++ks)
+              umma_bf16_ts(base + O_COL, base + (c & 1) * KT + ks * 8,
+                           umma_desc_sw128_mn(vt + ks * 16 * 128, KV_HALF), idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(smem_u32(&bs.o_done[t]));
           }
           __syncwarp();
+          used = true;
         }
+        // the stage is free once this issuer's products on it are done (a
+        // commit covers every product the thread issued before it)
+        if (elect_one()) {
+          if (used)
+            umma_commit(smem_u32(&bs.kv_empty[s]));
+          else
+            mbar_arrive(smem_u32(&bs.kv_empty[s]));
+        }
+        __syncwarp();
       }
       if (!ok) break;
-      u0 += it.n;
+      u0 += it.n + 1;
       cs += n_t;
     }
     if (!ok && lane == 0) atomicExch(&bs.abort, 1);
@@ -476,10 +464,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == PRODUCER_WARP && lane == 0) {
       // the last copy into each buffer may still be in flight
       if (bs.q_issued > 0) mbar_wait(smem_u32(&bs.q_full), (bs.q_issued - 1) & 1);
-      for (int u = max(0, bs.k_issued - STAGES); u < bs.k_issued; ++u)
-        mbar_wait(smem_u32(&bs.k_full[u % STAGES]), (u / STAGES) & 1);
-      for (int u = max(0, bs.v_issued - STAGES); u < bs.v_issued; ++u)
-        mbar_wait(smem_u32(&bs.v_full[u % STAGES]), (u / STAGES) & 1);
+      for (int u = max(0, bs.kv_issued - STAGES); u < bs.kv_issued; ++u)
+        mbar_wait(smem_u32(&bs.kv_full[u % STAGES]), (u / STAGES) & 1);
     }
     __syncthreads();
   }
