@@ -134,13 +134,14 @@ def test_decode_three_kernel_path_matches_oracle(weights, B, starts, s_max):
 
 
 @pytest.mark.parametrize("split", SPLITS)
-def test_decode_every_start_position_invalid_is_reported(weights, split):
+@pytest.mark.parametrize("B", [1, 2])   # B=1: the one-token W_O path, W_O rows on the CTAs past the attention's
+def test_decode_every_start_position_invalid_is_reported(weights, split, B):
     """No valid sequence: the fused grid must still finish (its last phase
     waits on no sequence) and leave every cache row untouched."""
-    c = H.make_case(2, 1, [3, 4], 16, weights=weights)
+    c = H.make_case(B, 1, [3, 4][:B], 16, weights=weights)
     d = c.dev
-    sp = torch.tensor([11, 12], dtype=torch.int32, device="cuda")   # both > max_start_pos 9
-    ws = G.make_workspace(2, 1, 10)
+    sp = torch.tensor([11, 12][:B], dtype=torch.int32, device="cuda")   # > max_start_pos 9
+    ws = G.make_workspace(B, 1, 10)
     with attention_split(split):
         G.decode(d["x"], sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"], d["cache_v"],
                  workspace=ws)
@@ -148,13 +149,13 @@ def test_decode_every_start_position_invalid_is_reported(weights, split):
     assert G.device_status(ws, clear=True) == 1
     assert torch.equal(d["cache_k"], d["cache_k0"]) and torch.equal(d["cache_v"], d["cache_v0"])
     # the workspace (its grid counters included) is ready for the next call
-    sp.copy_(torch.tensor([3, 4], dtype=torch.int32))
+    sp.copy_(torch.tensor([3, 4][:B], dtype=torch.int32))
     with attention_split(split):
         out = G.decode(d["x"], sp, 9, d["wq"], d["wk"], d["wv"], d["wo"], H.rope_for(c), d["cache_k"],
                        d["cache_v"], workspace=ws)
     torch.cuda.synchronize()
     assert G.device_status(ws) == 0
-    for b in range(2):
+    for b in range(B):
         H.compare_sequence(c, out, b)
 
 
@@ -200,6 +201,7 @@ def test_decode_workloads_full(weights, name, split):
 
 @pytest.mark.parametrize("B,starts,s_max", [
     (1, [0], 2),                                  # one key per head: o_h = v_{h//4}
+    (1, [1000], 1001),                            # one sequence over 8 stages (the one-token W_O path)
     (2, [127, 128], 130),                         # a stage of 128 keys whole, and one key past it
     (5, [126, 255, 256, 383, 1], 400),            # stage edges from both sides, ragged
     (19, [int(v) for v in np.random.default_rng(19).integers(0, 900, 19)], 900),  # every SM holds a pair
