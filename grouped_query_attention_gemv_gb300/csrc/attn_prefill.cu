@@ -38,13 +38,13 @@
 //                      and frees O for the next item's products.
 // TMEM (512 columns): Q tile t owns [256t, 256t+256): S slots at +0 and +64,
 // O at +128. While one warpgroup works on its scores the tensor core runs
-// the other tile's products and the next key tile's scores. The K/V rings
-// hold 4 tiles each. Cycle stamps of one CTA in steady state: a key tile
-// every ~1500 cycles, with the issuers' loop (S_j, then O_{j-1} once P_{j-1}
-// is stored) and the softmax chain (~800 cycles from S to P) in step; a K
-// tile lands ~4700 cycles after its copy is issued with 128 KB of tiles in
-// flight per SM. A fifth stage made that ~6200 cycles and left the period
-// as it was; two stages made the copy latency the period.
+// the other tile's products and the next key tile's scores. The K/V ring
+// holds 4 stages. Cycle stamps of one CTA in steady state: a key tile every
+// ~1450 cycles, set by each issuer's loop (a barrier wait, S_j, a wait on
+// P_{j-1}, O_{j-1}, commits) in step with the softmax chain (~800 cycles
+// from S to P); the copies land well ahead (these K tiles stream at ~70
+// bytes a cycle per SM), and a fifth stage left the period as it was; two
+// stages made the copy latency the period.
 // O is rescaled only when a row's running max grows by more than 2^8 over the
 // max its P values were taken against (the result is the same: every P and
 // the sum use that reference).
